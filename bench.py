@@ -1,0 +1,513 @@
+#!/usr/bin/env python3
+"""Benchmark of the drafter decode-step hot path on one GB300.
+
+One step = dflash_step_bookkeeping + dflash_ctx_kv_update + L x
+(dflash_block_kv_scatter + dflash_block_attention) on the Qwen3-8B-shaped
+drafter (D = 4096, L = 5, hq = 32, nkv = 8, hd = 128, T = 16, page 64) at
+B = 1 and a 32K context, on seeded synthetic inputs resident in HBM.  The KV
+stream alone (640 MiB/step) is larger than L2, so no explicit flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
+only comparison arm this method has) on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from context_kv_update_gb300 import inputs  # noqa: E402
+
+METRIC = "drafter step µs (ctx-KV update + block attn) at B=1, 32K ctx; attn HBM GB/s"
+UNIT = "us/step"
+WORKLOAD = "qwen3_8b"
+CTX = 32768
+
+# DRAM traffic per attention launch from the committed ncu capture, keyed by
+# the hash of the attention sources it was taken on (None = not captured).
+ATTN_TRAFFIC = {"sources_sha": None, "bytes_per_launch": None,
+                "profile": "profiles/attention_qwen3_8b_32k.md"}
+
+
+def attention_sources_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("attention.cu", "attention_tc.cu", "attention_common.cuh", "sm100_ptx.cuh"):
+        p = os.path.join(ROOT, "context_kv_update_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, r in rows for k in range(4) if r[k] == "Active"})
+        loaded = [s for s, mx, _ in rows if s > 0.5 * mx] or [s for s, _, _ in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx for _, mx, _ in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- our arm
+
+
+class Step:
+    """Device buffers + the launch sequence of one drafter step."""
+
+    def __init__(self, dl, prob, dev_status=True):
+        import torch
+        self.dl, self.prob = dl, prob
+        g = prob["g"]
+        self.g = g
+        self.geom = dl.make_geom(g)
+        B, T, L = prob["B"], g["T"], g["L"]
+        dev = "cuda"
+        td = self._td
+        self.raw_offsets = td(prob["raw_offsets"])
+        self.acc = td(prob["acc"])
+        self.n_acc = td(prob["n_acc"])
+        self.ctx_pre = td(prob["ctx_len"])
+        self.ctx_len = self.ctx_pre.clone()
+        self.hidden = td(prob["hidden"])
+        self.weights = {k: td(prob[k]) for k in ("w_fc", "g_h", "w_kv", "g_k")}
+        self.pool = td(prob["pool"])
+        self.q = td(prob["q"])
+        self.blk_k = td(prob["blk_k"])
+        self.blk_v = td(prob["blk_v"])
+        self.sinks = td(prob["sinks"]) if prob["use_sinks"] else None
+        M = g["max_pages"]
+        self.outs = {}
+        for k in dl.STEP_OUTPUT_FIELDS:
+            shape = (B, M) if k == "block_table" else (B, T) if k in (
+                "emb_ids", "ctx_pos", "q_pos", "ctx_dst_page", "ctx_dst_slot", "ctx_wmask",
+                "blk_page", "blk_slot", "blk_mask") else (B,)
+            dt = torch.uint8 if k in ("ctx_wmask", "blk_mask") else torch.int32
+            self.outs[k] = torch.zeros(shape, dtype=dt, device=dev)
+        self.ctx_ws = torch.empty(dl.dflash_ctx_workspace_bytes(self.geom, B), dtype=torch.uint8,
+                                  device=dev)
+        self.attn_ws = torch.empty(dl.dflash_attention_workspace_bytes(self.geom, B, T, 0),
+                                   dtype=torch.uint8, device=dev)
+        self.attn_out = torch.empty((L, B, T, g["hq"], g["hd"]), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev) if dev_status else None
+        self.scale = inputs.attention_scale(g)
+        self.launches_per_step = None
+
+    @staticmethod
+    def _td(a):
+        import torch
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    def run(self, events=None):
+        """Enqueue one step on the current stream.  events: optional list of
+        (start, end) torch events recorded around each attention call."""
+        dl, g, o = self.dl, self.g, self.outs
+        self.ctx_len.copy_(self.ctx_pre)
+        dl.dflash_step_bookkeeping(self.geom, self.raw_offsets, 1, self.acc, self.n_acc,
+                                   self.ctx_pre, None, self.prob["max_ctx"], self.prob["mask_id"],
+                                   o, self.status)
+        dl.dflash_ctx_kv_update(self.geom, self.hidden, self.n_acc, self.ctx_len, o["alloc_limit"],
+                                o["block_table"], None, self.weights, self.pool, self.ctx_ws,
+                                self.status)
+        for layer in range(g["L"]):
+            dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer], self.blk_v[layer],
+                                       o["blk_page"], o["blk_slot"], o["blk_mask"], self.pool,
+                                       self.status)
+            if events is not None:
+                events[layer][0].record()
+            dl.dflash_block_attention(self.geom, layer, self.q[layer], self.pool, o["block_table"],
+                                      o["seq_lens"], self.attn_out[layer], self.attn_ws,
+                                      window=self.prob["window"], sinks=self.sinks,
+                                      scale=self.scale, dev_status=self.status)
+            if events is not None:
+                events[layer][1].record()
+
+
+def kernel_launches_per_step(g, hidden_is_f32=False) -> int:
+    # bookkeeping 1; update: prep, fc gemm, hidden norm, kv gemm, epilogue = 5;
+    # per layer: scatter 1 + attention (split + merge) 2
+    return 1 + 5 + g["L"] * 3
+
+
+def make_events(n_layers, count):
+    import torch
+    kw = {"enable_timing": True}
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        kw["external"] = True
+    except TypeError:
+        return None
+    return [[(torch.cuda.Event(**kw), torch.cuda.Event(**kw)) for _ in range(n_layers)]
+            for _ in range(count)]
+
+
+def run_ours(args, rank, world):
+    import torch
+    from context_kv_update_gb300 import build
+    build.build()
+    import context_kv_update_gb300 as dl
+    dl.load()
+    torch.cuda.set_device(rank % max(1, torch.cuda.device_count()))
+    cfg = inputs.workload(WORKLOAD, ctx=[CTX])
+    prob = inputs.make_problem(cfg, seed=rank)
+    g = prob["g"]
+    step = Step(dl, prob)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # eager warm-up (also resolves one-time host work), then graph capture
+    with torch.cuda.stream(stream):
+        step.run()
+    torch.cuda.synchronize()
+    st = int(step.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the first step")
+
+    chunk = max(1, min(args.steps, 25))
+    ev = make_events(g["L"], chunk)
+    g_chunk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_chunk, stream=stream):
+        for c in range(chunk):
+            step.run(ev[c] if ev is not None else None)
+    g_one = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_one, stream=stream):
+        step.run()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    # warm-up: at least W steps and about a second of load for the clock record
+    t0 = time.time()
+    w = 0
+    while w < args.warmup or time.time() - t0 < 1.0:
+        g_one.replay()
+        w += 1
+        if w % 200 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    full, rest = divmod(args.steps, chunk)
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(full):
+            g_chunk.replay()
+        for _ in range(rest):
+            g_one.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = start.elapsed_time(end)
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # per-launch attention duration over the last replayed chunk
+    attn_ms = None
+    if ev is not None and full > 0:
+        durs = [s.elapsed_time(e) for per in ev for (s, e) in per]
+        attn_ms = sum(durs) / len(durs)
+    else:
+        # no external events in this torch: time the attention calls eagerly
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(g["L"])]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step.run([evs[i] for i in range(g["L"])])
+        torch.cuda.synchronize()
+        attn_ms = sum(s.elapsed_time(e) for s, e in evs) / len(evs)
+
+    e2e = run_e2e(dl, step, stream, min(args.steps, 200))
+    st = int(step.status.item())
+    return dict(ms_step=ms_step, attn_ms=attn_ms, clocks=clocks, e2e=e2e, prob=prob, status=st,
+                warmup_done=w)
+
+
+def run_e2e(dl, step, stream, steps):
+    """Same step through the public API with inputs from pinned host memory
+    and the outputs read back every step (copies inside the timed region)."""
+    import torch
+    prob, g = step.prob, step.g
+    host_in = {
+        "raw_offsets": (prob["raw_offsets"], step.raw_offsets),
+        "acc": (prob["acc"], step.acc),
+        "n_acc": (prob["n_acc"], step.n_acc),
+        "ctx_pre": (prob["ctx_len"], step.ctx_pre),
+        "hidden": (prob["hidden"], step.hidden),
+        "q": (prob["q"], step.q),
+        "blk_k": (prob["blk_k"], step.blk_k),
+        "blk_v": (prob["blk_v"], step.blk_v),
+    }
+    pinned = {}
+    for k, (a, d) in host_in.items():
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        pinned[k] = (t.pin_memory(), d)
+    out_host = torch.empty(step.attn_out.shape, dtype=torch.bfloat16).pin_memory()
+    ctx_host = torch.empty(step.outs["ctx_len_new"].shape, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t, _ in pinned.values())
+    d2h = out_host.numel() * 2 + ctx_host.numel() * 4
+
+    def one():
+        for t, d in pinned.values():
+            d.copy_(t, non_blocking=True)
+        step.run()
+        out_host.copy_(step.attn_out, non_blocking=True)
+        ctx_host.copy_(step.outs["ctx_len_new"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        one()
+    for _ in range(5):
+        gr.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            gr.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1000.0 / steps
+    return {"value": round(us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------- oracle (CPU)
+
+
+def oracle_step_seconds(prob, *, update_rows=None, attn_layers=None, attn_tokens=None,
+                        attn_heads=None):
+    """Wall time of the CPU oracle on one step: bookkeeping + context update
+    + L x (scatter + attention).  With sample sizes given, only that slice runs
+    and each part is scaled up by the fraction it covers."""
+    import oracle
+    g = prob["g"]
+    L, T, hq, nkv = g["L"], g["T"], g["hq"], g["nkv"]
+    pool = prob["pool"]  # updated in place, as the step does
+    t0 = time.perf_counter()
+    bk, _ = oracle.bookkeeping(prob["raw_offsets"], prob["acc"], prob["n_acc"], prob["ctx_len"],
+                               None, M=g["max_pages"], T=T, P=g["P"], off_div=1,
+                               max_ctx=prob["max_ctx"], mask_id=prob["mask_id"])
+    t_bk = time.perf_counter() - t0
+    n = int(prob["n_acc"].sum())
+    rows = n if update_rows is None else max(1, min(update_rows, n))
+    n_acc = prob["n_acc"] if rows == n else np.array([rows] + [0] * (prob["B"] - 1), np.int32)
+    t0 = time.perf_counter()
+    oracle.ctx_kv_update_gqa(g, prob["hidden"], n_acc, prob["ctx_len"], bk["alloc_limit"],
+                             bk["block_table"], None, prob["w_fc"], prob["g_h"], prob["w_kv"],
+                             prob["g_k"], pool)
+    t_up = (time.perf_counter() - t0) * (n / rows)
+    layers = L if attn_layers is None else max(1, min(attn_layers, L))
+    toks = T if attn_tokens is None else max(1, min(attn_tokens, T))
+    heads = hq if attn_heads is None else max(nkv, min(attn_heads, hq)) // nkv * nkv
+    scale_attn = (L / layers) * (hq * T) / (heads * toks)
+    t_at = 0.0
+    for layer in range(layers):
+        t0 = time.perf_counter()
+        oracle.block_kv_scatter_gqa(g, layer, prob["blk_k"][layer], prob["blk_v"][layer],
+                                    bk["blk_page"], bk["blk_slot"], bk["blk_mask"], pool)
+        # the last `toks` queries of the block (their key ranges end at kv_len)
+        q = np.ascontiguousarray(prob["q"][layer][:, T - toks:, :heads])
+        oracle.attention_gqa(dict(g, hq=heads), layer, q, pool, bk["block_table"],
+                             bk["seq_lens"], window=prob["window"],
+                             sinks=prob["sinks"][layer][:heads] if prob["use_sinks"] else None,
+                             scale=inputs.attention_scale(g))
+        t_at += (time.perf_counter() - t0) * scale_attn
+    return t_bk + t_up + t_at, dict(update_rows=rows, attn_layers=layers, attn_tokens=toks,
+                                    attn_heads=heads)
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    cfg = inputs.workload(WORKLOAD, ctx=[CTX])
+    prob = inputs.make_problem(cfg, seed=0)
+    sample = dict(update_rows=1, attn_layers=1, attn_tokens=1, attn_heads=prob["g"]["nkv"])
+    for _ in range(args.warmup):
+        oracle_step_seconds(prob, **sample)
+    times = []
+    meta = None
+    for _ in range(args.steps):
+        t, meta = oracle_step_seconds(prob, **sample)
+        times.append(t)
+    us = statistics.mean(times) * 1e6
+    desc = (f"each step: bookkeeping; {meta['update_rows']} accepted row through the context "
+            f"update (scaled to all accepted rows); {meta['attn_layers']} layer of scatter + "
+            f"attention for {meta['attn_tokens']} query token x {meta['attn_heads']} heads "
+            f"(scaled to 5 layers x 16 tokens x 32 heads)")
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+            "higher_is_better": False, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "qwen3_8b_drafter_ctx32k", "B": 1, "ctx_len": CTX},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def cpu_baseline(prob):
+    """The oracle as it stands on the host cores: one full step (about 10-30 s
+    of CPU work on 16 cores)."""
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    t, meta = oracle_step_seconds(prob)
+    return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "one full step (bookkeeping, context update of all accepted rows, "
+                      "5 x (scatter + attention over all 16 x 32 query rows at 32K keys))"}
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    prob = res["prob"]
+    g = prob["g"]
+    # attention reads every cached key of the step: c' + T keys (c' = c + n)
+    kv_len = int(min(prob["ctx_len"][0] + prob["n_acc"][0], prob["alloc_limit"][0])) + g["T"]
+    attn_bytes = kv_len * g["nkv"] * g["hd"] * 2 * 2
+    peaks = measured_peaks()
+    achieved = attn_bytes / (res["attn_ms"] * 1e-3) / 1e9
+    traffic = None
+    if ATTN_TRAFFIC["sources_sha"] == attention_sources_sha():
+        traffic = ATTN_TRAFFIC["bytes_per_launch"]
+    us = res["ms_step"] * 1000.0
+    line = {
+        "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) hidden/q/KV, N(0,0.02) weights)",
+        "config": {"workload": "qwen3_8b_drafter_ctx32k", "B": 1, "ctx_len": CTX,
+                   "kv_len": kv_len, "layers": g["L"], "hq": g["hq"], "nkv": g["nkv"],
+                   "hd": g["hd"], "block": g["T"], "page": g["P"], "d_model": g["D"],
+                   "timing": "CUDA-graph replay of whole steps, CUDA events on the stream",
+                   "l2": "inputs larger than L2 (KV 640 MiB + weights 117 MB per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "attn_gbs": round(achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "kernel": "dflash_block_attention (split + merge)",
+                     "bytes_per_launch": attn_bytes,
+                     "launch_ms": round(res["attn_ms"], 5),
+                     "peak_source": peaks["source"] + " hbm_gbs (of " + peaks["source"] + ")"},
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": kernel_launches_per_step(g) * args.steps,
+        "device_status": res["status"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

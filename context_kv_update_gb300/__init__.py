@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) library for the data-parallel hot path of a DFlash / DSpark
+block drafter's decode step: bookkeeping, context-KV update, block-KV scatter
+and split-KV block attention, behind the C ABI of include/dflash.h.
+
+The Python names below are the C entry points of the same names (ctypes
+marshalling only).  ``inputs`` holds the seeded synthetic workloads.
+"""
+from ._lib import (DflashError, Geom, StepOutputs, Weights, STEP_OUTPUT_FIELDS,  # noqa: F401
+                   dflash_attention_num_segments, dflash_attention_workspace_bytes,
+                   dflash_block_attention, dflash_block_kv_scatter, dflash_ctx_kv_update,
+                   dflash_ctx_workspace_bytes, dflash_step_bookkeeping, load, make_geom,
+                   KIND_GQA, KIND_MLA, MASK_CAUSAL_TAIL, MASK_BLOCK_BIDIR)

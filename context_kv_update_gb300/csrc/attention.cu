@@ -1,0 +1,180 @@
+// attention.cu -- decode-shaped split-KV block attention over the paged cache.
+//
+// Follows vLLM PR #54092 (Purpose item 2, Changes item 2): the drafter's
+// small uniform query block (1 bonus + N drafts) runs the split-KV ("3D")
+// form: the KV range is cut into segments, each segment writes per-query-token
+// partial softmax state (max, sum, weighted values), and a reduce kernel
+// merges them; the segment layout is re-based on the visible window (a
+// sliding window lights only the last slices of an equal split of the whole
+// context) and shared by the main kernel and the reduce; per-head sink logits
+// join the merge.
+//
+// Workspace (fp32): m[B, Tq, hq, S], l[B, Tq, hq, S], o[B, Tq, hq, S, dv],
+// with m in natural-log units of the scaled scores.  A segment with no visible
+// key for a row writes m = -inf, l = 0 and leaves o unwritten; the merge never
+// reads o of such a segment.
+#include <math.h>
+
+#include "attention_common.cuh"
+
+namespace dflash {
+namespace {
+
+// ----------------------------------------------------------- main (SIMT)
+// grid (S, nkv, B); 8 warps, warp w handles the group's query rows w, w+8, ...
+template <int QK_PER_LANE, int V_PER_LANE>
+__global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p) {
+  griddep_launch();
+  const int s = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  SegRange sr = segment_range(p, r, s);
+  const int rows = p.Tq * p.G;
+  for (int rho = warp; rho < rows; rho += 8) {
+    const int i = rho / p.G, h = kvh * p.G + rho % p.G;
+    const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
+    int lo, hi;
+    row_key_range(p, sr.kv_len, i, &lo, &hi);
+    lo = max(lo, sr.k0);
+    hi = min(hi, sr.k1 - 1);
+    if (sr.k0 >= sr.k1 || hi < lo) {
+      if (lane == 0) {
+        p.ws_m[wsi] = -INFINITY;
+        p.ws_l[wsi] = 0.f;
+      }
+      continue;
+    }
+    float qv[QK_PER_LANE];
+    const uint16_t *qrow = p.q + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.dq;
+    const uint16_t *qrrow =
+        p.q_rope ? p.q_rope + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.drope : nullptr;
+#pragma unroll
+    for (int e = 0; e < QK_PER_LANE; ++e) {
+      const int d = lane + 32 * e;
+      float v = 0.f;
+      if (d < p.dq) v = bf16_to_f32(qrow[d]);
+      else if (qrrow && d < p.dq + p.drope) v = bf16_to_f32(qrrow[d - p.dq]);
+      qv[e] = v;
+    }
+    float o[V_PER_LANE];
+#pragma unroll
+    for (int e = 0; e < V_PER_LANE; ++e) o[e] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    for (int j = lo; j <= hi; ++j) {
+      const uint16_t *krow, *vrow;
+      if (!key_rows(p, r, kvh, j, &krow, &vrow)) continue;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < QK_PER_LANE; ++e) {
+        const int d = lane + 32 * e;
+        if (d < p.dqk) dot += qv[e] * bf16_to_f32(krow[d]);
+      }
+      dot = warp_sum(dot) * p.scale;
+      const float mn = fmaxf(m, dot);
+      const float corr = __expf(m - mn);
+      const float pj = __expf(dot - mn);
+      l = l * corr + pj;
+#pragma unroll
+      for (int e = 0; e < V_PER_LANE; ++e) {
+        const int d = lane + 32 * e;
+        const float vv = d < p.dv ? bf16_to_f32(vrow[d]) : 0.f;
+        o[e] = o[e] * corr + pj * vv;
+      }
+      m = mn;
+    }
+    if (lane == 0) {
+      p.ws_m[wsi] = m;
+      p.ws_l[wsi] = l;
+    }
+    if (m != -INFINITY) {
+      float *orow = p.ws_o + wsi * p.dv;
+#pragma unroll
+      for (int e = 0; e < V_PER_LANE; ++e) {
+        const int d = lane + 32 * e;
+        if (d < p.dv) orow[d] = o[e];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ----------------------------------------------------------- merge
+// grid (B * Tq * hq), block = dv threads.
+__global__ void attn_merge_kernel(const AttnParams p) {
+  griddep_wait();
+  const int row = blockIdx.x;  // (r * Tq + i) * hq + h
+  const int h = row % p.hq;
+  const int d = threadIdx.x;
+  const size_t base = static_cast<size_t>(row) * p.S;
+  float M = p.sinks ? p.sinks[h] : -INFINITY;
+  for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.ws_m[base + s]);
+  float acc = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    den = p.sinks ? __expf(p.sinks[h] - M) : 0.f;
+    for (int s = 0; s < p.S; ++s) {
+      const float ms = p.ws_m[base + s];
+      if (ms == -INFINITY) continue;
+      const float w = __expf(ms - M);
+      den += w * p.ws_l[base + s];
+      if (d < p.dv) acc += w * p.ws_o[(base + s) * p.dv + d];
+    }
+  }
+  if (d < p.dv)
+    p.out[static_cast<size_t>(row) * p.dv + d] = f32_to_bf16_rn(den > 0.f ? acc / den : 0.f);
+}
+
+int attention_num_segments(const dflash_geom &g, int B, int Tq) {
+  const int sms = device_sm_count();
+  const int heads = (g.kind == DFLASH_KIND_GQA) ? g.nkv : 1;
+  const long long ctas = static_cast<long long>(B) * heads;
+  int S = static_cast<int>(sms / (ctas > 0 ? ctas : 1));
+  if (S < 1) S = 1;
+  const long long max_tiles =
+      (static_cast<long long>(g.max_pages) * g.page_size + kAttnTileKeys - 1) / kAttnTileKeys;
+  if (S > max_tiles) S = static_cast<int>(max_tiles > 0 ? max_tiles : 1);
+  (void)Tq;
+  return S;
+}
+
+size_t attention_workspace_bytes(const dflash_geom &g, int B, int Tq, int S) {
+  if (S <= 0) S = attention_num_segments(g, B, Tq);
+  const int dv = (g.kind == DFLASH_KIND_GQA) ? g.head_dim : g.latent_dim;
+  const size_t rows = static_cast<size_t>(B) * Tq * g.hq * S;
+  size_t off = align_up(rows * sizeof(float), 256) * 2;
+  off += rows * dv * sizeof(float);
+  return align_up(off, 256);
+}
+
+cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int Tq, const void *q,
+                                   const void *q_rope, const void *pool, const int32_t *tbl,
+                                   const int32_t *kv_len, int32_t window, const float *sinks,
+                                   float scale, int mask_mode, int S, void *ws, void *out,
+                                   int32_t *st, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  if (S <= 0) S = attention_num_segments(g, B, Tq);
+  AttnParams p = make_attn_params(g, B, layer, Tq, q, q_rope, pool, tbl, kv_len, window, sinks,
+                                  scale, mask_mode, S, ws, out, st);
+  cudaError_t e;
+  if (g.kind == DFLASH_KIND_GQA) {
+    attn_split_simt_kernel<4, 4><<<dim3(S, g.nkv, B), 256, 0, s>>>(p);
+  } else {
+    attn_split_simt_kernel<18, 16><<<dim3(S, 1, B), 256, 0, s>>>(p);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_attn_merge(p, s);
+}
+
+cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(p.B * p.Tq * p.hq);
+  cfg.blockDim = dim3(p.dv);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
+}
+
+}  // namespace dflash

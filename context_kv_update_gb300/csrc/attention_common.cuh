@@ -1,0 +1,153 @@
+// attention_common.cuh -- parameters, masks and the window-rebased segment
+// layout shared by the split-KV attention kernels and the merge.
+#pragma once
+
+#include <math.h>
+
+#include "dflash_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace dflash {
+
+using ptx::griddep_launch;
+using ptx::griddep_wait;
+
+struct AttnParams {
+  int kind, B, Tq, hq, nkv, G, layer, NP, P, M;
+  int dq, drope, dqk, dv, W;  // q width, q_rope width, score width, value width, latent row
+  int window, mask_mode, S;
+  float scale;
+  const uint16_t *q, *q_rope, *pool;
+  const int32_t *tbl, *kv_len;
+  const float *sinks;
+  float *ws_m, *ws_l, *ws_o;
+  uint16_t *out;
+  int32_t *st;
+};
+
+inline AttnParams make_attn_params(const dflash_geom &g, int B, int layer, int Tq, const void *q,
+                                   const void *q_rope, const void *pool, const int32_t *tbl,
+                                   const int32_t *kv_len, int32_t window, const float *sinks,
+                                   float scale, int mask_mode, int S, void *ws, void *out,
+                                   int32_t *st) {
+  AttnParams p;
+  p.kind = g.kind;
+  p.B = B;
+  p.Tq = Tq;
+  p.hq = g.hq;
+  p.nkv = (g.kind == DFLASH_KIND_GQA) ? g.nkv : 1;
+  p.G = g.hq / p.nkv;
+  p.layer = layer;
+  p.NP = g.num_pool_pages;
+  p.P = g.page_size;
+  p.M = g.max_pages;
+  if (g.kind == DFLASH_KIND_GQA) {
+    p.dq = g.head_dim;
+    p.drope = 0;
+    p.dv = g.head_dim;
+    p.W = g.head_dim;
+  } else {
+    p.dq = g.latent_dim;
+    p.drope = g.rope_dim;
+    p.dv = g.latent_dim;
+    p.W = g.latent_dim + g.rope_dim;
+  }
+  p.dqk = p.dq + p.drope;
+  p.window = window;
+  p.mask_mode = mask_mode;
+  p.S = S;
+  p.scale = scale;
+  p.q = static_cast<const uint16_t *>(q);
+  p.q_rope = static_cast<const uint16_t *>(q_rope);
+  p.pool = static_cast<const uint16_t *>(pool);
+  p.tbl = tbl;
+  p.kv_len = kv_len;
+  p.sinks = sinks;
+  const size_t rows = static_cast<size_t>(B) * Tq * g.hq * S;
+  char *w = static_cast<char *>(ws);
+  p.ws_m = reinterpret_cast<float *>(w);
+  p.ws_l = reinterpret_cast<float *>(w + align_up(rows * sizeof(float), 256));
+  p.ws_o = reinterpret_cast<float *>(w + 2 * align_up(rows * sizeof(float), 256));
+  p.out = static_cast<uint16_t *>(out);
+  p.st = st;
+  return p;
+}
+
+cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s);
+
+// kv_len of request r, clamped to [0, M*P] (flagging out-of-range values).
+__device__ __forceinline__ int clamped_kv_len(const AttnParams &p, int r, bool report) {
+  int kl = p.kv_len[r];
+  const long long cap = static_cast<long long>(p.M) * p.P;
+  if (kl < 0 || kl > cap) {
+    if (report) raise_status(p.st, DFLASH_DEV_KV_LEN_RANGE);
+    kl = kl < 0 ? 0 : static_cast<int>(cap);
+  }
+  return kl;
+}
+
+// Visible keys [lo, hi] of query token i (hi < lo: none).
+__device__ __forceinline__ void row_key_range(const AttnParams &p, int kv_len, int i, int *lo,
+                                              int *hi) {
+  const int pos = kv_len - p.Tq + i;
+  *hi = (p.mask_mode == DFLASH_MASK_CAUSAL_TAIL) ? pos : kv_len - 1;
+  int l = 0;
+  if (p.window > 0) {
+    const int w0 = pos - p.window + 1;
+    l = w0 > 0 ? w0 : 0;
+  }
+  *lo = l;
+}
+
+// Key range [k0, k1) of segment s of request r: the union of the block's
+// visible ranges, [lo_0, kv_len), re-based to start at its first 128-key tile
+// and cut into S runs of whole tiles.
+struct SegRange {
+  int kv_len, k0, k1, t0, t1;
+};
+__device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, int s) {
+  SegRange sr;
+  sr.kv_len = clamped_kv_len(p, r, s == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+  sr.k0 = sr.k1 = sr.t0 = sr.t1 = 0;
+  if (sr.kv_len <= 0) return sr;
+  int lo0, hi0;
+  row_key_range(p, sr.kv_len, 0, &lo0, &hi0);
+  const int tile_lo = lo0 / kAttnTileKeys;
+  const int tile_hi = (sr.kv_len - 1) / kAttnTileKeys + 1;
+  const int ntiles = tile_hi - tile_lo;
+  const int per = (ntiles + p.S - 1) / p.S;
+  sr.t0 = tile_lo + s * per;
+  sr.t1 = min(tile_hi, sr.t0 + per);
+  if (sr.t0 >= sr.t1) {
+    sr.t0 = sr.t1 = 0;
+    return sr;
+  }
+  sr.k0 = max(lo0, sr.t0 * kAttnTileKeys);
+  sr.k1 = min(sr.kv_len, sr.t1 * kAttnTileKeys);
+  return sr;
+}
+
+// Cache rows of key j (GQA: K and V of head kvh; MLA: the latent row twice).
+// False when the table maps j outside the pool (flagged).
+__device__ __forceinline__ bool key_rows(const AttnParams &p, int r, int kvh, int j,
+                                         const uint16_t **krow, const uint16_t **vrow) {
+  const int lp = j / p.P;
+  const int page = p.tbl[static_cast<int64_t>(r) * p.M + lp];
+  if (page < 0 || page >= p.NP) {
+    raise_status(p.st, DFLASH_DEV_BAD_PAGE);
+    return false;
+  }
+  const int slot = j - lp * p.P;
+  if (p.kind == DFLASH_KIND_GQA) {
+    const size_t base = ((static_cast<size_t>(p.layer) * p.NP + page) * 2) * p.nkv;
+    *krow = p.pool + (((base + 0 * p.nkv) + kvh) * p.P + slot) * static_cast<size_t>(p.dq);
+    *vrow = p.pool + (((base + 1 * p.nkv) + kvh) * p.P + slot) * static_cast<size_t>(p.dq);
+  } else {
+    *krow = p.pool + ((static_cast<size_t>(p.layer) * p.NP + page) * p.P + slot) *
+                         static_cast<size_t>(p.W);
+    *vrow = *krow;
+  }
+  return true;
+}
+
+}  // namespace dflash

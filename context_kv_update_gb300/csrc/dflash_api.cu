@@ -1,0 +1,192 @@
+// dflash_api.cu -- the extern "C" entry points declared in include/dflash.h:
+// argument validation, then the launchers of the other translation units.
+// Nothing here allocates, synchronises or reads device memory.
+#include <cmath>
+#include <mutex>
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
+void fill_rope_freqs(RopeFreqs *rf, int dim, double theta) {
+  for (int j = 0; j < dim / 2 && j < kMaxHeadDim / 2; ++j)
+    rf->f[j] = std::pow(theta, -2.0 * static_cast<double>(j) / static_cast<double>(dim));
+}
+
+namespace {
+
+bool geom_ok(const dflash_geom *g) {
+  if (!g) return false;
+  if (g->num_layers < 1 || g->d_in < 1 || g->d_model < 1 || g->hq < 1 || g->page_size < 1 ||
+      g->max_pages < 1 || g->num_pool_pages < 1 || g->block_size < 1)
+    return false;
+  if (g->kind == DFLASH_KIND_GQA) {
+    if (g->nkv < 1 || g->head_dim < 8 || g->hq % g->nkv != 0) return false;
+  } else if (g->kind == DFLASH_KIND_MLA) {
+    if (g->latent_dim < 8 || g->rope_dim < 2) return false;
+  } else {
+    return false;
+  }
+  if (!(g->rope_theta > 0.0) || !(g->eps_hidden >= 0.0) || !(g->eps_k >= 0.0)) return false;
+  return true;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+int dflash_abi_version(void) { return 1; }
+
+const char *dflash_status_string(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED_GEOM: return "unsupported geometry";
+    case DFLASH_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
+
+extern "C" int dflash_step_bookkeeping(const dflash_geom *g, int B, const int32_t *raw_offsets,
+                                       int64_t off_row_stride, int32_t off_div,
+                                       const int32_t *accepted_tokens, int64_t acc_row_stride,
+                                       const int32_t *n_accepted, const int32_t *ctx_len_pre,
+                                       const uint8_t *valid, int32_t max_ctx,
+                                       int32_t mask_token_id, const dflash_step_outputs *out,
+                                       int32_t *dev_status, dflash_stream_t stream) {
+  if (!g || B < 0 || off_div < 1 || !out) return DFLASH_ERR_INVALID_ARG;
+  if (g->max_pages < 1 || g->page_size < 1 || g->block_size < 1) return DFLASH_ERR_INVALID_ARG;
+  if (B == 0) return DFLASH_OK;
+  if (!raw_offsets || !accepted_tokens || !n_accepted || !ctx_len_pre) return DFLASH_ERR_INVALID_ARG;
+  if (off_row_stride < g->max_pages || acc_row_stride < g->block_size) return DFLASH_ERR_INVALID_ARG;
+  if (max_ctx < 0) return DFLASH_ERR_INVALID_ARG;
+  const dflash_step_outputs &o = *out;
+  if (!o.n_pages || !o.block_table || !o.alloc_limit || !o.bonus || !o.emb_ids || !o.ctx_pos ||
+      !o.q_pos || !o.ctx_dst_page || !o.ctx_dst_slot || !o.ctx_wmask || !o.blk_page ||
+      !o.blk_slot || !o.blk_mask || !o.ctx_len_new || !o.seq_lens)
+    return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(launch_bookkeeping(*g, B, raw_offsets, off_row_stride, off_div,
+                                        accepted_tokens, acc_row_stride, n_accepted, ctx_len_pre,
+                                        valid, max_ctx, mask_token_id, o, dev_status,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t dflash_ctx_workspace_bytes(const dflash_geom *g, int B) {
+  if (!geom_ok(g) || B < 0) return 0;
+  return ctx_workspace_bytes(*g, B);
+}
+
+extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hidden,
+                                    int hidden_dtype, const int32_t *n_accepted, int32_t *ctx_len,
+                                    const int32_t *alloc_limit, const int32_t *block_table,
+                                    const uint8_t *valid, const dflash_weights *w, void *kv_pool,
+                                    void *workspace, size_t ws_bytes, int32_t *dev_status,
+                                    dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || !w) return DFLASH_ERR_INVALID_ARG;
+  if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
+    return DFLASH_ERR_INVALID_ARG;
+  if (g->d_in % 64 != 0 || g->d_model % 64 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  if (g->kind == DFLASH_KIND_GQA) {
+    if (g->head_dim % 8 != 0 || g->head_dim > kMaxHeadDim || g->head_dim % 2 != 0)
+      return DFLASH_ERR_UNSUPPORTED_GEOM;
+  } else {
+    if (g->latent_dim + g->rope_dim > 1024 || g->rope_dim % 2 != 0 || g->rope_dim > kMaxHeadDim ||
+        (g->latent_dim + g->rope_dim) % 8 != 0)
+      return DFLASH_ERR_UNSUPPORTED_GEOM;
+  }
+  if (B == 0) return DFLASH_OK;
+  if (!hidden || !n_accepted || !ctx_len || !alloc_limit || !block_table || !kv_pool || !workspace)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!w->w_fc || !w->gamma_h || !w->w_kv || !w->gamma_k) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w->w_fc) || !aligned16(w->w_kv) || !aligned16(kv_pool) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (ws_bytes < ctx_workspace_bytes(*g, B)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_ctx_kv_update(*g, B, hidden, hidden_dtype, n_accepted, ctx_len,
+                                          alloc_limit, block_table, valid, *w, kv_pool, workspace,
+                                          dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_block_kv_scatter(const dflash_geom *g, int B, int layer, const void *blk_k,
+                                       const void *blk_v, const int32_t *blk_page,
+                                       const int32_t *blk_slot, const uint8_t *blk_mask,
+                                       void *kv_pool, int32_t *dev_status,
+                                       dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || layer < 0 || layer >= g->num_layers) return DFLASH_ERR_INVALID_ARG;
+  if (B == 0) return DFLASH_OK;
+  if (!blk_k || !blk_page || !blk_slot || !blk_mask || !kv_pool) return DFLASH_ERR_INVALID_ARG;
+  if (g->kind == DFLASH_KIND_GQA) {
+    if (!blk_v || !aligned16(blk_v)) return DFLASH_ERR_INVALID_ARG;
+    if (g->head_dim % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  } else {
+    if (blk_v) return DFLASH_ERR_INVALID_ARG;
+    if ((g->latent_dim + g->rope_dim) % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  }
+  if (!aligned16(blk_k) || !aligned16(kv_pool)) return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(launch_block_scatter(*g, B, layer, blk_k, blk_v, blk_page, blk_slot, blk_mask,
+                                          kv_pool, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_attention_num_segments(const dflash_geom *g, int B, int Tq) {
+  if (!geom_ok(g) || B < 1 || Tq < 1) return 0;
+  return attention_num_segments(*g, B, Tq);
+}
+
+extern "C" size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, int Tq,
+                                                   int num_segments) {
+  if (!geom_ok(g) || B < 0 || Tq < 1 || num_segments < 0) return 0;
+  return attention_workspace_bytes(*g, B, Tq, num_segments);
+}
+
+extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq,
+                                      const void *q, const void *q_rope, const void *kv_pool,
+                                      const int32_t *block_table, const int32_t *kv_len,
+                                      int32_t window, const float *sinks, float scale,
+                                      int mask_mode, int num_segments, void *workspace,
+                                      size_t ws_bytes, void *out, int32_t *dev_status,
+                                      dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || Tq < 1 || layer < 0 || layer >= g->num_layers || window < 0 ||
+      num_segments < 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (mask_mode != DFLASH_MASK_CAUSAL_TAIL && mask_mode != DFLASH_MASK_BLOCK_BIDIR)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DFLASH_ERR_INVALID_ARG;
+  if (g->kind == DFLASH_KIND_GQA) {
+    if (g->head_dim != 64 && g->head_dim != 128) return DFLASH_ERR_UNSUPPORTED_GEOM;
+    if (q_rope) return DFLASH_ERR_INVALID_ARG;
+  } else {
+    if (g->latent_dim != 512 || g->rope_dim != 64) return DFLASH_ERR_UNSUPPORTED_GEOM;
+    if (!q_rope) return DFLASH_ERR_INVALID_ARG;
+  }
+  const int P = g->page_size;
+  if (P % 8 != 0 || !(kAttnTileKeys % P == 0 || P % kAttnTileKeys == 0))
+    return DFLASH_ERR_UNSUPPORTED_GEOM;
+  if (B == 0) return DFLASH_OK;
+  if (!q || !kv_pool || !block_table || !kv_len || !workspace || !out) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(workspace) || !aligned16(out) ||
+      (q_rope && !aligned16(q_rope)))
+    return DFLASH_ERR_INVALID_ARG;
+  const int S = num_segments > 0 ? num_segments : attention_num_segments(*g, B, Tq);
+  if (ws_bytes < attention_workspace_bytes(*g, B, Tq, S)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_block_attention(*g, B, layer, Tq, q, q_rope, kv_pool, block_table,
+                                            kv_len, window, sinks, scale, mask_mode, S, workspace,
+                                            out, dev_status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}

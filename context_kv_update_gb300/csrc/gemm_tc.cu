@@ -1,0 +1,319 @@
+// gemm_tc.cu -- stream-K tcgen05 GEMM for the weight-bound context projection
+// (fc, then the K/V or latent projection stacked over every drafter layer,
+// TensorRT-LLM PR #13995 "migrate draft path to per-layer cached K/V pool").
+//
+// CTA = 6 warps: warp 0 issues TMA loads (one elected lane), warp 1 issues
+// tcgen05.mma (one lane), warps 2-5 drain the TMEM accumulator (warp w reads
+// TMEM lanes 32*(w%4)..+31) and write fp32 partial tiles.  A ring of `stages`
+// shared-memory slots, each one 128x64 weight tile + one NTILEx64 activation
+// tile, is guarded by full/empty mbarriers; the accumulator by acc_full /
+// acc_empty.  Every wait is bounded (ptx::mbar_wait) so a broken pipeline
+// winds the kernel down instead of hanging it.
+#include "gemm_tc.cuh"
+
+#include <algorithm>
+#include <mutex>
+
+namespace dflash {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kMaxSmem = 227 * 1024;
+
+struct GemmParams {
+  int K, ntile, mtiles, kblocks, maxt, stages;
+  long long units;
+  float *part;
+  uint32_t idesc;
+  uint32_t tmem_cols;
+  int pdl_wait;
+  int32_t *status;
+};
+
+__host__ __device__ inline uint32_t a_tile_bytes() { return 128u * 64u * 2u; }
+__host__ __device__ inline uint32_t b_tile_bytes(int ntile) { return static_cast<uint32_t>(ntile) * 128u; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  const uint32_t abytes = a_tile_bytes(), bbytes = b_tile_bytes(p.ntile);
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + S * abytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * bbytes);
+  uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S, *acc_empty = bars + 2 * S + 1;
+  uint64_t *drain = bars + 2 * S + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 3);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *consumed = reinterpret_cast<int *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(acc_empty), 4);
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // The next kernel of the chain only prefetches what does not depend on this
+  // one and then waits for this grid to complete, so it may launch now.
+  griddep_launch();
+
+  const long long C = gridDim.x, c = blockIdx.x, U = p.units, KB = p.kblocks;
+  const long long u_lo = c * U / C, u_hi = (c + 1) * U / C;
+  const long long t_first = u_lo / KB, t_last = (u_hi - 1) / KB;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint64_t pol_w = ptx::policy_evict_first();
+      long long issued = 0;
+      bool ok = true;
+      // Prologue: weight tiles of the first ring slots do not depend on the
+      // previous kernel, so they are in flight before the dependency wait.
+      const long long pre = std::min<long long>(S, u_hi - u_lo);
+      for (long long u = u_lo; u < u_lo + pre; ++u) {
+        const long long t = u / KB;
+        const int kb = static_cast<int>(u - t * KB);
+        const int m = static_cast<int>(t % p.mtiles);
+        const int s = static_cast<int>(u - u_lo);
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), abytes + bbytes);
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + s * abytes), &tmW, kb * 64, m * 128,
+                              ptx::smem_u32(&full[s]), pol_w);
+      }
+      if (p.pdl_wait) griddep_wait();
+      for (long long u = u_lo; u < u_lo + pre; ++u) {
+        const long long t = u / KB;
+        const int kb = static_cast<int>(u - t * KB);
+        const int nt = static_cast<int>(t / p.mtiles);
+        const int s = static_cast<int>(u - u_lo);
+        ptx::tma_load_2d(ptx::smem_u32(sB + s * bbytes), &tmX, kb * 64, nt * p.ntile,
+                         ptx::smem_u32(&full[s]));
+      }
+      issued = pre;
+      for (long long u = u_lo + pre; u < u_hi; ++u) {
+        const long long it = u - u_lo;
+        const int s = static_cast<int>(it % S);
+        const uint32_t ph = static_cast<uint32_t>((it / S) & 1);
+        if (!ptx::mbar_wait(ptx::smem_u32(&empty[s]), ph ^ 1u, abort_flag)) { ok = false; break; }
+        const long long t = u / KB;
+        const int kb = static_cast<int>(u - t * KB);
+        const int m = static_cast<int>(t % p.mtiles);
+        const int nt = static_cast<int>(t / p.mtiles);
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), abytes + bbytes);
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + s * abytes), &tmW, kb * 64, m * 128,
+                              ptx::smem_u32(&full[s]), pol_w);
+        ptx::tma_load_2d(ptx::smem_u32(sB + s * bbytes), &tmX, kb * 64, nt * p.ntile,
+                         ptx::smem_u32(&full[s]));
+        ++issued;
+      }
+      if (!ok) {
+        // wind down: let the copies already issued land before the CTA exits
+        for (long long it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
+          volatile int dummy = 0;
+          ptx::mbar_wait(ptx::smem_u32(&full[it % S]), static_cast<uint32_t>((it / S) & 1), &dummy);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      long long it = 0;
+      int tile_i = 0;
+      bool ok = true;
+      for (long long t = t_first; t <= t_last && ok; ++t, ++tile_i) {
+        const long long ua = std::max(u_lo, t * KB), ub = std::min(u_hi, (t + 1) * KB);
+        if (!ptx::mbar_wait(ptx::smem_u32(acc_empty), static_cast<uint32_t>(tile_i & 1) ^ 1u,
+                            abort_flag)) { ok = false; break; }
+        ptx::tc_fence_after();
+        for (long long u = ua; u < ub; ++u, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = static_cast<uint32_t>((it / S) & 1);
+          if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), ph, abort_flag)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_base = ptx::smem_u32(sA + s * abytes);
+          const uint32_t b_base = ptx::smem_u32(sB + s * bbytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ptx::mma_bf16(tmem, ptx::desc_kmajor_sw128(a_base, k), ptx::desc_kmajor_sw128(b_base, k),
+                          p.idesc, (u > ua || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&empty[s]));
+          *reinterpret_cast<volatile int *>(consumed) = static_cast<int>(it + 1);
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_u32(acc_full));
+      }
+      if (!ok) {
+        // make sure no MMA is still reading shared memory / writing TMEM
+        ptx::mma_commit(ptx::smem_u32(drain));
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> fp32 partial tiles
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int tile_i = 0;
+    for (long long t = t_first; t <= t_last; ++t, ++tile_i) {
+      if (!ptx::mbar_wait(ptx::smem_u32(acc_full), static_cast<uint32_t>(tile_i & 1), abort_flag))
+        break;
+      ptx::tc_fence_after();
+      const long long local = t - t_first;
+      float *dst = p.part + ((c * p.maxt + local) * p.ntile) * 128 + row;
+      for (int n0 = 0; n0 < p.ntile; n0 += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0), r);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(acc_empty));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) raise_status(p.status, DFLASH_DEV_WAIT_TIMEOUT);
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct Schedule {
+  int ntile, nt, mtiles, kblocks, ctas, maxt, stages;
+  long long units;
+};
+
+Schedule make_schedule(int M, int K, int Npad) {
+  Schedule s;
+  s.ntile = Npad <= 256 ? Npad : 256;
+  s.nt = (Npad + s.ntile - 1) / s.ntile;
+  s.mtiles = (M + 127) / 128;
+  s.kblocks = (K + 63) / 64;
+  s.units = static_cast<long long>(s.nt) * s.mtiles * s.kblocks;
+  const long long sms = device_sm_count();
+  s.ctas = static_cast<int>(std::min<long long>(s.units, sms));
+  const long long per = (s.units + s.ctas - 1) / s.ctas;
+  s.maxt = static_cast<int>((per + s.kblocks - 1) / s.kblocks + 1);
+  const int stage_bytes = static_cast<int>(a_tile_bytes() + b_tile_bytes(s.ntile));
+  s.stages = std::min(8, (kMaxSmem - 2048) / stage_bytes);
+  return s;
+}
+
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
+// box of box_rows x 64 columns and 128-byte swizzle.
+cudaError_t make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_elems, uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_elems * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t gemm_partial_bytes(int M, int K, int Npad) {
+  const Schedule s = make_schedule(M, K, Npad);
+  return static_cast<size_t>(s.ctas) * s.maxt * s.ntile * 128 * sizeof(float);
+}
+
+cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
+                        GemmOut *out, bool pdl, cudaStream_t st) {
+  const int Npad = static_cast<int>(align_up(static_cast<size_t>(N), 16));
+  const Schedule s = make_schedule(M, K, Npad);
+  CUtensorMap tmW, tmX;
+  cudaError_t e;
+  if ((e = make_tmap_bf16_2d(&tmW, W, M, K, K, 128, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tmX, X, N, K, K, s.ntile, 64)) != cudaSuccess) return e;
+
+  GemmParams p;
+  p.K = K;
+  p.ntile = s.ntile;
+  p.mtiles = s.mtiles;
+  p.kblocks = s.kblocks;
+  p.maxt = s.maxt;
+  p.stages = s.stages;
+  p.units = s.units;
+  p.part = part;
+  p.idesc = ptx::idesc_bf16_f32(128, s.ntile);
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(s.ntile)) cols <<= 1;
+  p.tmem_cols = cols;
+  p.pdl_wait = 1;
+  p.status = nullptr;
+
+  const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
+                      (2 * s.stages + 3) * 8 + 16;
+  if ((e = ensure_smem_limit(gemm_tc_kernel, kMaxSmem)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(s.ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, p)) != cudaSuccess) return e;
+
+  out->part = part;
+  out->ntile = s.ntile;
+  out->mtiles = s.mtiles;
+  out->kblocks = s.kblocks;
+  out->ctas = s.ctas;
+  out->maxt = s.maxt;
+  out->units = s.units;
+  return cudaSuccess;
+}
+
+}  // namespace dflash

@@ -1,0 +1,62 @@
+// gemm_tc.cuh -- the weight-streaming projection GEMM (tcgen05 + TMA) used by
+// the context-KV update, and the device-side reader of its partial sums.
+//
+// Y[n, m] = sum_k X[n, k] * W[m, k]: X = activations [Npad, K] bf16 (a few to a
+// few hundred rows), W = weights [M, K] bf16.  The weights sit on the MMA's M
+// side (128 rows per tile, K-major, 128-byte swizzle) and the activation rows
+// on its N side, so a decode-sized batch still fills the 128-row datapath.
+// The (N tile, M tile, 64-deep K block) units are spread evenly over one CTA
+// per SM (stream-K): each CTA streams exactly its share of the weights once
+// and writes one fp32 partial tile per output tile it touched.  Consumers sum
+// the partials of a tile in CTA order (deterministic), see gemm_out_value.
+#pragma once
+
+#include <cuda.h>
+
+#include "dflash_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace dflash {
+
+using ptx::griddep_launch;
+using ptx::griddep_wait;
+
+// Where a GEMM left its result: partial tiles plus the stream-K schedule.
+struct GemmOut {
+  const float *part;
+  int ntile;        // activation rows per N tile (16..256)
+  int mtiles;       // ceil(M / 128)
+  int kblocks;      // ceil(K / 64)
+  int ctas;         // CTAs of the launch
+  int maxt;         // partial-tile slots per CTA
+  long long units;  // n_tiles * mtiles * kblocks
+};
+
+// Sum of the partials of output (n, m), in increasing CTA order.
+__device__ __forceinline__ float gemm_out_value(const GemmOut &y, int n, int m) {
+  const int nt = n / y.ntile, nn = n - nt * y.ntile;
+  const long long t = static_cast<long long>(nt) * y.mtiles + (m >> 7);
+  const int row = m & 127;
+  const long long U = y.units, C = y.ctas, KB = y.kblocks;
+  const long long a = t * KB, b = (t + 1) * KB;
+  const long long c0 = ((a + 1) * C - 1) / U;
+  const long long c1 = (b * C - 1) / U;
+  float acc = 0.f;
+  for (long long c = c0; c <= c1; ++c) {
+    const long long local = t - (c * U / C) / KB;
+    acc += y.part[((c * y.maxt + local) * y.ntile + nn) * 128 + row];
+  }
+  return acc;
+}
+
+// Bytes of partial-tile storage a GEMM of this shape needs on this device.
+size_t gemm_partial_bytes(int M, int K, int Npad);
+
+// Enqueue Y = X W^T.  X: [Npad, K] bf16 (rows >= N may hold anything; they
+// are computed but never read back), W: [M, K] bf16.  `pdl` launches with
+// programmatic stream serialization: the kernel prefetches weight tiles before
+// waiting on the previous kernel's output.
+cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
+                        GemmOut *out, bool pdl, cudaStream_t s);
+
+}  // namespace dflash

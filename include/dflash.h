@@ -1,0 +1,316 @@
+/*
+ * dflash.h -- C ABI of the GB300 (sm_103a) drafter decode-step library.
+ *
+ * The library implements the data-parallel hot path of one decode step of a
+ * DFlash / DSpark block drafter:
+ *   1. the bookkeeping around the context-KV update (block-table decode,
+ *      bonus / mask embedding ids, query and context positions, write masks,
+ *      ctx_len advance, block placement);
+ *   2. the context-KV update itself (fc -> hidden RMSNorm -> stacked per-layer
+ *      K/V or latent projection -> k RMSNorm + RoPE -> masked paged store);
+ *   3. the block-KV scatter and the decode-shaped split-KV block attention.
+ *
+ * Conventions shared by every call
+ *  - All pointers named as device buffers are device pointers the caller owns
+ *    and keeps alive until the work on `stream` has finished.  No call
+ *    allocates memory, synchronises the host, or reads a device value on the
+ *    host, so every call may be captured in a CUDA graph.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; a return of DFLASH_OK means "validated and
+ *    enqueued", not "finished".
+ *  - bf16 means IEEE bfloat16 (1-8-7).  Every tensor is dense row-major in the
+ *    stated shape unless a row stride is given.  Device buffers read with
+ *    vector loads or TMA (KV pool, weights, hidden, q, block K/V, workspace)
+ *    must be 16-byte aligned.
+ *  - Per-request scalars (n_accepted, ctx_len, kv_len, ...) live in device
+ *    arrays and are read on the device only.
+ *  - Errors: a call returns a dflash_status_code.  Host-detectable problems
+ *    (null pointers, bad geometry, misalignment, small workspace) return an
+ *    error and enqueue nothing; there is no fallback path.  Problems in device
+ *    data (a page id outside the pool, n_accepted outside [1, T], kv_len
+ *    beyond the table) never fault: the affected row is masked or clamped and
+ *    a DFLASH_DEV_* bit is OR-ed into *dev_status when dev_status is non-NULL.
+ *
+ * KV pool layouts (one plane per drafter layer, pages shared by all layers)
+ *  - GQA: bf16 [L][num_pool_pages][2][nkv][page_size][head_dim]; index 0 of
+ *    the third axis is K, 1 is V.  One (layer, page, K|V, head) block is
+ *    page_size * head_dim contiguous values.
+ *  - MLA: bf16 [L][num_pool_pages][page_size][latent_dim + rope_dim]; one
+ *    latent row per token: RMS-normed latent then the rotated rope part.
+ *
+ * Sources (page title and part):
+ *  [TRT-20548] TensorRT-LLM issue #20548, Proposal.
+ *  [TRT-20550] TensorRT-LLM PR #20550, Description and the follow-up commit
+ *              "spec_tail_kernels.py".
+ *  [TRT-13995] TensorRT-LLM PR #13995 "DFlash performance optimizations",
+ *              commits "migrate draft path to per-layer cached K/V pool",
+ *              "fuse cross-layer k_norm", "match RoPE between context and
+ *              query", "fuse query-input build", "drop K-1 filler tokens".
+ *  [VLLM-54092] vLLM PR #54092, Purpose item 2 and Changes item 2.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st *dflash_stream_t;
+
+/* Return codes. */
+enum dflash_status_code {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,        /* null / misaligned pointer, bad count or index */
+  DFLASH_ERR_UNSUPPORTED_GEOM = 2,   /* geometry outside what the kernels implement */
+  DFLASH_ERR_WORKSPACE_TOO_SMALL = 3,
+  DFLASH_ERR_CUDA = 4                /* a CUDA runtime / driver call failed */
+};
+
+/* Bits OR-ed into *dev_status by device code. */
+#define DFLASH_DEV_BAD_NACCEPTED 1u   /* live row with n_accepted outside [1, T]: treated as dummy */
+#define DFLASH_DEV_BAD_CTX_LEN 2u     /* live row with ctx_len < 0: treated as dummy */
+#define DFLASH_DEV_CTX_OUTRUN 4u      /* ctx_len already beyond the allocation limit */
+#define DFLASH_DEV_BAD_PAGE 8u        /* table entry outside [0, num_pool_pages): row/key masked */
+#define DFLASH_DEV_KV_LEN_RANGE 16u   /* kv_len < 0 or > max_pages * page_size: clamped */
+#define DFLASH_DEV_WAIT_TIMEOUT 32u   /* an on-chip pipeline wait hit its iteration limit */
+
+enum dflash_kind { DFLASH_KIND_GQA = 0, DFLASH_KIND_MLA = 1 };
+enum dflash_mask_mode { DFLASH_MASK_CAUSAL_TAIL = 0, DFLASH_MASK_BLOCK_BIDIR = 1 };
+enum dflash_dtype { DFLASH_DTYPE_BF16 = 0, DFLASH_DTYPE_F32 = 1 };
+
+/* Drafter geometry.  Filled once by the caller. */
+typedef struct dflash_geom {
+  int32_t kind;            /* DFLASH_KIND_GQA or DFLASH_KIND_MLA */
+  int32_t num_layers;      /* L: drafter layers sharing one page table */
+  int32_t d_in;            /* fc input width (target hidden size) */
+  int32_t d_model;         /* fc output width = drafter hidden size */
+  int32_t hq;              /* query heads */
+  int32_t nkv;             /* KV heads (GQA); 1 for MLA */
+  int32_t head_dim;        /* GQA head dim (64 or 128) */
+  int32_t latent_dim;      /* MLA latent width (512) */
+  int32_t rope_dim;        /* MLA rotated width (64) */
+  int32_t page_size;       /* P: tokens per page */
+  int32_t max_pages;       /* M: entries per block-table row */
+  int32_t num_pool_pages;  /* pages in each layer plane of the pool */
+  int32_t block_size;      /* T = K + 1 rows per request (bonus + K drafts) */
+  int32_t reserved0;
+  double rope_theta;       /* RoPE base */
+  double eps_hidden;       /* eps of the hidden RMSNorm */
+  double eps_k;            /* eps of the k (or latent) RMSNorm, shared by all layers */
+} dflash_geom;
+
+/* Weights of the context projection, packed once by the caller.  All bf16.
+ *  w_fc    [d_model, d_in]
+ *  gamma_h [d_model]
+ *  w_kv    GQA: [L][2][nkv][head_dim][d_model]  (K rows, then V rows, per layer)
+ *          MLA: [L][latent_dim + rope_dim][d_model]
+ *  gamma_k GQA: [L][head_dim] (shared by the heads of a layer)
+ *          MLA: [L][latent_dim]
+ * The stacking of every layer's K/V projection into one matrix is what lets
+ * one GEMM serve all drafter layers [TRT-13995, "per-layer cached K/V pool";
+ * "fuse cross-layer k_norm": stacked k_norm weights, one eps]. */
+typedef struct dflash_weights {
+  const void *w_fc;
+  const void *gamma_h;
+  const void *w_kv;
+  const void *gamma_k;
+} dflash_weights;
+
+/* Outputs of dflash_step_bookkeeping (all device, int32 unless noted;
+ * [B] or [B, T] or [B, M] dense). */
+typedef struct dflash_step_outputs {
+  int32_t *n_pages;      /* [B]    pages the request owns (count of offsets >= 0) */
+  int32_t *block_table;  /* [B, M] max(offset, 0) / off_div */
+  int32_t *alloc_limit;  /* [B]    A = min(max_ctx, n_pages * P) */
+  int32_t *bonus;        /* [B]    accepted[n-1] */
+  int32_t *emb_ids;      /* [B, T] bonus, then mask_token_id */
+  int32_t *ctx_pos;      /* [B, T] c + i (RoPE positions of the context rows) */
+  int32_t *q_pos;        /* [B, T] c' + i (positions of the block's queries) */
+  int32_t *ctx_dst_page; /* [B, T] physical page of context row i, -1 if masked */
+  int32_t *ctx_dst_slot; /* [B, T] slot in that page, -1 if masked */
+  uint8_t *ctx_wmask;    /* [B, T] 1 = row i is written */
+  int32_t *blk_page;     /* [B, T] DraftBlockPlacement: page of q_pos, -1 if unplaced */
+  int32_t *blk_slot;     /* [B, T] slot of q_pos, -1 if unplaced */
+  uint8_t *blk_mask;     /* [B, T] 1 = placed (q_pos < n_pages * P on a mapped page) */
+  int32_t *ctx_len_new;  /* [B]    c' = min(c + n, A) (advertised context length) */
+  int32_t *seq_lens;     /* [B]    c' + T (kv_len of the block attention) */
+} dflash_step_outputs;
+
+/* ---------------------------------------------------------------------
+ * dflash_step_bookkeeping -- one launch for the per-step bookkeeping groups
+ * [TRT-20548 Proposal; TRT-20550 Description: "_refresh_ctx_block_tables",
+ * "gen-request prologue", "ctx_len advance", and the follow-up commit:
+ * block-table decode "clamped and divided offsets", bonus token, query and
+ * RoPE positions, destination pages / offsets / write mask, ctx_len advance
+ * with the dummy slot emptied, advertised context length, seq_lens,
+ * DraftBlockPlacement].
+ *
+ * raw_offsets     device int32, row r at raw_offsets + r*off_row_stride,
+ *                 max_pages entries (a strided view is fine); negative = no page.
+ * off_div         >= 1; decoded page = max(offset, 0) / off_div.
+ * accepted_tokens device int32, row r at accepted_tokens + r*acc_row_stride,
+ *                 block_size entries.
+ * n_accepted      device int32 [B], accepted rows n (1..T) including the bonus.
+ * ctx_len_pre     device int32 [B], context length c before the step.
+ * valid           device uint8 [B] or NULL (all live); 0 = dummy slot.
+ * A row is live when valid != 0, 1 <= n <= T and c >= 0; any other row is a
+ * dummy: n_pages = alloc_limit = ctx_len_new = seq_lens = 0, positions 0,
+ * masks 0, pages/slots -1, emb_ids and bonus = mask_token_id.  The decoded
+ * table row is written for every row.
+ * Errors: DFLASH_ERR_INVALID_ARG for null pointers, B < 0, off_div < 1,
+ * strides below the row widths; DFLASH_ERR_CUDA when the launch fails.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_step_bookkeeping(const dflash_geom *g, int B, const int32_t *raw_offsets,
+                            int64_t off_row_stride, int32_t off_div,
+                            const int32_t *accepted_tokens, int64_t acc_row_stride,
+                            const int32_t *n_accepted, const int32_t *ctx_len_pre,
+                            const uint8_t *valid, int32_t max_ctx, int32_t mask_token_id,
+                            const dflash_step_outputs *out, int32_t *dev_status,
+                            dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * dflash_ctx_workspace_bytes -- device scratch needed by dflash_ctx_kv_update
+ * for B requests (depends on the geometry and the current device's SM count).
+ * Returns 0 for an invalid geometry.
+ * ------------------------------------------------------------------- */
+DFLASH_API size_t dflash_ctx_workspace_bytes(const dflash_geom *g, int B);
+
+/* ---------------------------------------------------------------------
+ * dflash_ctx_kv_update -- the per-step context-KV update
+ * [TRT-20548 Proposal: context-KV mask, clamp, paged write, ctx_len advance;
+ * TRT-20550 Description "TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION": fc +
+ * hidden_norm + latent GEMM + RMSNorm/RoPE; TRT-13995 "per-layer cached K/V
+ * pool" (one GEMM stacked across drafter layers on the K+1 accepted rows),
+ * "fuse cross-layer k_norm" (one RMSNorm over [N, L, nkv, hd], mask
+ * multiply), "match RoPE between context and query" (one cos/sin
+ * convention)].
+ *
+ * For every request r and row i < T with write mask
+ *   w = live(r) && i < n_r && c_r + i < alloc_limit[r]
+ *       && block_table[r, (c_r+i)/P] in [0, num_pool_pages),
+ * computes  x = bf16(hidden[r, i]),  h = bf16(W_fc x),
+ *           hn = bf16(h * gamma_h / sqrt(mean(h^2) + eps_hidden)),
+ * then for every layer l (GQA, per KV head):
+ *           k = W_k[l] hn,  v = W_v[l] hn   (fp32 accumulation),
+ *           k' = RoPE(k * gamma_k[l] / sqrt(mean(k^2) + eps_k), c_r + i),
+ * and stores bf16(k'), bf16(v) at (page, slot) = (block_table[r, p/P], p%P)
+ * of layer l; (MLA) c = W_dkv[l] hn, stores bf16(RMSNorm(c[:lat]) * gamma)
+ * || bf16(RoPE(c[lat:], p)).  RoPE is rotate-half with
+ * f_j = rope_theta^(-2j/d), the angle p * f_j formed in double precision and
+ * reduced modulo 2*pi before the fp32 sin/cos.  Rows with w = 0 are not
+ * stored: every other pool entry is left bit-identical.  Finally, in place,
+ * ctx_len[r] = live(r) ? min(c_r + n_r, alloc_limit[r]) : 0.
+ *
+ * hidden       device [B, T, d_in], bf16 or fp32 per hidden_dtype.
+ * ctx_len      device int32 [B]: read as c (pre-step), overwritten with c'.
+ * alloc_limit  device int32 [B] (e.g. from dflash_step_bookkeeping).
+ * block_table  device int32 [B, max_pages] physical page ids (entry < 0 =
+ *              unmapped, the row is masked).
+ * valid        device uint8 [B] or NULL.
+ * workspace    device scratch of at least dflash_ctx_workspace_bytes(g, B)
+ *              bytes, 256-byte aligned; its contents are clobbered.
+ * Errors: DFLASH_ERR_INVALID_ARG (null / misaligned pointers, B < 0, bad
+ * dtype), DFLASH_ERR_UNSUPPORTED_GEOM (head_dim not a multiple of 8 or
+ * > 256, d_in or d_model not a multiple of 64, MLA widths other than
+ * 512 + 64), DFLASH_ERR_WORKSPACE_TOO_SMALL, DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hidden, int hidden_dtype,
+                         const int32_t *n_accepted, int32_t *ctx_len,
+                         const int32_t *alloc_limit, const int32_t *block_table,
+                         const uint8_t *valid, const dflash_weights *w, void *kv_pool,
+                         void *workspace, size_t ws_bytes, int32_t *dev_status,
+                         dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * dflash_block_kv_scatter -- write the block's own K/V (GQA) or latent rows
+ * (MLA) of one layer into the pool at the DraftBlockPlacement
+ * [TRT-20548 Proposal: "a per-layer index_put of the block latents into the
+ * pool"; TRT-20550 Description: "each layer's block latents go into the pool
+ * with one scatter kernel"].
+ *
+ * blk_k    GQA: device bf16 [B, T, nkv, head_dim]; MLA: [B, T, latent+rope].
+ * blk_v    GQA: device bf16 [B, T, nkv, head_dim]; MLA: must be NULL.
+ * blk_page, blk_slot  device int32 [B, T]; blk_mask device uint8 [B, T].
+ * Rows with blk_mask = 0 are skipped; a placed row whose page is outside the
+ * pool or slot outside [0, P) is skipped and flags DFLASH_DEV_BAD_PAGE.
+ * Errors: DFLASH_ERR_INVALID_ARG, DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_block_kv_scatter(const dflash_geom *g, int B, int layer, const void *blk_k,
+                            const void *blk_v, const int32_t *blk_page,
+                            const int32_t *blk_slot, const uint8_t *blk_mask, void *kv_pool,
+                            int32_t *dev_status, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * dflash_attention_num_segments -- the split count `num_segments = 0`
+ * resolves to for this geometry and batch (a launch heuristic that fills the
+ * GPU's SMs; it never depends on device data).
+ * dflash_attention_workspace_bytes -- scratch for dflash_block_attention with
+ * that many segments (0 = the automatic count).  0 for invalid arguments.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_attention_num_segments(const dflash_geom *g, int B, int Tq);
+DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, int Tq, int num_segments);
+
+/* ---------------------------------------------------------------------
+ * dflash_block_attention -- decode-shaped block attention of one drafter
+ * layer over the paged cache, split over KV segments, with an optional
+ * sliding window and per-head sink logits [VLLM-54092 Purpose 2 and
+ * Changes 2: 3D split-KV for small uniform q (1 bonus + N drafts), per-query-
+ * token segment buffers, the segment layout re-based on the visible window
+ * and shared by the main kernel and the reduce; sinks].
+ *
+ * For request r, query token i < Tq and head h (kv head h / (hq/nkv)):
+ *   p_i = kv_len[r] - Tq + i,
+ *   visible keys j: lo_i <= j <= hi_i with hi_i = p_i (CAUSAL_TAIL) or
+ *   kv_len[r]-1 (BLOCK_BIDIR), lo_i = window > 0 ? max(0, p_i-window+1) : 0,
+ *   s_j = scale * <q, k_j>,  M = max(max_j s_j, sink_h),
+ *   out = sum_j e^(s_j-M) v_j / (sum_j e^(s_j-M) + e^(sink_h-M))
+ * (no sink term when sinks == NULL; out = 0 when no key is visible).
+ * Key j lives at page block_table[r, j/P], slot j%P of layer `layer`.
+ * The visible span [lo_0, hi_{Tq-1}] is cut into num_segments slices of whole
+ * 128-key tiles; each (request, kv head, slice) CTA writes a partial
+ * (max, sum, weighted values) to the workspace and a second pass merges them
+ * (log-sum-exp) with the sink.
+ *
+ * GQA: q device bf16 [B, Tq, hq, head_dim]; q_rope NULL; out bf16
+ *      [B, Tq, hq, head_dim].
+ * MLA: q device bf16 [B, Tq, hq, latent] (absorbed latent query), q_rope
+ *      bf16 [B, Tq, hq, rope]; s_j = scale*(<q, c_j> + <q_rope, r_j>),
+ *      values c_j; out bf16 [B, Tq, hq, latent].
+ * kv_len      device int32 [B] (seq_lens of the bookkeeping).
+ * sinks       device fp32 [hq] or NULL.
+ * num_segments 0 = automatic, else >= 1.
+ * workspace   device scratch >= dflash_attention_workspace_bytes(...), 16-byte
+ *             aligned; clobbered.
+ * Errors: DFLASH_ERR_INVALID_ARG, DFLASH_ERR_UNSUPPORTED_GEOM (hq not a
+ * multiple of nkv, head_dim not 64 or 128, page_size not dividing 128 or a
+ * multiple of 128, Tq * hq / nkv > 128 for GQA), DFLASH_ERR_WORKSPACE_TOO_SMALL,
+ * DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq, const void *q,
+                           const void *q_rope, const void *kv_pool,
+                           const int32_t *block_table, const int32_t *kv_len, int32_t window,
+                           const float *sinks, float scale, int mask_mode, int num_segments,
+                           void *workspace, size_t ws_bytes, void *out, int32_t *dev_status,
+                           dflash_stream_t stream);
+
+/* Human-readable name of a dflash_status_code (static string). */
+DFLASH_API const char *dflash_status_string(int code);
+
+/* Library ABI version (increments when a signature changes). */
+DFLASH_API int dflash_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

@@ -1,0 +1,121 @@
+"""The C-ABI library loads and exports every symbol include/dflash.h declares;
+host-side validation rejects bad arguments before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from context_kv_update_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dflash.h")).read()
+    return re.findall(r"DFLASH_API\s+[\w\s\*]+?\b(dflash_\w+)\s*\(", src)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared())
+    for n in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
+              "dflash_block_attention", "dflash_ctx_workspace_bytes",
+              "dflash_attention_workspace_bytes", "dflash_attention_num_segments"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from context_kv_update_gb300 import _lib
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(_lib.EXPORTS)
+    # nothing else leaks out of the shared object
+    out = os.popen(f"nm -D --defined-only {_lib.LIB_PATH}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(_declared())
+
+
+def test_struct_sizes_match_header(lib):
+    from context_kv_update_gb300 import _lib
+    assert ctypes.sizeof(_lib.Geom) == 14 * 4 + 3 * 8
+    assert ctypes.sizeof(_lib.Weights) == 4 * 8
+    assert ctypes.sizeof(_lib.StepOutputs) == 15 * 8
+
+
+def _geom():
+    from context_kv_update_gb300 import inputs, make_geom
+    prob = inputs.make_problem(inputs.workload("tiny"), seed=0, with_pool=False, with_weights=False)
+    return make_geom(prob["g"])
+
+
+def test_validation_rejects_without_launching(lib):
+    from context_kv_update_gb300 import _lib
+    g = _geom()
+    G = ctypes.byref(g)
+    null = None
+    # null geometry / negative batch / bad layer / bad mask mode
+    assert lib.dflash_block_attention(None, 1, 0, 4, null, null, null, null, null, 0, null, 1.0, 0,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_block_attention(G, -1, 0, 4, null, null, null, null, null, 0, null, 1.0, 0,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_block_attention(G, 1, 5, 4, null, null, null, null, null, 0, null, 1.0, 0,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_block_attention(G, 1, 0, 4, null, null, null, null, null, 0, null, 1.0, 7,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # null buffers
+    assert lib.dflash_block_attention(G, 1, 0, 4, null, null, null, null, null, 0, null, 1.0, 0,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # B == 0 is a no-op
+    assert lib.dflash_block_attention(G, 0, 0, 4, null, null, null, null, null, 0, null, 1.0, 0,
+                                      0, null, 0, null, null, null) == _lib.DFLASH_OK
+    # misaligned q
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    assert lib.dflash_block_attention(G, 1, 0, 4, odd, null, p, p, p, 0, null, 1.0, 0, 1, p,
+                                      1 << 30, p, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.dflash_block_attention(G, 1, 0, 4, p, null, p, p, p, 0, null, 1.0, 0, 1, p, 16, p,
+                                      null, null) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    # unsupported head dim
+    g2 = _geom()
+    g2.head_dim = 96
+    assert lib.dflash_block_attention(ctypes.byref(g2), 1, 0, 4, p, null, p, p, p, 0, null, 1.0,
+                                      0, 1, p, 1 << 30, p, null,
+                                      null) == _lib.DFLASH_ERR_UNSUPPORTED_GEOM
+    # MLA requires q_rope; GQA forbids it
+    assert lib.dflash_block_attention(G, 1, 0, 4, p, p, p, p, p, 0, null, 1.0, 0, 1, p, 1 << 30, p,
+                                      null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # ctx update: bad dtype, workspace too small, missing weights
+    w = _lib.Weights(0x1000, 0x1000, 0x1000, 0x1000)
+    assert lib.dflash_ctx_kv_update(G, 1, p, 9, p, p, p, p, null, ctypes.byref(w), p, p, 1 << 30,
+                                    null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_update(G, 1, p, 0, p, p, p, p, null, ctypes.byref(w), p, p, 64, null,
+                                    null) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    w0 = _lib.Weights(0x1000, None, 0x1000, 0x1000)
+    assert lib.dflash_ctx_kv_update(G, 1, p, 0, p, p, p, p, null, ctypes.byref(w0), p, p, 1 << 30,
+                                    null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # bookkeeping: off_div < 1, stride below the row width
+    outs = _lib.StepOutputs(*([0x1000] * 15))
+    assert lib.dflash_step_bookkeeping(G, 1, p, 16, 0, p, 4, p, p, null, 100, 7,
+                                       ctypes.byref(outs), null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_step_bookkeeping(G, 1, p, 3, 1, p, 4, p, p, null, 100, 7,
+                                       ctypes.byref(outs), null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # scatter: MLA-only NULL blk_v rule, bad layer
+    assert lib.dflash_block_kv_scatter(G, 1, 0, p, null, p, p, p, p, null,
+                                       null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_block_kv_scatter(G, 1, 3, p, p, p, p, p, p, null,
+                                       null) == _lib.DFLASH_ERR_INVALID_ARG
+
+
+def test_workspace_queries(lib):
+    from context_kv_update_gb300 import _lib
+    g = _geom()
+    assert lib.dflash_ctx_workspace_bytes(ctypes.byref(g), 1) > 0
+    assert lib.dflash_attention_workspace_bytes(ctypes.byref(g), 1, 4, 3) >= 3 * 4 * 4 * (64 + 2) * 4
+    assert lib.dflash_attention_workspace_bytes(None, 1, 4, 3) == 0
+    assert lib.dflash_status_string(3) == b"workspace too small"

@@ -1,0 +1,191 @@
+"""GPU parity of the split-KV block attention against the CPU oracle's direct
+definition (abs 2e-2 + rel 1e-2 on bf16 outputs, fp32 accumulation), across
+query counts, windows, sinks, mask modes, group sizes, segment counts, ragged
+tails, NaN-poisoned workspaces and the full-size workloads."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from context_kv_update_gb300 import inputs
+from tests.gpu_helpers import assert_close, bf16_f64, bits, rel_rms_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dl():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from context_kv_update_gb300 import build
+    build.build()
+    import context_kv_update_gb300 as dl
+    dl.load()
+    return dl
+
+
+def _gqa_case(seed, kv_lens, *, hq, nkv, hd, P, Tq, L=1, extra_pages=3):
+    rng = np.random.default_rng(seed)
+    B = len(kv_lens)
+    M = max(-(-k // P) for k in kv_lens) + 2
+    NP = sum(-(-k // P) for k in kv_lens) + extra_pages
+    perm = rng.permutation(NP).astype(np.int32)
+    tbl = np.zeros((B, M), np.int32)  # decoded tables are clamped at 0
+    pos = 0
+    for r, k in enumerate(kv_lens):
+        n = -(-k // P)
+        tbl[r, :n] = perm[pos:pos + n]
+        pos += n
+    pool = inputs.f32_to_bf16_bits(rng.standard_normal((L, NP, 2, nkv, P, hd), dtype=np.float32))
+    q = inputs.f32_to_bf16_bits(rng.standard_normal((B, Tq, hq, hd), dtype=np.float32))
+    sinks = rng.standard_normal(hq).astype(np.float32)
+    g = dict(kind="gqa", L=L, D_in=64, D=64, hq=hq, nkv=nkv, hd=hd, P=P, T=Tq, max_pages=M,
+             num_pool_pages=NP, rope_theta=1e6, eps_h=1e-6, eps_k=1e-6)
+    return g, pool, tbl, q, sinks
+
+
+def _run_gpu(dl, g, layer, q, pool, tbl, kv_len, *, window=0, sinks=None, mask_mode=0, S=0,
+             poison=True, q_rope=None, scale=None, pool_d=None):
+    import torch
+    geom = dl.make_geom(g)
+    B, Tq, hq = q.shape[:3]
+    dv = g["hd"] if g["kind"] == "gqa" else g["latent"]
+    ws = torch.empty(dl.dflash_attention_workspace_bytes(geom, B, Tq, S), dtype=torch.uint8,
+                     device="cuda")
+    if poison:
+        ws.fill_(0xFF)  # every float in the workspace starts as NaN
+    out = torch.full((B, Tq, hq, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dl.dflash_block_attention(geom, layer, to_dev(q), pool_d if pool_d is not None else to_dev(pool),
+                              to_dev(tbl), to_dev(np.asarray(kv_len, np.int32)), out, ws,
+                              q_rope=None if q_rope is None else to_dev(q_rope), window=window,
+                              sinks=None if sinks is None else to_dev(sinks), scale=scale,
+                              mask_mode=mask_mode, num_segments=S, dev_status=st)
+    torch.cuda.synchronize()
+    return bf16_f64(bits(out)), int(st.item())
+
+
+@pytest.mark.parametrize("Tq", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("window,use_sinks", [(0, False), (0, True), (100, True), (1024, False)])
+def test_attention_qwen_geometry(dl, Tq, window, use_sinks):
+    kv_lens = [700 + Tq, 1, 129, 2048]
+    g, pool, tbl, q, sinks = _gqa_case(Tq * 7 + window, kv_lens, hq=32, nkv=8, hd=128, P=64, Tq=Tq)
+    s = sinks if use_sinks else None
+    ref = oracle.attention_gqa(g, 0, q, pool, tbl, np.array(kv_lens), window=window, sinks=s)
+    got, st = _run_gpu(dl, g, 0, q, pool, tbl, kv_lens, window=window, sinks=s)
+    assert_close(got, ref, f"Tq={Tq} window={window} sinks={use_sinks}")
+    assert st == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("hq,nkv,hd,P", [(4, 2, 64, 16), (24, 8, 128, 64), (12, 2, 128, 32),
+                                         (32, 2, 128, 64), (6, 1, 64, 128)])
+def test_attention_group_sizes_and_pages(dl, mode, hq, nkv, hd, P):
+    kv_lens = [5, 300, 1000]
+    Tq = 3
+    g, pool, tbl, q, sinks = _gqa_case(hq * 100 + P + mode, kv_lens, hq=hq, nkv=nkv, hd=hd, P=P,
+                                       Tq=Tq, L=2)
+    ref = oracle.attention_gqa(g, 1, q, pool, tbl, np.array(kv_lens), sinks=sinks, mask_mode=mode)
+    got, st = _run_gpu(dl, g, 1, q, pool, tbl, kv_lens, sinks=sinks, mask_mode=mode)
+    assert_close(got, ref, f"hq={hq} nkv={nkv} hd={hd} P={P} mode={mode}")
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 64, 1000])
+def test_attention_segment_counts(dl, S):
+    kv_lens = [1500, 17, 640]
+    g, pool, tbl, q, sinks = _gqa_case(S, kv_lens, hq=8, nkv=2, hd=128, P=64, Tq=4)
+    ref = oracle.attention_gqa(g, 0, q, pool, tbl, np.array(kv_lens), window=600, sinks=sinks)
+    got, _ = _run_gpu(dl, g, 0, q, pool, tbl, kv_lens, window=600, sinks=sinks, S=S)
+    assert_close(got, ref, f"S={S}")
+
+
+def test_attention_empty_and_short_contexts(dl):
+    # kv_len 0 -> all outputs 0; kv_len < Tq -> early queries see nothing (0)
+    kv_lens = [0, 2, 3]
+    g, pool, tbl, q, sinks = _gqa_case(11, [1, 2, 3], hq=4, nkv=2, hd=64, P=16, Tq=4)
+    for s in (None, sinks):
+        ref = oracle.attention_gqa(g, 0, q, pool, tbl, np.array(kv_lens), sinks=s)
+        got, _ = _run_gpu(dl, g, 0, q, pool, tbl, kv_lens, sinks=s)
+        assert_close(got, ref, "short contexts")
+        assert np.all(got[0] == 0.0)
+
+
+def test_attention_peaked_scores(dl):
+    # q aligned with single keys so the outputs are O(1): the tolerance bites
+    kv_lens = [4000]
+    g, pool, tbl, q, sinks = _gqa_case(12, kv_lens, hq=8, nkv=2, hd=128, P=64, Tq=2)
+    rng = np.random.default_rng(5)
+    for h in range(8):
+        for i in range(2):
+            j = int(rng.integers(0, 3999))
+            k = bf16_f64(pool[0, tbl[0, j // 64], 0, h // 4, j % 64])
+            q[0, i, h] = inputs.f32_to_bf16_bits((k * 0.9).astype(np.float32))
+    ref = oracle.attention_gqa(g, 0, q, pool, tbl, np.array(kv_lens))
+    got, _ = _run_gpu(dl, g, 0, q, pool, tbl, kv_lens)
+    assert_close(got, ref, "peaked")
+    assert np.max(np.abs(ref)) > 0.5
+    assert rel_rms_err(got, ref) < 1e-2
+
+
+def test_attention_kv_len_out_of_range_flags(dl):
+    kv_lens = [64]
+    g, pool, tbl, q, _ = _gqa_case(13, kv_lens, hq=4, nkv=2, hd=64, P=16, Tq=2)
+    cap = g["max_pages"] * g["P"]
+    _, st = _run_gpu(dl, g, 0, q, pool, tbl, [cap + 5])
+    assert st & 16
+
+
+# ---------------------------------------------------------- full sizes
+
+
+def test_attention_sliding_window_full_size(dl):
+    """Sliding-window drafter workload: hq=32, hkv=2, Tq=3, window 1024 + sinks,
+    kv_len 131072, page 64 (and the same read with the window off)."""
+    cfg = inputs.workload("sliding_window")
+    prob = inputs.make_problem(cfg, seed=0, with_weights=False)
+    g = prob["g"]
+    kv_len = np.array([131072], np.int32)
+    q = prob["q"][0]
+    for window in (1024, 0):
+        ref = oracle.attention_gqa(g, 0, q, prob["pool"], prob["pages"], kv_len, window=window,
+                                   sinks=prob["sinks"][0])
+        got, st = _run_gpu(dl, g, 0, q, prob["pool"], prob["pages"], kv_len, window=window,
+                           sinks=prob["sinks"][0])
+        assert_close(got, ref, f"sliding window={window}")
+        assert st == 0
+
+
+def test_attention_qwen_32k_full_size_one_layer(dl):
+    """Qwen3-8B-shaped drafter at 32K context: all 16 queries x 32 heads of a
+    layer, in the launch configuration the benchmark uses (automatic split)."""
+    prob = inputs.make_problem(inputs.workload("qwen3_8b"), seed=0, with_weights=False)
+    g = prob["g"]
+    kv_len = np.array([32768 + 16], np.int32)
+    layer = 3
+    q = prob["q"][layer]
+    ref = oracle.attention_gqa(g, layer, q, prob["pool"], prob["pages"], kv_len)
+    got, st = _run_gpu(dl, g, layer, q, prob["pool"], prob["pages"], kv_len)
+    assert_close(got, ref, "qwen 32k")
+    assert st == 0
+
+
+@pytest.mark.parametrize("ctx,mode,window", [(300, 0, 0), (4096, 0, 0), (2500, 1, 700)])
+def test_attention_mla(dl, ctx, mode, window):
+    """Absorbed-latent attention of the MLA drafter (hq = 64, one shared
+    512 + 64 latent per token)."""
+    cfg = inputs.workload("mla", ctx=[ctx])
+    prob = inputs.make_problem(cfg, seed=ctx, with_weights=False)
+    g = prob["g"]
+    kv_len = np.array([ctx + g["T"]], np.int32)
+    layer = 1
+    ql, qr = prob["q_lat"][layer], prob["q_rope"][layer]
+    sinks = prob["sinks"][layer] if mode == 1 else None
+    scale = inputs.attention_scale(g)
+    ref = oracle.attention_mla(g, layer, ql, qr, prob["pool"], prob["pages"], kv_len,
+                               window=window, sinks=sinks, scale=scale, mask_mode=mode)
+    got, st = _run_gpu(dl, g, layer, ql, prob["pool"], prob["pages"], kv_len, window=window,
+                       sinks=sinks, mask_mode=mode, q_rope=qr, scale=scale)
+    assert_close(got, ref, f"mla ctx={ctx}")
+    assert st == 0
