@@ -352,6 +352,46 @@ def run_e2e(dl, step, stream, steps):
             "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
+def run_kernel_only(args):
+    """One call of the step, launched eagerly `steps` times after `warmup`
+    launches, on the benchmark workload (used under ncu; prints its mean)."""
+    import torch
+    from context_kv_update_gb300 import build
+    build.build()
+    import context_kv_update_gb300 as dl
+    dl.load()
+    prob = inputs.make_problem(inputs.workload(WORKLOAD, ctx=[CTX]), seed=0)
+    step = Step(dl, prob)
+    step.run()
+    torch.cuda.synchronize()
+    o = step.outs
+    layer = 0
+
+    def call():
+        if args.kernel == "attention":
+            dl.dflash_block_attention(step.geom, layer, step.q[layer], step.pool, o["block_table"],
+                                      o["seq_lens"], step.attn_out[layer], step.attn_ws,
+                                      window=prob["window"], sinks=step.sinks, scale=step.scale,
+                                      dev_status=step.status)
+        else:
+            step.ctx_len.copy_(step.ctx_pre)
+            dl.dflash_ctx_kv_update(step.geom, step.hidden, step.n_acc, step.ctx_len,
+                                    o["alloc_limit"], o["block_table"], None, step.weights,
+                                    step.pool, step.ctx_ws, step.status)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        call()
+    e.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel": args.kernel, "mean_us": s.elapsed_time(e) * 1000 / args.steps,
+                      "status": int(step.status.item())}))
+
+
 # ---------------------------------------------------------- oracle (CPU)
 
 
@@ -449,6 +489,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None, choices=["attention", "update"],
+                    help="run only this call of the step, eagerly (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -461,6 +503,9 @@ def main():
         return
 
     import torch
+    if args.kernel is not None:
+        run_kernel_only(args)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, rank, world)

@@ -156,11 +156,12 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
                                   scale, mask_mode, S, ws, out, st);
   cudaError_t e;
   if (g.kind == DFLASH_KIND_GQA) {
-    attn_split_simt_kernel<4, 4><<<dim3(S, g.nkv, B), 256, 0, s>>>(p);
+    e = launch_attn_tc(p, g, s);
   } else {
     attn_split_simt_kernel<18, 16><<<dim3(S, 1, B), 256, 0, s>>>(p);
+    e = cudaGetLastError();
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   return launch_attn_merge(p, s);
 }
 

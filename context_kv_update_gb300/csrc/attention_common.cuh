@@ -74,6 +74,7 @@ inline AttnParams make_attn_params(const dflash_geom &g, int B, int layer, int T
 }
 
 cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s);
 
 // kv_len of request r, clamped to [0, M*P] (flagging out-of-range values).
 __device__ __forceinline__ int clamped_kv_len(const AttnParams &p, int r, bool report) {
@@ -100,7 +101,7 @@ __device__ __forceinline__ void row_key_range(const AttnParams &p, int kv_len, i
 }
 
 // Key range [k0, k1) of segment s of request r: the union of the block's
-// visible ranges, [lo_0, kv_len), re-based to start at its first 128-key tile
+// visible ranges, [lo_0, kv_len), re-based to start at its first key tile
 // and cut into S runs of whole tiles.
 struct SegRange {
   int kv_len, k0, k1, t0, t1;

@@ -1,0 +1,394 @@
+// attention_tc.cu -- split-KV block attention (GQA) on the 5th-generation
+// tensor cores.
+//
+// Follows vLLM PR #54092 (Purpose item 2, Changes item 2): small uniform query
+// blocks (1 bonus + N drafts) run split over KV segments with per-query-token
+// partial softmax state and a separate reduce; the segment layout is re-based
+// on the visible window; sinks join the reduce.
+//
+// One CTA = (segment s, row tile rt) x KV head x request.  Its 128 MMA rows
+// are the query rows (token i, head h) of the KV head's group (G = hq / nkv
+// heads x Tq tokens; rows past G*Tq are zero padding).  Per 64-key tile:
+//   TMA   K and V pages of the tile -> shared memory ring (`nst` stages)
+//   MMA   S = Q K^T     (M=128, N=64, K=hd)  -> TMEM S buffer (2 buffers)
+//   warps 2-5: one thread per row: mask, online max with lazy rescale (the
+//         reference max only moves when the tile max exceeds it by 2^8, so O
+//         in TMEM is rarely rescaled), P = exp2(s - m) -> bf16 -> smem
+//   MMA   O += P V      (M=128, N=hd, K=64)  -> TMEM O accumulator
+// and at the end each real row writes (m, l, O) of its segment to the
+// workspace for the merge kernel.
+//
+// Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma and owns
+// the TMEM allocation, warps 2-5 run the softmax (warp w reads TMEM lanes
+// 32*(w%4)..+31).  Every mbarrier wait is bounded; a timeout raises
+// DFLASH_DEV_WAIT_TIMEOUT and the CTA winds down without hanging.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "attention_common.cuh"
+
+namespace dflash {
+
+cudaError_t make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_elems, uint32_t box_rows, uint32_t box_cols);
+
+namespace {
+
+constexpr int kKT = kAttnTileKeys;  // 64 keys per tile
+constexpr int kRows = 128;
+constexpr int kThreadsTC = 192;
+constexpr int kSmemBudget = 210 * 1024;
+// V is the MMA's B operand stored N(=dim)-contiguous: 128-byte swizzled rows of
+// 64 dims, one row per key; next 64-dim chunk at kVChunk bytes, next 8 keys at
+// 1024 bytes.
+constexpr uint32_t kVChunk = kKT * 128;
+
+struct TcParams {
+  AttnParams a;
+  int GT, RT, box_rows, nst, chunks;
+  uint32_t q_off, p_off, kv_off, stage_bytes, k_bytes, bar_off;
+  uint32_t tmem_cols, idesc_qk, idesc_pv, v_lbo, v_sbo;
+  float scale_log2;
+};
+
+__device__ __forceinline__ uint32_t sw128_off(int row, int unit16) {
+  return static_cast<uint32_t>(row * 128 + ((unit16 ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const TcParams P) {
+  const AttnParams &p = P.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = sm + P.q_off;
+  uint8_t *sP = sm + P.p_off;
+  uint8_t *sKV = sm + P.kv_off;
+  const int nst = P.nst;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
+  uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
+  uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+  volatile int *consumed = reinterpret_cast<volatile int *>(tslot + 2);
+
+  const int s = blockIdx.x / P.RT, rt = blockIdx.x % P.RT;
+  const int kvh = blockIdx.y, r = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SegRange sr = segment_range(p, r, s);
+  const int ntiles = sr.t1 - sr.t0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&kv_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&kv_empty[i]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&s_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&s_full[1]), 1);
+    ptx::mbar_init(ptx::smem_u32(p_full), 4);
+    ptx::mbar_init(ptx::smem_u32(o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tm);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tslot), P.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle).
+  if (warp >= 2 && ntiles > 0) {
+    const int row = 32 * (warp & 3) + lane;
+    const int R = rt * kRows + row;
+    const bool real = R < P.GT;
+    const int i = real ? R / p.G : 0;
+    const int h = kvh * p.G + (real ? R % p.G : 0);
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        p.q + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.dq);
+    for (int c = 0; c < P.chunks; ++c) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 v = real ? src[c * 8 + u] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sQ + c * (kRows * 128) + sw128_off(row, u)) = v;
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  griddep_launch();
+
+  const uint32_t tm_s = tmem;          // S buffers: columns [0, 64) and [64, 128)
+  const uint32_t tm_o = tmem + 2 * kKT;  // O accumulator: hd columns
+  const int boxes = kKT / P.box_rows;
+
+  if (ntiles > 0 && warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % nst;
+        if (t >= nst &&
+            !ptx::mbar_wait(ptx::smem_u32(&kv_empty[st]), static_cast<uint32_t>(((t / nst) & 1) ^ 1),
+                            abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
+        const int kbase = (sr.t0 + t) * kKT;
+        uint8_t *stage = sKV + st * P.stage_bytes;
+        for (int b = 0; b < boxes; ++b) {
+          const int key0 = kbase + b * P.box_rows;
+          const int lp = key0 / p.P;
+          int page = 0;
+          if (lp < p.M && key0 < sr.kv_len) {
+            page = p.tbl[static_cast<int64_t>(r) * p.M + lp];
+            if (page < 0 || page >= p.NP) {
+              raise_status(p.st, DFLASH_DEV_BAD_PAGE);
+              page = 0;
+            }
+          }
+          const int slot0 = key0 - lp * p.P;
+          for (int kv = 0; kv < 2; ++kv) {
+            const long long row0 =
+                ((((static_cast<long long>(p.layer) * p.NP + page) * 2 + kv) * p.nkv + kvh) * p.P) +
+                slot0;
+            for (int c = 0; c < P.chunks; ++c) {
+              const uint32_t dst = ptx::smem_u32(stage + kv * P.k_bytes + c * kVChunk +
+                                                 b * P.box_rows * 128);
+              ptx::tma_load_2d(dst, &tm, c * 64, static_cast<int32_t>(row0),
+                               ptx::smem_u32(&kv_full[st]));
+            }
+          }
+        }
+        ++issued;
+      }
+      if (!ok) {
+        for (int t = *consumed; t < issued; ++t) {
+          volatile int dummy = 0;
+          ptx::mbar_wait(ptx::smem_u32(&kv_full[t % nst]), static_cast<uint32_t>((t / nst) & 1),
+                         &dummy);
+        }
+      }
+    }
+  } else if (ntiles > 0 && warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      bool ok = true;
+      auto issue_qk = [&](int t) -> bool {
+        const int st = t % nst;
+        if (!ptx::mbar_wait(ptx::smem_u32(&kv_full[st]), static_cast<uint32_t>((t / nst) & 1),
+                            abort_flag))
+          return false;
+        *consumed = t + 1;
+        ptx::tc_fence_after();
+        const uint32_t kb = ptx::smem_u32(sKV + st * P.stage_bytes);
+        const uint32_t qb = ptx::smem_u32(sQ);
+        for (int ks = 0; ks < P.chunks * 4; ++ks) {
+          const int c = ks >> 2, j = ks & 3;
+          ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * (kRows * 128), j),
+                        ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
+        return true;
+      };
+      ok = issue_qk(0);
+      if (ok && ntiles > 1) ok = issue_qk(1);
+      for (int t = 0; t < ntiles && ok; ++t) {
+        if (!ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const int st = t % nst;
+        const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
+        const uint32_t pb = ptx::smem_u32(sP);
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+          ptx::mma_bf16(tm_o, ptx::desc_kmajor_sw128(pb, ks),
+                        ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
+                        P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(o_done));
+        ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
+        if (t + 2 < ntiles) ok = issue_qk(t + 2);
+      }
+      if (!ok) {
+        ptx::mma_commit(ptx::smem_u32(drain));
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ softmax / epilogue
+    const int q4 = warp & 3;
+    const int row = 32 * q4 + lane;
+    const int R = rt * kRows + row;
+    const bool real = R < P.GT;
+    const int i = real ? R / p.G : 0;
+    const int h = kvh * p.G + (real ? R % p.G : 0);
+    int lo = 0, hi = -1;
+    if (real) row_key_range(p, sr.kv_len, i, &lo, &hi);
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const bool got_s = ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
+                                        static_cast<uint32_t>((t >> 1) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, got_s)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t sv[kKT];
+#pragma unroll
+      for (int c = 0; c < kKT; c += 16)
+        ptx::tmem_ld16(tm_s + lane_off + (t & 1) * kKT + c, *reinterpret_cast<uint32_t(*)[16]>(&sv[c]));
+      ptx::tmem_wait_ld();
+      const int kbase = (sr.t0 + t) * kKT;
+      const int c_lo = lo - kbase, c_hi = hi - kbase;  // visible columns [c_lo, c_hi]
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKT; ++c) {
+        const float x = (c >= c_lo && c <= c_hi) ? __uint_as_float(sv[c]) * P.scale_log2 : -INFINITY;
+        sv[c] = __float_as_uint(x);
+        tmax = fmaxf(tmax, x);
+      }
+      float corr = 1.f;
+      bool need = false;
+      if (m_ref == -INFINITY) {
+        m_ref = tmax;
+      } else if (tmax > m_ref + 8.f) {
+        corr = exp2f(m_ref - tmax);
+        m_ref = tmax;
+        need = true;
+      }
+      uint32_t pk[kKT / 2];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKT; c += 2) {
+        const float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
+        const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_ref);
+        const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_ref);
+        sum += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      l = l * corr + sum;
+      // PV of the previous tile must be done before O is rescaled and before
+      // the single P buffer is overwritten.
+      if (t > 0) {
+        const bool got_o = ptx::mbar_wait(ptx::smem_u32(o_done),
+                                          static_cast<uint32_t>((t - 1) & 1), abort_flag);
+        if (!__all_sync(0xffffffffu, got_o)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          for (int c = 0; c < p.dv; c += 16) {
+            uint32_t ov[16];
+            ptx::tmem_ld16(tm_o + lane_off + c, ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+            ptx::tmem_st16(tm_o + lane_off + c, ov);
+          }
+          ptx::tmem_wait_st();
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4 *>(sP + sw128_off(row, u)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
+    }
+    // epilogue: (m, l, O) of this segment
+    if (ntiles > 0 && ok) {
+      const bool got_o = ptx::mbar_wait(ptx::smem_u32(o_done),
+                                        static_cast<uint32_t>((ntiles - 1) & 1), abort_flag);
+      ok = __all_sync(0xffffffffu, got_o);
+      ptx::tc_fence_after();
+    }
+    const bool any = real && ok && ntiles > 0 && m_ref != -INFINITY;
+    const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
+    if (real) {
+      p.ws_m[wsi] = any ? m_ref * 0.69314718055994530942f : -INFINITY;
+      p.ws_l[wsi] = any ? l : 0.f;
+    }
+    // TMEM loads are warp-collective: the whole warp loads when any lane needs it.
+    if (__any_sync(0xffffffffu, any)) {
+      float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wsi * p.dv);
+      for (int c = 0; c < p.dv; c += 16) {
+        uint32_t ov[16];
+        ptx::tmem_ld16(tm_o + lane_off + c, ov);
+        ptx::tmem_wait_ld();
+        if (any) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            dst[(c + e) / 4] = make_float4(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1]),
+                                           __uint_as_float(ov[e + 2]), __uint_as_float(ov[e + 3]));
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) raise_status(p.st, DFLASH_DEV_WAIT_TIMEOUT);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, P.tmem_cols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s) {
+  TcParams P;
+  P.a = a;
+  const int hd = g.head_dim;
+  P.chunks = hd / 64;
+  P.GT = a.Tq * a.G;
+  P.RT = (P.GT + kRows - 1) / kRows;
+  P.box_rows = a.P < kKT ? a.P : kKT;
+  const uint32_t q_bytes = P.chunks * kRows * 128;
+  const uint32_t p_bytes = kRows * 128;
+  P.k_bytes = P.chunks * kVChunk;
+  P.stage_bytes = 2 * P.k_bytes;
+  P.q_off = 0;
+  P.p_off = q_bytes;
+  P.kv_off = q_bytes + p_bytes;
+  P.nst = std::min<int>(8, static_cast<int>((kSmemBudget - q_bytes - p_bytes) / P.stage_bytes));
+  P.bar_off = P.kv_off + P.nst * P.stage_bytes;
+  const uint32_t smem = 1024 + P.bar_off + (2 * P.nst + 6) * 8 + 16;
+  P.tmem_cols = (2 * kKT + hd) <= 256 ? 256 : 512;
+  P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
+  P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);
+  P.v_lbo = kVChunk;
+  P.v_sbo = 1024;
+  P.scale_log2 = a.scale * 1.4426950408889634f;
+
+  CUtensorMap tm;
+  const uint64_t rows = static_cast<uint64_t>(g.num_layers) * g.num_pool_pages * 2 * g.nkv *
+                        static_cast<uint64_t>(g.page_size);
+  cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
+  if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_limit(attn_tc_kernel, 227 * 1024)) != cudaSuccess) return e;
+  dim3 grid(a.S * P.RT, a.nkv, a.B);
+  attn_tc_kernel<<<grid, kThreadsTC, smem, s>>>(tm, P);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -178,6 +178,10 @@ extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, in
   const int P = g->page_size;
   if (P % 8 != 0 || !(kAttnTileKeys % P == 0 || P % kAttnTileKeys == 0))
     return DFLASH_ERR_UNSUPPORTED_GEOM;
+  // TMA row coordinates of the pool are signed 32-bit
+  const long long pool_rows = static_cast<long long>(g->num_layers) * g->num_pool_pages * P *
+                              (g->kind == DFLASH_KIND_GQA ? 2LL * g->nkv : 1LL);
+  if (pool_rows >= (1LL << 31)) return DFLASH_ERR_UNSUPPORTED_GEOM;
   if (B == 0) return DFLASH_OK;
   if (!q || !kv_pool || !block_table || !kv_len || !workspace || !out) return DFLASH_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(workspace) || !aligned16(out) ||
