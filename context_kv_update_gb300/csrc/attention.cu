@@ -99,28 +99,55 @@ __global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p
 }  // namespace
 
 // ----------------------------------------------------------- merge
-// grid (B * Tq * hq), block = dv threads.
-__global__ void attn_merge_kernel(const AttnParams p) {
+// One warp per output row (r, i, h); lane l owns dims [2l, 2l+2) of each
+// 64-dim slice.  m_s and l_s of the segments are spread over the lanes (S may
+// exceed 32), the weights e^(m_s - M) are broadcast by shuffle or re-read.
+template <int DV>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
   griddep_wait();
-  const int row = blockIdx.x;  // (r * Tq + i) * hq + h
+  constexpr int NV = DV / 64;  // float2 per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;  // (r * Tq + i) * hq + h
+  if (row >= p.B * p.Tq * p.hq) return;
   const int h = row % p.hq;
-  const int d = threadIdx.x;
   const size_t base = static_cast<size_t>(row) * p.S;
-  float M = p.sinks ? p.sinks[h] : -INFINITY;
-  for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.ws_m[base + s]);
-  float acc = 0.f, den = 0.f;
+  const float sink = p.sinks ? p.sinks[h] : -INFINITY;
+  float M = -INFINITY;
+  for (int s = lane; s < p.S; s += 32) M = fmaxf(M, p.ws_m[base + s]);
+  M = fmaxf(warp_max(M), sink);
+  float2 acc[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) acc[k] = make_float2(0.f, 0.f);
+  float den = 0.f;
   if (M != -INFINITY) {
-    den = p.sinks ? __expf(p.sinks[h] - M) : 0.f;
-    for (int s = 0; s < p.S; ++s) {
+    for (int s = lane; s < p.S; s += 32) {
       const float ms = p.ws_m[base + s];
-      if (ms == -INFINITY) continue;
-      const float w = __expf(ms - M);
-      den += w * p.ws_l[base + s];
-      if (d < p.dv) acc += w * p.ws_o[(base + s) * p.dv + d];
+      if (ms != -INFINITY) den += __expf(ms - M) * p.ws_l[base + s];
+    }
+    den = warp_sum(den) + (p.sinks ? __expf(sink - M) : 0.f);
+    const float2 *o = reinterpret_cast<const float2 *>(p.ws_o + base * DV);
+    for (int s0 = 0; s0 < p.S; s0 += 32) {
+      const int sl = s0 + lane;
+      const float msl = sl < p.S ? p.ws_m[base + sl] : -INFINITY;
+      const float wl = msl == -INFINITY ? 0.f : __expf(msl - M);
+      const int n = min(32, p.S - s0);
+      for (int j = 0; j < n; ++j) {
+        const float w = __shfl_sync(0xffffffffu, wl, j);
+        if (w == 0.f) continue;  // empty segment: its o was never written
+        const float2 *os = o + static_cast<size_t>(s0 + j) * (DV / 2);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          const float2 v = os[k * 32 + lane];
+          acc[k].x += w * v.x;
+          acc[k].y += w * v.y;
+        }
+      }
     }
   }
-  if (d < p.dv)
-    p.out[static_cast<size_t>(row) * p.dv + d] = f32_to_bf16_rn(den > 0.f ? acc / den : 0.f);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint32_t *out = reinterpret_cast<uint32_t *>(p.out + static_cast<size_t>(row) * DV);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) out[k * 32 + lane] = ptx::pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
 }
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq) {
@@ -168,14 +195,19 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
 cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(p.B * p.Tq * p.hq);
-  cfg.blockDim = dim3(p.dv);
+  cfg.gridDim = dim3((p.B * p.Tq * p.hq + 3) / 4);
+  cfg.blockDim = dim3(128);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
+  switch (p.dv) {
+    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
+    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<512>, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace dflash

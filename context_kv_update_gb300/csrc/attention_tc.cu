@@ -56,10 +56,6 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int unit16) {
   return static_cast<uint32_t>(row * 128 + ((unit16 ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
-}
-
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const TcParams P) {
   const AttnParams &p = P.a;
@@ -90,7 +86,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&s_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&s_full[1]), 1);
-    ptx::mbar_init(ptx::smem_u32(p_full), 4);
+    // one arrival per softmax warp that owns at least one real row
+    const int real_rows = min(kRows, P.GT - static_cast<int>(blockIdx.x % P.RT) * kRows);
+    ptx::mbar_init(ptx::smem_u32(p_full), static_cast<uint32_t>((real_rows + 31) / 32));
     ptx::mbar_init(ptx::smem_u32(o_done), 1);
     ptx::mbar_init(ptx::smem_u32(drain), 1);
     *abort_flag = 0;
@@ -234,6 +232,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int row = 32 * q4 + lane;
     const int R = rt * kRows + row;
     const bool real = R < P.GT;
+    // warps whose 32 rows are all padding sit the tile loop out (warp-uniform)
+    const bool warp_active = rt * kRows + 32 * q4 < P.GT;
     const int i = real ? R / p.G : 0;
     const int h = kvh * p.G + (real ? R % p.G : 0);
     int lo = 0, hi = -1;
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = 0; t < ntiles && warp_active; ++t) {
       const bool got_s = ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
                                         static_cast<uint32_t>((t >> 1) & 1), abort_flag);
       if (!__all_sync(0xffffffffu, got_s)) {
@@ -249,38 +249,51 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         break;
       }
       ptx::tc_fence_after();
-      uint32_t sv[kKT];
-#pragma unroll
-      for (int c = 0; c < kKT; c += 16)
-        ptx::tmem_ld16(tm_s + lane_off + (t & 1) * kKT + c, *reinterpret_cast<uint32_t(*)[16]>(&sv[c]));
-      ptx::tmem_wait_ld();
+      float sv[kKT];
+      static_assert(kKT == 64, "one 64-column TMEM load per tile");
+      ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT, sv);
       const int kbase = (sr.t0 + t) * kKT;
-      const int c_lo = lo - kbase, c_hi = hi - kbase;  // visible columns [c_lo, c_hi]
-      float tmax = -INFINITY;
+      if (!(lo <= kbase && hi >= kbase + kKT - 1)) {  // a tile the row sees only in part
 #pragma unroll
-      for (int c = 0; c < kKT; ++c) {
-        const float x = (c >= c_lo && c <= c_hi) ? __uint_as_float(sv[c]) * P.scale_log2 : -INFINITY;
-        sv[c] = __float_as_uint(x);
-        tmax = fmaxf(tmax, x);
+        for (int c = 0; c < kKT; ++c)
+          if (kbase + c < lo || kbase + c > hi) sv[c] = -INFINITY;
       }
+      // tile maximum of the raw scores (tree), then into the exp2 domain
+      float mx[kKT / 2];
+#pragma unroll
+      for (int c = 0; c < kKT / 2; ++c) mx[c] = fmaxf(sv[c], sv[c + kKT / 2]);
+#pragma unroll
+      for (int w = kKT / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+      const float tmax = mx[0] * P.scale_log2;
       float corr = 1.f;
       bool need = false;
       if (m_ref == -INFINITY) {
         m_ref = tmax;
       } else if (tmax > m_ref + 8.f) {
-        corr = exp2f(m_ref - tmax);
+        corr = ptx::ex2(m_ref - tmax);
         m_ref = tmax;
         need = true;
       }
       uint32_t pk[kKT / 2];
       float sum = 0.f;
+      if (m_ref != -INFINITY) {
+        const float nm = -m_ref;
 #pragma unroll
-      for (int c = 0; c < kKT; c += 2) {
-        const float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
-        const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_ref);
-        const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_ref);
-        sum += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kKT; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
+#pragma unroll
+        for (int c = 0; c < kKT / 2; ++c) pk[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
+#pragma unroll
+        for (int c = 0; c < kKT / 2; ++c) mx[c] = sv[c] + sv[c + kKT / 2];
+#pragma unroll
+        for (int w = kKT / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) mx[c] += mx[c + w];
+        sum = mx[0];
+      } else {
+#pragma unroll
+        for (int c = 0; c < kKT / 2; ++c) pk[c] = 0u;
       }
       l = l * corr + sum;
       // PV of the previous tile must be done before O is rescaled and before
@@ -296,8 +309,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (__any_sync(0xffffffffu, need)) {
           for (int c = 0; c < p.dv; c += 16) {
             uint32_t ov[16];
-            ptx::tmem_ld16(tm_o + lane_off + c, ov);
-            ptx::tmem_wait_ld();
+            ptx::tmem_ld16_sync(tm_o + lane_off + c, ov);
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
             ptx::tmem_st16(tm_o + lane_off + c, ov);
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
     }
     // epilogue: (m, l, O) of this segment
-    if (ntiles > 0 && ok) {
+    if (ntiles > 0 && ok && warp_active) {
       const bool got_o = ptx::mbar_wait(ptx::smem_u32(o_done),
                                         static_cast<uint32_t>((ntiles - 1) & 1), abort_flag);
       ok = __all_sync(0xffffffffu, got_o);
@@ -332,8 +344,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wsi * p.dv);
       for (int c = 0; c < p.dv; c += 16) {
         uint32_t ov[16];
-        ptx::tmem_ld16(tm_o + lane_off + c, ov);
-        ptx::tmem_wait_ld();
+        ptx::tmem_ld16_sync(tm_o + lane_off + c, ov);
         if (any) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
@@ -378,7 +389,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);
   P.v_lbo = kVChunk;
   P.v_sbo = 1024;
-  P.scale_log2 = a.scale * 1.4426950408889634f;
+  P.scale_log2 = a.scale * 1.4426950408889634f;  // scale > 0 (validated by the caller)
 
   CUtensorMap tm;
   const uint64_t rows = static_cast<uint64_t>(g.num_layers) * g.num_pool_pages * 2 * g.nkv *

@@ -80,21 +80,19 @@ __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, i
 
 // ----------------------------------------------------- hidden RMSNorm
 // One CTA per row: h = bf16(sum of partials), hn = bf16(h * g / rms(h)).
-__global__ void __launch_bounds__(256) hidden_norm_kernel(const GemmOut y, const uint16_t *gamma,
-                                                          uint16_t *hn, int N, int Npad, int D,
-                                                          float eps) {
+__global__ void __launch_bounds__(1024) hidden_norm_kernel(const GemmOut y, const uint16_t *gamma,
+                                                           uint16_t *hn, int D, float eps) {
   __shared__ float red[32];
+  __shared__ GemmTileTable tb;
   extern __shared__ float hbuf[];  // [D]
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
-  if (n >= N) {
-    for (int d = threadIdx.x; d < D; d += blockDim.x) hn[static_cast<size_t>(n) * D + d] = 0;
-    return;
-  }
+  const int nt = n / y.ntile, nn = n - nt * y.ntile;
+  gemm_tile_table(y, static_cast<long long>(nt) * y.mtiles, y.mtiles, &tb);
   float ss = 0.f;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const float h = bf16_to_f32(f32_to_bf16_rn(gemm_out_value(y, n, d)));
+    const float h = bf16_to_f32(f32_to_bf16_rn(gemm_table_value(y, tb, nn, d)));
     hbuf[d] = h;
     ss += h * h;
   }
@@ -145,6 +143,7 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
                                     int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float kbuf[kMaxHeadDim];
+  __shared__ GemmTileTable tb;
   griddep_wait();
   const int n = blockIdx.x;
   const int head = blockIdx.y;  // ((l * 2 + kv) * nkv + h)
@@ -165,7 +164,11 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int l = head / (2 * nkv);
   const int kv = (head / nkv) & 1;
   const int h = head % nkv;
-  float v = gemm_out_value(y, n, head * hd + d);
+  const int nt = n / y.ntile, nn = n - nt * y.ntile;
+  const int m0 = head * hd;  // first weight row of this head
+  const long long t0 = static_cast<long long>(nt) * y.mtiles + (m0 >> 7);
+  gemm_tile_table(y, t0, ((m0 + hd - 1) >> 7) - (m0 >> 7) + 1, &tb);
+  float v = gemm_table_value(y, tb, nn, (m0 & 127) + d);
   if (kv == 0) {
     const float ss = block_sum(v * v, red);
     const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
@@ -190,6 +193,7 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
                                     int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float rbuf[kMaxHeadDim];
+  __shared__ GemmTileTable tb;
   griddep_wait();
   const int n = blockIdx.x;
   const int l = blockIdx.y;
@@ -207,7 +211,11 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int r = n / m.T, i = n % m.T;
   int page, slot, pos;
   if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) return;
-  const float v = gemm_out_value(y, n, l * W + d);
+  const int nt = n / y.ntile, nn = n - nt * y.ntile;
+  const int m0 = l * W;
+  const long long t0 = static_cast<long long>(nt) * y.mtiles + (m0 >> 7);
+  gemm_tile_table(y, t0, ((m0 + W - 1) >> 7) - (m0 >> 7) + 1, &tb);
+  const float v = gemm_table_value(y, tb, nn, (m0 & 127) + d);
   const float ss = block_sum(d < lat ? v * v : 0.f, red);
   float outv;
   if (d < lat) {
@@ -260,23 +268,21 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
                        /*pdl=*/true, s)) != cudaSuccess)
     return e;
 
-  // hidden RMSNorm (also zero-fills the padded rows of hn)
+  // hidden RMSNorm
   {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(d.Npad);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3(d.N);
+    cfg.blockDim = dim3(1024);
     cfg.dynamicSmemBytes = sizeof(float) * d.D;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cfg.dynamicSmemBytes > 48 * 1024) {
-      if ((e = ensure_smem_limit(hidden_norm_kernel, 200 * 1024)) != cudaSuccess) return e;
-    }
+    if ((e = ensure_smem_limit(hidden_norm_kernel, 64 * 1024)) != cudaSuccess) return e;
     if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, y1,
-                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.N, d.Npad, d.D,
+                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
                                 static_cast<float>(g.eps_hidden))) != cudaSuccess)
       return e;
   }

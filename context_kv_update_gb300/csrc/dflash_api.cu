@@ -102,6 +102,9 @@ extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
   if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
     return DFLASH_ERR_INVALID_ARG;
   if (g->d_in % 64 != 0 || g->d_model % 64 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  // partial-sum tables of the projection hold up to 64 output tiles per row
+  // and d/64 + 1 contributors per tile
+  if (g->d_in > 8192 || g->d_model > 8192) return DFLASH_ERR_UNSUPPORTED_GEOM;
   if (g->kind == DFLASH_KIND_GQA) {
     if (g->head_dim % 8 != 0 || g->head_dim > kMaxHeadDim || g->head_dim % 2 != 0)
       return DFLASH_ERR_UNSUPPORTED_GEOM;
@@ -167,7 +170,7 @@ extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, in
     return DFLASH_ERR_INVALID_ARG;
   if (mask_mode != DFLASH_MASK_CAUSAL_TAIL && mask_mode != DFLASH_MASK_BLOCK_BIDIR)
     return DFLASH_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return DFLASH_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return DFLASH_ERR_INVALID_ARG;
   if (g->kind == DFLASH_KIND_GQA) {
     if (g->head_dim != 64 && g->head_dim != 128) return DFLASH_ERR_UNSUPPORTED_GEOM;
     if (q_rope) return DFLASH_ERR_INVALID_ARG;

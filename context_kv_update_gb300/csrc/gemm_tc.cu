@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *dst = p.part + ((c * p.maxt + local) * p.ntile) * 128 + row;
       for (int n0 = 0; n0 < p.ntile; n0 += 16) {
         uint32_t r[16];
-        ptx::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0), r);
-        ptx::tmem_wait_ld();
+        ptx::tmem_ld16_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
+                            r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
       }
@@ -220,7 +220,8 @@ Schedule make_schedule(int M, int K, int Npad) {
   s.mtiles = (M + 127) / 128;
   s.kblocks = (K + 63) / 64;
   s.units = static_cast<long long>(s.nt) * s.mtiles * s.kblocks;
-  const long long sms = device_sm_count();
+  // one CTA per SM, capped so the consumers' partial-tile tables stay bounded
+  const long long sms = std::min(device_sm_count(), 160);
   s.ctas = static_cast<int>(std::min<long long>(s.units, sms));
   const long long per = (s.units + s.ctas - 1) / s.ctas;
   s.maxt = static_cast<int>((per + s.kblocks - 1) / s.kblocks + 1);

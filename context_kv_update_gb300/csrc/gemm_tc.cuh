@@ -32,7 +32,8 @@ struct GemmOut {
   long long units;  // n_tiles * mtiles * kblocks
 };
 
-// Sum of the partials of output (n, m), in increasing CTA order.
+// Sum of the partials of output (n, m), in increasing CTA order (one-off
+// reads; bulk readers use GemmTileTable).
 __device__ __forceinline__ float gemm_out_value(const GemmOut &y, int n, int m) {
   const int nt = n / y.ntile, nn = n - nt * y.ntile;
   const long long t = static_cast<long long>(nt) * y.mtiles + (m >> 7);
@@ -46,6 +47,58 @@ __device__ __forceinline__ float gemm_out_value(const GemmOut &y, int n, int m) 
     const long long local = t - (c * U / C) / KB;
     acc += y.part[((c * y.maxt + local) * y.ntile + nn) * 128 + row];
   }
+  return acc;
+}
+
+// Shared-memory table of the partial tiles behind output tiles [t0, t0 + nt):
+// for tile k, entries base[start[k] .. start[k] + cnt[k]) are the float offsets
+// of its partial tiles in CTA order.  Built by the whole block.
+constexpr int kTableMaxTiles = 64;
+constexpr int kTableMaxEntries = kTableMaxTiles + 160 + 8;
+struct GemmTileTable {
+  long long base[kTableMaxEntries];
+  int start[kTableMaxTiles];
+  int cnt[kTableMaxTiles];
+};
+
+__device__ __forceinline__ void gemm_tile_table(const GemmOut &y, long long t0, int nt,
+                                                GemmTileTable *tb) {
+  const long long U = y.units, C = y.ctas, KB = y.kblocks;
+  for (int k = threadIdx.x; k < nt; k += blockDim.x) {
+    const long long t = t0 + k;
+    const long long c0 = ((t * KB + 1) * C - 1) / U;
+    const long long c1 = ((t + 1) * KB * C - 1) / U;
+    tb->cnt[k] = static_cast<int>(c1 - c0 + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int k = 0; k < nt; ++k) {
+      tb->start[k] = acc;
+      acc += tb->cnt[k];
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < nt; k += blockDim.x) {
+    const long long t = t0 + k;
+    const long long c0 = ((t * KB + 1) * C - 1) / U;
+    for (int j = 0; j < tb->cnt[k]; ++j) {
+      const long long c = c0 + j;
+      const long long local = t - (c * U / C) / KB;
+      tb->base[tb->start[k] + j] = (c * y.maxt + local) * y.ntile * 128;
+    }
+  }
+  __syncthreads();
+}
+
+// Value at (row nn of the N tile, column m) using a table built for tiles
+// starting at t0 (m counted from the start of tile t0).
+__device__ __forceinline__ float gemm_table_value(const GemmOut &y, const GemmTileTable &tb, int nn,
+                                                  int m) {
+  const int k = m >> 7, row = m & 127;
+  const long long off = static_cast<long long>(nn) * 128 + row;
+  float acc = 0.f;
+  for (int j = 0; j < tb.cnt[k]; ++j) acc += y.part[tb.base[tb.start[k] + j] + off];
   return acc;
 }
 
