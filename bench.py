@@ -366,13 +366,16 @@ def run_kernel_only(args):
     torch.cuda.synchronize()
     o = step.outs
     layer = 0
+    ws = torch.empty(dl.dflash_attention_workspace_bytes(step.geom, prob["B"], prob["g"]["T"],
+                                                         args.segments), dtype=torch.uint8,
+                     device="cuda")
 
     def call():
         if args.kernel == "attention":
             dl.dflash_block_attention(step.geom, layer, step.q[layer], step.pool, o["block_table"],
-                                      o["seq_lens"], step.attn_out[layer], step.attn_ws,
+                                      o["seq_lens"], step.attn_out[layer], ws,
                                       window=prob["window"], sinks=step.sinks, scale=step.scale,
-                                      dev_status=step.status)
+                                      num_segments=args.segments, dev_status=step.status)
         else:
             step.ctx_len.copy_(step.ctx_pre)
             dl.dflash_ctx_kv_update(step.geom, step.hidden, step.n_acc, step.ctx_len,
@@ -388,7 +391,8 @@ def run_kernel_only(args):
         call()
     e.record()
     torch.cuda.synchronize()
-    print(json.dumps({"kernel": args.kernel, "mean_us": s.elapsed_time(e) * 1000 / args.steps,
+    print(json.dumps({"kernel": args.kernel, "segments": args.segments,
+                      "mean_us": s.elapsed_time(e) * 1000 / args.steps,
                       "status": int(step.status.item())}))
 
 
@@ -491,6 +495,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None, choices=["attention", "update"],
                     help="run only this call of the step, eagerly (for profiler captures)")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="attention split count for --kernel attention (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

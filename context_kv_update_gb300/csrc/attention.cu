@@ -99,13 +99,16 @@ __global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p
 }  // namespace
 
 // ----------------------------------------------------------- merge
-// One warp per output row (r, i, h); lane l owns dims [2l, 2l+2) of each
-// 64-dim slice.  m_s and l_s of the segments are spread over the lanes (S may
-// exceed 32), the weights e^(m_s - M) are broadcast by shuffle or re-read.
-template <int DV>
+// One warp per output row (r, i, h).  Lane l owns vector l (and l + 32, ...)
+// of the DV values; the segments' m_s, l_s sit one per lane and their weights
+// e^(m_s - M) are broadcast by shuffle.  The partial O rows of a group of
+// segments are all loaded before any is used, so the loads overlap.
+template <typename Vec, int DV, int GROUP>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+  griddep_launch();
   griddep_wait();
-  constexpr int NV = DV / 64;  // float2 per lane
+  constexpr int VE = sizeof(Vec) / sizeof(float);  // floats per vector
+  constexpr int NV = DV / (32 * VE);                // vectors per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;  // (r * Tq + i) * hq + h
   if (row >= p.B * p.Tq * p.hq) return;
@@ -115,51 +118,72 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
   float M = -INFINITY;
   for (int s = lane; s < p.S; s += 32) M = fmaxf(M, p.ws_m[base + s]);
   M = fmaxf(warp_max(M), sink);
-  float2 acc[NV];
+  float acc[NV][VE];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) acc[k] = make_float2(0.f, 0.f);
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < VE; ++e) acc[k][e] = 0.f;
   float den = 0.f;
   if (M != -INFINITY) {
-    for (int s = lane; s < p.S; s += 32) {
-      const float ms = p.ws_m[base + s];
-      if (ms != -INFINITY) den += __expf(ms - M) * p.ws_l[base + s];
-    }
-    den = warp_sum(den) + (p.sinks ? __expf(sink - M) : 0.f);
-    const float2 *o = reinterpret_cast<const float2 *>(p.ws_o + base * DV);
+    const Vec *o = reinterpret_cast<const Vec *>(p.ws_o + base * DV);
     for (int s0 = 0; s0 < p.S; s0 += 32) {
       const int sl = s0 + lane;
       const float msl = sl < p.S ? p.ws_m[base + sl] : -INFINITY;
       const float wl = msl == -INFINITY ? 0.f : __expf(msl - M);
+      den += wl == 0.f ? 0.f : wl * p.ws_l[base + sl];
       const int n = min(32, p.S - s0);
-      for (int j = 0; j < n; ++j) {
-        const float w = __shfl_sync(0xffffffffu, wl, j);
-        if (w == 0.f) continue;  // empty segment: its o was never written
-        const float2 *os = o + static_cast<size_t>(s0 + j) * (DV / 2);
+      for (int j0 = 0; j0 < n; j0 += GROUP) {
+        Vec v[GROUP][NV];
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-          const float2 v = os[k * 32 + lane];
-          acc[k].x += w * v.x;
-          acc[k].y += w * v.y;
+        for (int jj = 0; jj < GROUP; ++jj) {
+          // empty segments (weight 0) were never written: skip their loads
+          const float w = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
+          if (j0 + jj < n && w != 0.f) {
+            const Vec *os = o + static_cast<size_t>(s0 + j0 + jj) * (DV / VE);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) v[jj][k] = os[k * 32 + lane];
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < GROUP; ++jj) {
+          const float w = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
+          if (j0 + jj < n && w != 0.f) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+              const float *f = reinterpret_cast<const float *>(&v[jj][k]);
+#pragma unroll
+              for (int e = 0; e < VE; ++e) acc[k][e] += w * f[e];
+            }
+          }
         }
       }
     }
+    den = warp_sum(den) + (p.sinks ? __expf(sink - M) : 0.f);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint32_t *out = reinterpret_cast<uint32_t *>(p.out + static_cast<size_t>(row) * DV);
 #pragma unroll
-  for (int k = 0; k < NV; ++k) out[k * 32 + lane] = ptx::pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < VE; e += 2)
+      out[(k * 32 + lane) * (VE / 2) + e / 2] =
+          ptx::pack_bf16x2(acc[k][e] * inv, acc[k][e + 1] * inv);
 }
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq) {
-  const int sms = device_sm_count();
   const int heads = (g.kind == DFLASH_KIND_GQA) ? g.nkv : 1;
-  const long long ctas = static_cast<long long>(B) * heads;
-  int S = static_cast<int>(sms / (ctas > 0 ? ctas : 1));
+  const int rows = Tq * (g.hq / (heads > 0 ? heads : 1));
+  const int row_tiles = (rows + 127) / 128;
+  // the tensor-core kernel runs two CTAs per SM when a KV head's query rows fit
+  // in half an MMA tile (compact layout), one otherwise
+  const int per_sm = (g.kind == DFLASH_KIND_GQA && rows <= 64) ? 2 : 1;
+  const long long slots = static_cast<long long>(device_sm_count()) * per_sm;
+  const long long ctas = static_cast<long long>(B) * heads * row_tiles;
+  int S = static_cast<int>(slots / (ctas > 0 ? ctas : 1));
   if (S < 1) S = 1;
   const long long max_tiles =
       (static_cast<long long>(g.max_pages) * g.page_size + kAttnTileKeys - 1) / kAttnTileKeys;
   if (S > max_tiles) S = static_cast<int>(max_tiles > 0 ? max_tiles : 1);
-  (void)Tq;
   return S;
 }
 
@@ -203,9 +227,9 @@ cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   switch (p.dv) {
-    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p);
-    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
-    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<512>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float2, 64, 16>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float4, 128, 16>, p);
+    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float4, 512, 4>, p);
     default: return cudaErrorInvalidValue;
   }
 }

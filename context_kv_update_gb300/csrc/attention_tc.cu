@@ -46,8 +46,8 @@ constexpr uint32_t kVChunk = kKT * 128;
 
 struct TcParams {
   AttnParams a;
-  int GT, RT, box_rows, nst, chunks;
-  uint32_t q_off, p_off, kv_off, stage_bytes, k_bytes, bar_off;
+  int GT, RT, box_rows, nst, chunks, compact;
+  uint32_t q_off, q_cs, p_off, kv_off, stage_bytes, k_bytes, bar_off;
   uint32_t tmem_cols, idesc_qk, idesc_pv, v_lbo, v_sbo;
   float scale_log2;
 };
@@ -76,8 +76,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int s = blockIdx.x / P.RT, rt = blockIdx.x % P.RT;
   const int kvh = blockIdx.y, r = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SegRange sr = segment_range(p, r, s);
-  const int ntiles = sr.t1 - sr.t0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
@@ -100,8 +98,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::tmem_alloc(ptx::smem_u32(tslot), P.tmem_cols);
     ptx::tmem_relinquish();
   }
-  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle).
-  if (warp >= 2 && ntiles > 0) {
+  // Everything above overlaps the previous kernel's tail; inputs are read
+  // only after it has completed.
+  griddep_wait();
+  const SegRange sr = segment_range(p, r, s);
+  const int ntiles = sr.t1 - sr.t0;
+  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle).  In the
+  // compact layout only rows 0-63 exist; the MMA's rows 64-127 read whatever
+  // follows (the next chunk or the P buffer) and their results are unused.
+  const int q_rows = P.compact ? 64 : kRows;
+  if (warp >= 2 && ntiles > 0 && 32 * (warp & 3) < q_rows) {
     const int row = 32 * (warp & 3) + lane;
     const int R = rt * kRows + row;
     const bool real = R < P.GT;
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint4 v = real ? src[c * 8 + u] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sQ + c * (kRows * 128) + sw128_off(row, u)) = v;
+        *reinterpret_cast<uint4 *>(sQ + c * P.q_cs + sw128_off(row, u)) = v;
       }
     }
     ptx::fence_proxy_async_smem();
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const uint32_t qb = ptx::smem_u32(sQ);
         for (int ks = 0; ks < P.chunks * 4; ++ks) {
           const int c = ks >> 2, j = ks & 3;
-          ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * (kRows * 128), j),
+          ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * P.q_cs, j),
                         ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk, ks > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
@@ -374,14 +380,20 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.GT = a.Tq * a.G;
   P.RT = (P.GT + kRows - 1) / kRows;
   P.box_rows = a.P < kKT ? a.P : kKT;
-  const uint32_t q_bytes = P.chunks * kRows * 128;
+  // Compact layout when the group's rows fit in 64: Q chunks of 64 rows
+  // (8 KB) back to back, small enough for two CTAs per SM.
+  P.compact = P.GT <= 64 ? 1 : 0;
+  P.q_cs = P.compact ? 64 * 128 : kRows * 128;
+  const uint32_t q_bytes = P.chunks * P.q_cs;
   const uint32_t p_bytes = kRows * 128;
   P.k_bytes = P.chunks * kVChunk;
   P.stage_bytes = 2 * P.k_bytes;
   P.q_off = 0;
   P.p_off = q_bytes;
   P.kv_off = q_bytes + p_bytes;
-  P.nst = std::min<int>(8, static_cast<int>((kSmemBudget - q_bytes - p_bytes) / P.stage_bytes));
+  const int budget = P.compact ? 110 * 1024 : kSmemBudget;
+  P.nst = std::max(2, std::min<int>(8, static_cast<int>((budget - q_bytes - p_bytes) /
+                                                          P.stage_bytes)));
   P.bar_off = P.kv_off + P.nst * P.stage_bytes;
   const uint32_t smem = 1024 + P.bar_off + (2 * P.nst + 6) * 8 + 16;
   P.tmem_cols = (2 * kKT + hd) <= 256 ? 256 : 512;
@@ -397,9 +409,17 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
   if (e != cudaSuccess) return e;
   if ((e = ensure_smem_limit(attn_tc_kernel, 227 * 1024)) != cudaSuccess) return e;
-  dim3 grid(a.S * P.RT, a.nkv, a.B);
-  attn_tc_kernel<<<grid, kThreadsTC, smem, s>>>(tm, P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(a.S * P.RT, a.nkv, a.B);
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, tm, P);
 }
 
 }  // namespace dflash

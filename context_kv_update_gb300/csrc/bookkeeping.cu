@@ -35,7 +35,9 @@ struct BkArgs {
 
 __global__ void __launch_bounds__(128) bookkeeping_kernel(const BkArgs a) {
   __shared__ int s_cnt[4];
-  __shared__ int s_scalar[6];  // ok, n, c, A, c', cap-is-huge flag unused
+  __shared__ int s_scalar[6];  // ok, n, c, A, c', bonus
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r = blockIdx.x;
   const int32_t *orow = a.off + static_cast<int64_t>(r) * a.off_stride;
 
@@ -152,8 +154,16 @@ cudaError_t launch_bookkeeping(const dflash_geom &g, int B, const int32_t *off, 
   a.P = g.page_size;
   a.o = o;
   a.st = st;
-  bookkeeping_kernel<<<B, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bookkeeping_kernel, a);
 }
 
 }  // namespace dflash

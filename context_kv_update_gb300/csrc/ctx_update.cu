@@ -70,6 +70,7 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
 __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, int row_elems,
                             int n_pad_rows, const int32_t *ctx_len, int32_t *ctx_snap, int B) {
   griddep_launch();
+  griddep_wait();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   if (tid < B) ctx_snap[tid] = ctx_len[tid];
   if (hidden_f32 == nullptr) return;
@@ -144,6 +145,7 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   __shared__ float red[32];
   __shared__ float kbuf[kMaxHeadDim];
   __shared__ GemmTileTable tb;
+  griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
   const int head = blockIdx.y;  // ((l * 2 + kv) * nkv + h)
@@ -194,6 +196,7 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
   __shared__ float red[32];
   __shared__ float rbuf[kMaxHeadDim];
   __shared__ GemmTileTable tb;
+  griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
   const int l = blockIdx.y;
@@ -256,9 +259,20 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     int blocks = f32 ? (d.Npad * d.D_in + threads - 1) / threads : 1;
     if (blocks > 4 * device_sm_count()) blocks = 4 * device_sm_count();
     if (blocks * threads < B) blocks = (B + threads - 1) / threads;
-    prep_kernel<<<blocks, threads, 0, s>>>(f32 ? static_cast<const float *>(hidden) : nullptr, W.x,
-                                           d.N * d.D_in, d.D_in, d.Npad, ctx_len, W.ctx_snap, B);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, prep_kernel,
+                                f32 ? static_cast<const float *>(hidden) : nullptr, W.x,
+                                d.N * d.D_in, d.D_in, d.Npad, ctx_len, W.ctx_snap, B)) !=
+        cudaSuccess)
+      return e;
   }
   const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
 

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) block_scatter_kernel(
     const uint4 *blk_k, const uint4 *blk_v, const int32_t *page, const int32_t *slot,
     const uint8_t *mask, uint16_t *pool, int kind, int nkv, int hd, int W, int P, int NP, int layer,
     int32_t *st) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x;  // r * T + i
   if (!mask[row]) return;
   const int pg = page[row], sl = slot[row];
@@ -49,11 +51,20 @@ cudaError_t launch_block_scatter(const dflash_geom &g, int B, int layer, const v
                                  const uint8_t *mask, void *pool, int32_t *st, cudaStream_t s) {
   const int rows = B * g.block_size;
   if (rows == 0) return cudaSuccess;
-  block_scatter_kernel<<<rows, 256, 0, s>>>(
-      static_cast<const uint4 *>(blk_k), static_cast<const uint4 *>(blk_v), page, slot, mask,
-      static_cast<uint16_t *>(pool), g.kind, g.nkv, g.head_dim, g.latent_dim + g.rope_dim,
-      g.page_size, g.num_pool_pages, layer, st);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, block_scatter_kernel, static_cast<const uint4 *>(blk_k),
+                            static_cast<const uint4 *>(blk_v), page, slot, mask,
+                            static_cast<uint16_t *>(pool), static_cast<int>(g.kind), g.nkv,
+                            g.head_dim, g.latent_dim + g.rope_dim, g.page_size, g.num_pool_pages,
+                            layer, st);
 }
 
 }  // namespace dflash
