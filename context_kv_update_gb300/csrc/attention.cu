@@ -174,10 +174,8 @@ int attention_num_segments(const dflash_geom &g, int B, int Tq) {
   const int heads = (g.kind == DFLASH_KIND_GQA) ? g.nkv : 1;
   const int rows = Tq * (g.hq / (heads > 0 ? heads : 1));
   const int row_tiles = (rows + 127) / 128;
-  // the tensor-core kernel runs two CTAs per SM when a KV head's query rows fit
-  // in half an MMA tile (compact layout), one otherwise
-  const int per_sm = (g.kind == DFLASH_KIND_GQA && rows <= 64) ? 2 : 1;
-  const long long slots = static_cast<long long>(device_sm_count()) * per_sm;
+  // the tensor-core kernel runs one CTA per SM
+  const long long slots = static_cast<long long>(device_sm_count());
   const long long ctas = static_cast<long long>(B) * heads * row_tiles;
   int S = static_cast<int>(slots / (ctas > 0 ? ctas : 1));
   if (S < 1) S = 1;

@@ -135,33 +135,53 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int boxes = kKT / P.box_rows;
 
   if (ntiles > 0 && warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      int issued = 0;
-      bool ok = true;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % nst;
-        if (t >= nst &&
-            !ptx::mbar_wait(ptx::smem_u32(&kv_empty[st]), static_cast<uint32_t>(((t / nst) & 1) ^ 1),
-                            abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
-        const int kbase = (sr.t0 + t) * kKT;
-        uint8_t *stage = sKV + st * P.stage_bytes;
-        for (int b = 0; b < boxes; ++b) {
-          const int key0 = kbase + b * P.box_rows;
-          const int lp = key0 / p.P;
-          int page = 0;
-          if (lp < p.M && key0 < sr.kv_len) {
-            page = p.tbl[static_cast<int64_t>(r) * p.M + lp];
-            if (page < 0 || page >= p.NP) {
-              raise_status(p.st, DFLASH_DEV_BAD_PAGE);
-              page = 0;
-            }
+    // ------------------------------------------------ TMA producer (warp 0)
+    // The page ids of the segment are fetched warp-wide, one batch of 32
+    // (tile, box) lookups ahead, so no table read sits between two TMA issues.
+    const int tiles_per_batch = 32 / boxes;
+    auto fetch_page = [&](int t_batch) -> int {
+      const int tt = t_batch + lane / boxes, b = lane % boxes;
+      int page = 0;
+      if (tt < ntiles) {
+        const int key0 = (sr.t0 + tt) * kKT + b * P.box_rows;
+        const int lp = key0 / p.P;
+        if (lp < p.M && key0 < sr.kv_len) {
+          page = p.tbl[static_cast<int64_t>(r) * p.M + lp];
+          if (page < 0 || page >= p.NP) {
+            raise_status(p.st, DFLASH_DEV_BAD_PAGE);
+            page = 0;
           }
-          const int slot0 = key0 - lp * p.P;
+        }
+      }
+      return page;
+    };
+    int cur = fetch_page(0);
+    int nxt = fetch_page(tiles_per_batch);
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int tb = t % tiles_per_batch;
+      if (tb == 0 && t > 0) {
+        cur = nxt;
+        nxt = fetch_page(t + tiles_per_batch);
+      }
+      const int st = t % nst;
+      bool got = true;
+      if (lane == 0 && t >= nst)
+        got = ptx::mbar_wait(ptx::smem_u32(&kv_empty[st]),
+                             static_cast<uint32_t>(((t / nst) & 1) ^ 1), abort_flag);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
+      const int kbase = (sr.t0 + t) * kKT;
+      uint8_t *stage = sKV + st * P.stage_bytes;
+      for (int b = 0; b < boxes; ++b) {
+        const int page = __shfl_sync(0xffffffffu, cur, tb * boxes + b);
+        if (lane == 0) {
+          const int key0 = kbase + b * P.box_rows;
+          const int slot0 = key0 % p.P;
           for (int kv = 0; kv < 2; ++kv) {
             const long long row0 =
                 ((((static_cast<long long>(p.layer) * p.NP + page) * 2 + kv) * p.nkv + kvh) * p.P) +
@@ -174,14 +194,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
           }
         }
-        ++issued;
       }
-      if (!ok) {
-        for (int t = *consumed; t < issued; ++t) {
-          volatile int dummy = 0;
-          ptx::mbar_wait(ptx::smem_u32(&kv_full[t % nst]), static_cast<uint32_t>((t / nst) & 1),
-                         &dummy);
-        }
+      ++issued;
+    }
+    if (!ok && lane == 0) {
+      for (int t = *consumed; t < issued; ++t) {
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(&kv_full[t % nst]), static_cast<uint32_t>((t / nst) & 1),
+                       &dummy);
       }
     }
   } else if (ntiles > 0 && warp == 1) {
@@ -381,7 +401,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.RT = (P.GT + kRows - 1) / kRows;
   P.box_rows = a.P < kKT ? a.P : kKT;
   // Compact layout when the group's rows fit in 64: Q chunks of 64 rows
-  // (8 KB) back to back, small enough for two CTAs per SM.
+  // (8 KB) back to back, leaving more room for the KV ring.
   P.compact = P.GT <= 64 ? 1 : 0;
   P.q_cs = P.compact ? 64 * 128 : kRows * 128;
   const uint32_t q_bytes = P.chunks * P.q_cs;
@@ -391,7 +411,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.q_off = 0;
   P.p_off = q_bytes;
   P.kv_off = q_bytes + p_bytes;
-  const int budget = P.compact ? 110 * 1024 : kSmemBudget;
+  const int budget = kSmemBudget;
   P.nst = std::max(2, std::min<int>(8, static_cast<int>((budget - q_bytes - p_bytes) /
                                                           P.stage_bytes)));
   P.bar_off = P.kv_off + P.nst * P.stage_bytes;
