@@ -18,10 +18,12 @@
 // and at the end each real row writes (m, l, O) of its segment to the
 // workspace for the merge kernel.
 //
-// Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma and owns
-// the TMEM allocation, warps 2-5 run the softmax (warp w reads TMEM lanes
-// 32*(w%4)..+31).  Every mbarrier wait is bounded; a timeout raises
-// DFLASH_DEV_WAIT_TIMEOUT and the CTA winds down without hanging.
+// Roles (8 warps): warp 2 issues TMA, warp 3 issues tcgen05.mma and owns the
+// TMEM allocation, warps 4-7 run the softmax (warp w reads TMEM lanes
+// 32*(w%4)..+31), warps 0-1 only join the final barrier.  A warp's SM
+// sub-partition is w % 4, so the producer and the MMA issuer never share one
+// with the softmax warps of a compact (<= 64-row) group.  Every mbarrier wait is
+// bounded; a timeout raises DFLASH_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <cuda.h>
 
 #include <algorithm>
@@ -37,8 +39,8 @@ namespace {
 
 constexpr int kKT = kAttnTileKeys;  // 64 keys per tile
 constexpr int kRows = 128;
-constexpr int kThreadsTC = 192;
-constexpr int kSmemBudget = 210 * 1024;
+constexpr int kThreadsTC = 256;
+constexpr int kSmemBudget = 225 * 1024;
 // V is the MMA's B operand stored N(=dim)-contiguous: 128-byte swizzled rows of
 // 64 dims, one row per key; next 64-dim chunk at kVChunk bytes, next 8 keys at
 // 1024 bytes.
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
   }
-  if (warp == 1) {
+  if (warp == 3) {
     ptx::tmem_alloc(ptx::smem_u32(tslot), P.tmem_cols);
     ptx::tmem_relinquish();
   }
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   // compact layout only rows 0-63 exist; the MMA's rows 64-127 read whatever
   // follows (the next chunk or the P buffer) and their results are unused.
   const int q_rows = P.compact ? 64 : kRows;
-  if (warp >= 2 && ntiles > 0 && 32 * (warp & 3) < q_rows) {
+  if (warp >= 4 && ntiles > 0 && 32 * (warp & 3) < q_rows) {
     const int row = 32 * (warp & 3) + lane;
     const int R = rt * kRows + row;
     const bool real = R < P.GT;
@@ -134,8 +136,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const uint32_t tm_o = tmem + 2 * kKT;  // O accumulator: hd columns
   const int boxes = kKT / P.box_rows;
 
-  if (ntiles > 0 && warp == 0) {
-    // ------------------------------------------------ TMA producer (warp 0)
+  if (ntiles > 0 && warp == 2) {
+    // ------------------------------------------------ TMA producer (warp 2)
     // The page ids of the segment are fetched warp-wide, one batch of 32
     // (tile, box) lookups ahead, so no table read sits between two TMA issues.
     const int tiles_per_batch = 32 / boxes;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int st = t % nst;
       bool got = true;
       if (lane == 0 && t >= nst)
-        got = ptx::mbar_wait(ptx::smem_u32(&kv_empty[st]),
+        got = ptx::mbar_spin(ptx::smem_u32(&kv_empty[st]),
                              static_cast<uint32_t>(((t / nst) & 1) ^ 1), abort_flag);
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
@@ -204,47 +206,64 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                        &dummy);
       }
     }
-  } else if (ntiles > 0 && warp == 1) {
+  } else if (ntiles > 0 && warp == 3) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ MMA issuer (warp 3)
+      // Issues S_t = Q K_t^T as soon as K_t has landed and S buffer t&1 is
+      // free (PV_{t-2} issued), and O += P_t V_t as soon as P_t is ready,
+      // whichever comes first; neither waits behind the other.
+      const uint32_t qb = ptx::smem_u32(sQ);
+      const uint32_t pb = ptx::smem_u32(sP);
+      int next_qk = 0, next_pv = 0;
       bool ok = true;
-      auto issue_qk = [&](int t) -> bool {
-        const int st = t % nst;
-        if (!ptx::mbar_wait(ptx::smem_u32(&kv_full[st]), static_cast<uint32_t>((t / nst) & 1),
-                            abort_flag))
-          return false;
-        *consumed = t + 1;
-        ptx::tc_fence_after();
-        const uint32_t kb = ptx::smem_u32(sKV + st * P.stage_bytes);
-        const uint32_t qb = ptx::smem_u32(sQ);
-        for (int ks = 0; ks < P.chunks * 4; ++ks) {
-          const int c = ks >> 2, j = ks & 3;
-          ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * P.q_cs, j),
-                        ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk, ks > 0 ? 1u : 0u);
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (next_pv < ntiles) {
+        bool progressed = false;
+        if (next_qk < ntiles && next_qk <= next_pv + 1 &&
+            ptx::mbar_test(ptx::smem_u32(&kv_full[next_qk % nst]),
+                           static_cast<uint32_t>((next_qk / nst) & 1))) {
+          const int t = next_qk;
+          *consumed = t + 1;
+          ptx::tc_fence_after();
+          const uint32_t kb = ptx::smem_u32(sKV + (t % nst) * P.stage_bytes);
+          for (int ks = 0; ks < P.chunks * 4; ++ks) {
+            const int c = ks >> 2, j = ks & 3;
+            ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * P.q_cs, j),
+                          ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk,
+                          ks > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
+          ++next_qk;
+          progressed = true;
         }
-        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
-        return true;
-      };
-      ok = issue_qk(0);
-      if (ok && ntiles > 1) ok = issue_qk(1);
-      for (int t = 0; t < ntiles && ok; ++t) {
-        if (!ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const int st = t % nst;
-        const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
-        const uint32_t pb = ptx::smem_u32(sP);
+        if (next_pv < next_qk &&
+            ptx::mbar_test(ptx::smem_u32(p_full), static_cast<uint32_t>(next_pv & 1))) {
+          const int t = next_pv;
+          ptx::tc_fence_after();
+          const int st = t % nst;
+          const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
 #pragma unroll
-        for (int ks = 0; ks < kKT / 16; ++ks) {
-          ptx::mma_bf16(tm_o, ptx::desc_kmajor_sw128(pb, ks),
-                        ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
-                        P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kKT / 16; ++ks) {
+            ptx::mma_bf16(tm_o, ptx::desc_kmajor_sw128(pb, ks),
+                          ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
+                          P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(o_done));
+          ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
+          ++next_pv;
+          progressed = true;
         }
-        ptx::mma_commit(ptx::smem_u32(o_done));
-        ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
-        if (t + 2 < ntiles) ok = issue_qk(t + 2);
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 1023u) == 0) {
+          if (idle == 1024u) t_idle = ptx::globaltimer_ns();
+          if (*abort_flag || ptx::globaltimer_ns() - t_idle > ptx::kWaitLimitNs) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
         ptx::mma_commit(ptx::smem_u32(drain));
@@ -252,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 4) {
     // ------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles && warp_active; ++t) {
-      const bool got_s = ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
+      const bool got_s = ptx::mbar_spin(ptx::smem_u32(&s_full[t & 1]),
                                         static_cast<uint32_t>((t >> 1) & 1), abort_flag);
       if (!__all_sync(0xffffffffu, got_s)) {
         ok = false;
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // PV of the previous tile must be done before O is rescaled and before
       // the single P buffer is overwritten.
       if (t > 0) {
-        const bool got_o = ptx::mbar_wait(ptx::smem_u32(o_done),
+        const bool got_o = ptx::mbar_spin(ptx::smem_u32(o_done),
                                           static_cast<uint32_t>((t - 1) & 1), abort_flag);
         if (!__all_sync(0xffffffffu, got_o)) {
           ok = false;
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   ptx::tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) raise_status(p.st, DFLASH_DEV_WAIT_TIMEOUT);
-  if (warp == 1) {
+  if (warp == 3) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, P.tmem_cols);
   }

@@ -48,6 +48,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wall-clock limit of any single on-chip wait.  Nothing in these kernels
 // legitimately waits this long; reaching it means a pipeline stage will never
 // complete, and the kernel then winds down instead of spinning forever.
@@ -61,6 +74,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
     if ((++n & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Bounded spin on phase `parity` of `bar` with the non-blocking probe (for
+// latency-critical single-thread roles that own their SM sub-partition).
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_test(bar, parity)) {
+    if ((++n & 1023u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
         *abort = 1;
