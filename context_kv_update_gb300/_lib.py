@@ -38,7 +38,8 @@ DTYPE_F32 = 1
 EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_kv_update",
            "dflash_block_kv_scatter", "dflash_attention_num_segments",
            "dflash_attention_workspace_bytes", "dflash_block_attention", "dflash_status_string",
-           "dflash_abi_version")
+           "dflash_abi_version", "dflash_block_attention_noalloc",
+           "dflash_block_attention_noalloc_max_scratch_bytes")
 
 
 class DflashError(RuntimeError):
@@ -101,6 +102,12 @@ def load():
     lib.dflash_block_attention.argtypes = [G, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
                                            vp, vp, i32, vp, ctypes.c_float, ctypes.c_int,
                                            ctypes.c_int, vp, sz, vp, vp, vp]
+    lib.dflash_block_attention_noalloc.argtypes = [G, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
+                                                   vp, vp, vp, vp, i32, vp, ctypes.c_float,
+                                                   ctypes.c_int, ctypes.c_int, vp, vp, vp]
+    lib.dflash_block_attention_noalloc.restype = ctypes.c_int
+    lib.dflash_block_attention_noalloc_max_scratch_bytes.argtypes = []
+    lib.dflash_block_attention_noalloc_max_scratch_bytes.restype = sz
     lib.dflash_status_string.argtypes = [ctypes.c_int]
     lib.dflash_status_string.restype = ctypes.c_char_p
     lib.dflash_abi_version.argtypes = []
@@ -210,3 +217,23 @@ def dflash_block_attention(geom, layer, q, kv_pool, block_table, kv_len, out, wo
         _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _ptr(dev_status), _stream(stream)))
+
+
+def dflash_block_attention_noalloc_max_scratch_bytes() -> int:
+    return int(load().dflash_block_attention_noalloc_max_scratch_bytes())
+
+
+def dflash_block_attention_noalloc(geom, layer, q, kv_pool, block_table, kv_len, out, *,
+                                   q_rope=None, window=0, sinks=None, scale=None,
+                                   mask_mode=MASK_CAUSAL_TAIL, num_segments=0, dev_status=None,
+                                   stream=None):
+    """dflash_block_attention with the library's fixed scratch (no workspace
+    argument, nothing allocated)."""
+    lib = load()
+    B, Tq = int(q.shape[0]), int(q.shape[1])
+    if scale is None:
+        scale = (1.0 / (geom.head_dim ** 0.5)) if geom.kind == KIND_GQA else 1.0 / (192 ** 0.5)
+    _check("dflash_block_attention_noalloc", lib.dflash_block_attention_noalloc(
+        ctypes.byref(geom), B, layer, Tq, _ptr(q), _ptr(q_rope), _ptr(kv_pool), _ptr(block_table),
+        _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
+        _ptr(out), _ptr(dev_status), _stream(stream)))

@@ -303,6 +303,43 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
                            void *workspace, size_t ws_bytes, void *out, int32_t *dev_status,
                            dflash_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * dflash_block_attention_noalloc -- the same computation as
+ * dflash_block_attention, for callers that cannot allocate device memory
+ * where they run it: a plugin whose host framework owns every device buffer
+ * and gives it no allocator, code running while a stream is captured into a
+ * CUDA graph (no cudaMalloc there), or a real-time loop that must not block in
+ * an allocator.  The caller passes inputs and output as for
+ * dflash_block_attention; the split-KV scratch comes from one fixed array
+ * inside the library.  The pages describe no such entry point: it is a
+ * convenience of this library, with no counterpart in the method.
+ *
+ * Scratch: a file-scope device array of
+ * dflash_block_attention_noalloc_max_scratch_bytes() bytes (32 MiB), present
+ * on every GPU that loads the library until the process exits.  A call whose
+ * dflash_attention_workspace_bytes(g, B, Tq, num_segments) exceeds it returns
+ * DFLASH_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The array is shared by
+ * every call and keeps the last call's contents; nothing in it has to start
+ * at zero.  Calls whose GPU work overlaps (other streams, graph branches) race
+ * on it: serialise them.
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  The call allocates nothing and calls no allocating routine.
+ * Errors: as dflash_block_attention, plus DFLASH_ERR_WORKSPACE_TOO_SMALL for
+ * a problem larger than the fixed scratch and DFLASH_ERR_CUDA when the
+ * address look-up fails.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_block_attention_noalloc(const dflash_geom *g, int B, int layer, int Tq,
+                                              const void *q, const void *q_rope,
+                                              const void *kv_pool, const int32_t *block_table,
+                                              const int32_t *kv_len, int32_t window,
+                                              const float *sinks, float scale, int mask_mode,
+                                              int num_segments, void *out, int32_t *dev_status,
+                                              dflash_stream_t stream);
+
+/* Size in bytes of the fixed scratch used by dflash_block_attention_noalloc. */
+DFLASH_API size_t dflash_block_attention_noalloc_max_scratch_bytes(void);
+
 /* Human-readable name of a dflash_status_code (static string). */
 DFLASH_API const char *dflash_status_string(int code);
 
