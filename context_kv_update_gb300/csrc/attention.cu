@@ -99,75 +99,69 @@ __global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p
 }  // namespace
 
 // ----------------------------------------------------------- merge
-// One warp per output row (r, i, h).  Lane l owns vector l (and l + 32, ...)
-// of the DV values; the segments' m_s, l_s sit one per lane and their weights
-// e^(m_s - M) are broadcast by shuffle.  The partial O rows of a group of
-// segments are all loaded before any is used, so the loads overlap.
-template <typename Vec, int DV, int GROUP>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+// One CTA per output row (r, i, h), one thread per value dim.  Warp 0 turns
+// the segments' (m_s, l_s) into weights e^(m_s - M) (kept in shared memory)
+// and the denominator; then every thread sums its dim over the segments with
+// all loads of a batch of 8 segments in flight before their use.
+constexpr int kMergeMaxCachedSegs = 512;
+
+template <int DV>
+__global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
+  __shared__ float s_w[kMergeMaxCachedSegs];
+  __shared__ float s_M, s_den;
   griddep_launch();
   griddep_wait();
-  constexpr int VE = sizeof(Vec) / sizeof(float);  // floats per vector
-  constexpr int NV = DV / (32 * VE);                // vectors per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;  // (r * Tq + i) * hq + h
-  if (row >= p.B * p.Tq * p.hq) return;
+  const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
+  const int d = threadIdx.x;
   const size_t base = static_cast<size_t>(row) * p.S;
-  const float sink = p.sinks ? p.sinks[h] : -INFINITY;
-  float M = -INFINITY;
-  for (int s = lane; s < p.S; s += 32) M = fmaxf(M, p.ws_m[base + s]);
-  M = fmaxf(warp_max(M), sink);
-  float acc[NV][VE];
-#pragma unroll
-  for (int k = 0; k < NV; ++k)
-#pragma unroll
-    for (int e = 0; e < VE; ++e) acc[k][e] = 0.f;
-  float den = 0.f;
-  if (M != -INFINITY) {
-    const Vec *o = reinterpret_cast<const Vec *>(p.ws_o + base * DV);
-    for (int s0 = 0; s0 < p.S; s0 += 32) {
-      const int sl = s0 + lane;
-      const float msl = sl < p.S ? p.ws_m[base + sl] : -INFINITY;
-      const float wl = msl == -INFINITY ? 0.f : __expf(msl - M);
-      den += wl == 0.f ? 0.f : wl * p.ws_l[base + sl];
-      const int n = min(32, p.S - s0);
-      for (int j0 = 0; j0 < n; j0 += GROUP) {
-        Vec v[GROUP][NV];
-#pragma unroll
-        for (int jj = 0; jj < GROUP; ++jj) {
-          // empty segments (weight 0) were never written: skip their loads
-          const float w = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
-          if (j0 + jj < n && w != 0.f) {
-            const Vec *os = o + static_cast<size_t>(s0 + j0 + jj) * (DV / VE);
-#pragma unroll
-            for (int k = 0; k < NV; ++k) v[jj][k] = os[k * 32 + lane];
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < GROUP; ++jj) {
-          const float w = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
-          if (j0 + jj < n && w != 0.f) {
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-              const float *f = reinterpret_cast<const float *>(&v[jj][k]);
-#pragma unroll
-              for (int e = 0; e < VE; ++e) acc[k][e] += w * f[e];
-            }
-          }
-        }
-      }
+  const int S = p.S;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const float sink = p.sinks ? p.sinks[h] : -INFINITY;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, p.ws_m[base + s]);
+    M = fmaxf(warp_max(M), sink);
+    float den = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float ms = p.ws_m[base + s];
+      const float w = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+      if (s < kMergeMaxCachedSegs) s_w[s] = w;
+      if (w != 0.f) den += w * p.ws_l[base + s];
     }
-    den = warp_sum(den) + (p.sinks ? __expf(sink - M) : 0.f);
+    den = warp_sum(den);
+    if (lane == 0) {
+      s_M = M;
+      s_den = den + ((p.sinks && M != -INFINITY) ? __expf(sink - M) : 0.f);
+    }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  uint32_t *out = reinterpret_cast<uint32_t *>(p.out + static_cast<size_t>(row) * DV);
+  __syncthreads();
+  const float M = s_M, den = s_den;
+  float acc = 0.f;
+  if (M != -INFINITY) {
+    const float *o = p.ws_o + base * DV + d;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float w[8], v[8];
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + j;
+        w[j] = 0.f;
+        if (s < S) {
+          if (s < kMergeMaxCachedSegs) {
+            w[j] = s_w[s];
+          } else {
+            const float ms = p.ws_m[base + s];
+            w[j] = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+          }
+        }
+        // empty segments (weight 0) were never written: their o is not read
+        v[j] = (w[j] != 0.f) ? __ldcg(o + static_cast<size_t>(s) * DV) : 0.f;
+      }
 #pragma unroll
-    for (int e = 0; e < VE; e += 2)
-      out[(k * 32 + lane) * (VE / 2) + e / 2] =
-          ptx::pack_bf16x2(acc[k][e] * inv, acc[k][e + 1] * inv);
+      for (int j = 0; j < 8; ++j) acc += w[j] * v[j];
+    }
+  }
+  p.out[static_cast<size_t>(row) * DV + d] = f32_to_bf16_rn(den > 0.f ? acc / den : 0.f);
 }
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq) {
@@ -217,17 +211,17 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
 cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3((p.B * p.Tq * p.hq + 3) / 4);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(p.B * p.Tq * p.hq);
+  cfg.blockDim = dim3(p.dv);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   switch (p.dv) {
-    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float2, 64, 16>, p);
-    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float4, 128, 16>, p);
-    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<float4, 512, 4>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
+    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<512>, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int nst = P.nst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
   uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
-  uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1, *q_full = drain + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(q_full + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *consumed = reinterpret_cast<volatile int *>(tslot + 2);
 
@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::mbar_init(ptx::smem_u32(p_full), static_cast<uint32_t>((real_rows + 31) / 32));
     ptx::mbar_init(ptx::smem_u32(o_done), 1);
     ptx::mbar_init(ptx::smem_u32(drain), 1);
+    // one arrival per warp that stores Q rows (2 in the compact layout)
+    ptx::mbar_init(ptx::smem_u32(q_full), P.compact ? 2u : 4u);
     *abort_flag = 0;
     *consumed = 0;
     ptx::fence_mbar_init();
@@ -100,14 +102,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::tmem_alloc(ptx::smem_u32(tslot), P.tmem_cols);
     ptx::tmem_relinquish();
   }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  griddep_launch();
   // Everything above overlaps the previous kernel's tail; inputs are read
   // only after it has completed.
   griddep_wait();
   const SegRange sr = segment_range(p, r, s);
   const int ntiles = sr.t1 - sr.t0;
-  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle).  In the
-  // compact layout only rows 0-63 exist; the MMA's rows 64-127 read whatever
-  // follows (the next chunk or the P buffer) and their results are unused.
+  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle), in
+  // parallel with the producer's first loads; the MMA issuer waits on q_full.
+  // In the compact layout only rows 0-63 exist; the MMA's rows 64-127 read
+  // whatever follows (the next chunk or the P buffer) and are never used.
   const int q_rows = P.compact ? 64 : kRows;
   if (warp >= 4 && ntiles > 0 && 32 * (warp & 3) < q_rows) {
     const int row = 32 * (warp & 3) + lane;
@@ -125,12 +133,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
     }
     ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(q_full));
   }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = *tslot;
-  griddep_launch();
 
   const uint32_t tm_s = tmem;          // S buffers: columns [0, 64) and [64, 128)
   const uint32_t tm_o = tmem + 2 * kKT;  // O accumulator: hd columns
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const uint32_t qb = ptx::smem_u32(sQ);
       const uint32_t pb = ptx::smem_u32(sP);
       int next_qk = 0, next_pv = 0;
-      bool ok = true;
+      bool ok = ptx::mbar_spin(ptx::smem_u32(q_full), 0u, abort_flag);
       uint32_t idle = 0;
       uint64_t t_idle = 0;
       while (next_pv < ntiles) {
@@ -434,7 +439,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.nst = std::max(2, std::min<int>(8, static_cast<int>((budget - q_bytes - p_bytes) /
                                                           P.stage_bytes)));
   P.bar_off = P.kv_off + P.nst * P.stage_bytes;
-  const uint32_t smem = 1024 + P.bar_off + (2 * P.nst + 6) * 8 + 16;
+  const uint32_t smem = 1024 + P.bar_off + (2 * P.nst + 7) * 8 + 16;
   P.tmem_cols = (2 * kKT + hd) <= 256 ? 256 : 512;
   P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);

@@ -25,10 +25,14 @@ namespace {
 // ----------------------------------------------------------- workspace map
 struct CtxWs {
   int32_t *ctx_snap;  // [B]
+  int *counters;      // stream-K tile tickets: fc tiles, then K/V tiles
+  int n_counters;
   uint16_t *x;        // [Npad, D_in] bf16 (fp32 hidden converted)
   uint16_t *hn;       // [Npad, D]    bf16
-  float *part1;       // fc partial sums
-  float *part2;       // K/V partial sums
+  float *y1;          // [N, D]     fc output
+  float *y2;          // [N, Wrows] K/V (or latent) projection
+  float *part1;       // fc partial tiles
+  float *part2;       // K/V partial tiles
   size_t bytes;
 };
 
@@ -54,6 +58,13 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
   CtxWs w;
   w.ctx_snap = reinterpret_cast<int32_t *>(p + off);
   off = align_up(off + sizeof(int32_t) * (B > 0 ? B : 1), 256);
+  w.counters = reinterpret_cast<int *>(p + off);
+  w.n_counters = gemm_num_tiles(d.D, d.Npad) + gemm_num_tiles(d.Wrows, d.Npad);
+  off = align_up(off + sizeof(int) * w.n_counters, 256);
+  w.y1 = reinterpret_cast<float *>(p + off);
+  off = align_up(off + sizeof(float) * d.Npad * d.D, 256);
+  w.y2 = reinterpret_cast<float *>(p + off);
+  off = align_up(off + sizeof(float) * static_cast<size_t>(d.Npad) * d.Wrows, 256);
   w.x = reinterpret_cast<uint16_t *>(p + off);
   off = align_up(off + sizeof(uint16_t) * d.Npad * d.D_in, 256);
   w.hn = reinterpret_cast<uint16_t *>(p + off);
@@ -68,11 +79,13 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
 
 // ------------------------------------------------------------------ prep
 __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, int row_elems,
-                            int n_pad_rows, const int32_t *ctx_len, int32_t *ctx_snap, int B) {
+                            int n_pad_rows, const int32_t *ctx_len, int32_t *ctx_snap, int B,
+                            int *counters, int n_counters) {
   griddep_launch();
   griddep_wait();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   if (tid < B) ctx_snap[tid] = ctx_len[tid];
+  for (int k = tid; k < n_counters; k += gridDim.x * blockDim.x) counters[k] = 0;
   if (hidden_f32 == nullptr) return;
   const int total = n_pad_rows * row_elems;
   for (int e = tid; e < total; e += gridDim.x * blockDim.x)
@@ -81,19 +94,17 @@ __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, i
 
 // ----------------------------------------------------- hidden RMSNorm
 // One CTA per row: h = bf16(sum of partials), hn = bf16(h * g / rms(h)).
-__global__ void __launch_bounds__(1024) hidden_norm_kernel(const GemmOut y, const uint16_t *gamma,
+__global__ void __launch_bounds__(1024) hidden_norm_kernel(const float *y, const uint16_t *gamma,
                                                            uint16_t *hn, int D, float eps) {
   __shared__ float red[32];
-  __shared__ GemmTileTable tb;
   extern __shared__ float hbuf[];  // [D]
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
-  const int nt = n / y.ntile, nn = n - nt * y.ntile;
-  gemm_tile_table(y, static_cast<long long>(nt) * y.mtiles, y.mtiles, &tb);
+  const float *row = y + static_cast<size_t>(n) * D;
   float ss = 0.f;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const float h = bf16_to_f32(f32_to_bf16_rn(gemm_table_value(y, tb, nn, d)));
+    const float h = bf16_to_f32(f32_to_bf16_rn(row[d]));
     hbuf[d] = h;
     ss += h * h;
   }
@@ -139,12 +150,11 @@ __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, in
 
 // ------------------------------------------------------ GQA epilogue
 // grid (N rows, L*2*nkv heads), block = head_dim threads.
-__global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
+__global__ void epilogue_gqa_kernel(const float *y, int ldy, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_k, uint16_t *pool, int L, int nkv,
                                     int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float kbuf[kMaxHeadDim];
-  __shared__ GemmTileTable tb;
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
@@ -166,11 +176,7 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int l = head / (2 * nkv);
   const int kv = (head / nkv) & 1;
   const int h = head % nkv;
-  const int nt = n / y.ntile, nn = n - nt * y.ntile;
-  const int m0 = head * hd;  // first weight row of this head
-  const long long t0 = static_cast<long long>(nt) * y.mtiles + (m0 >> 7);
-  gemm_tile_table(y, t0, ((m0 + hd - 1) >> 7) - (m0 >> 7) + 1, &tb);
-  float v = gemm_table_value(y, tb, nn, (m0 & 127) + d);
+  float v = y[static_cast<size_t>(n) * ldy + head * hd + d];
   if (kv == 0) {
     const float ss = block_sum(v * v, red);
     const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
@@ -190,12 +196,11 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
 
 // ------------------------------------------------------ MLA epilogue
 // grid (N rows, L), block = lat + rope threads.
-__global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
+__global__ void epilogue_mla_kernel(const float *y, int ldy, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_kv, uint16_t *pool, int L, int lat,
                                     int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float rbuf[kMaxHeadDim];
-  __shared__ GemmTileTable tb;
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
@@ -214,11 +219,7 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int r = n / m.T, i = n % m.T;
   int page, slot, pos;
   if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) return;
-  const int nt = n / y.ntile, nn = n - nt * y.ntile;
-  const int m0 = l * W;
-  const long long t0 = static_cast<long long>(nt) * y.mtiles + (m0 >> 7);
-  gemm_tile_table(y, t0, ((m0 + W - 1) >> 7) - (m0 >> 7) + 1, &tb);
-  const float v = gemm_table_value(y, tb, nn, (m0 & 127) + d);
+  const float v = y[static_cast<size_t>(n) * ldy + l * W + d];
   const float ss = block_sum(d < lat ? v * v : 0.f, red);
   float outv;
   if (d < lat) {
@@ -270,16 +271,17 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, prep_kernel,
                                 f32 ? static_cast<const float *>(hidden) : nullptr, W.x,
-                                d.N * d.D_in, d.D_in, d.Npad, ctx_len, W.ctx_snap, B)) !=
+                                d.N * d.D_in, d.D_in, d.Npad, ctx_len, W.ctx_snap, B, W.counters,
+                                W.n_counters)) !=
         cudaSuccess)
       return e;
   }
   const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
 
   // fc GEMM
-  GemmOut y1;
-  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, &y1,
-                       /*pdl=*/true, s)) != cudaSuccess)
+  const int n_fc_tiles = gemm_num_tiles(d.D, d.Npad);
+  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, W.y1,
+                       W.counters, /*pdl=*/true, s)) != cudaSuccess)
     return e;
 
   // hidden RMSNorm
@@ -295,16 +297,15 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if ((e = ensure_smem_limit(hidden_norm_kernel, 64 * 1024)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, y1,
+    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, static_cast<const float *>(W.y1),
                                 static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
                                 static_cast<float>(g.eps_hidden))) != cudaSuccess)
       return e;
   }
 
   // stacked K/V (or latent) GEMM over every layer
-  GemmOut y2;
   if ((e = launch_gemm(W.hn, d.N, d.D, static_cast<const uint16_t *>(w.w_kv), d.Wrows, W.part2,
-                       &y2, /*pdl=*/true, s)) != cudaSuccess)
+                       W.y2, W.counters + n_fc_tiles, /*pdl=*/true, s)) != cudaSuccess)
     return e;
 
   // epilogue
@@ -331,14 +332,14 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
     cfg.blockDim = dim3(g.head_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_kernel, y2, m, rf,
+    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_kernel, static_cast<const float *>(W.y2), d.Wrows, m, rf,
                            static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
                            g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else {
     fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers);
     cfg.blockDim = dim3(g.latent_dim + g.rope_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_mla_kernel, y2, m, rf,
+    e = cudaLaunchKernelEx(&cfg, epilogue_mla_kernel, static_cast<const float *>(W.y2), d.Wrows, m, rf,
                            static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
                            g.num_layers, g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k),
                            ctx_len, B);

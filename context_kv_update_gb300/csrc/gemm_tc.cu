@@ -22,8 +22,11 @@ constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
   int K, ntile, mtiles, kblocks, maxt, stages;
+  int M, N;  // output columns (weight rows) and rows (activation rows)
   long long units;
   float *part;
+  float *y;       // dense result [N, M] fp32
+  int *counters;  // one per output tile, zero between launches
   uint32_t idesc;
   uint32_t tmem_cols;
   int pdl_wait;
@@ -170,14 +173,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: TMEM -> fp32 partial tiles
+    // ---------------- epilogue: TMEM -> dense result (stream-K fixup)
+    // A tile owned by one CTA is written straight to y.  A shared tile is
+    // written as a partial; the last of its CTAs to finish (per-tile ticket)
+    // sums every partial of the tile in CTA order -- the same order whoever
+    // is last -- and writes y, then resets the ticket for the next launch.
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    int *s_last = consumed + 1;  // shared flag written by the ticket holder
     int tile_i = 0;
     for (long long t = t_first; t <= t_last; ++t, ++tile_i) {
-      if (!ptx::mbar_wait(ptx::smem_u32(acc_full), static_cast<uint32_t>(tile_i & 1), abort_flag))
-        break;
+      const bool got = ptx::mbar_wait(ptx::smem_u32(acc_full), static_cast<uint32_t>(tile_i & 1),
+                                      abort_flag);
+      if (ptx::bar_or(1, 128, !got)) break;  // the 4 epilogue warps leave together
       ptx::tc_fence_after();
+      const long long c0 = ((t * KB + 1) * C - 1) / U;
+      const long long c1 = ((t + 1) * KB * C - 1) / U;
+      const int nt = static_cast<int>(t / p.mtiles);
+      const int m = static_cast<int>(t % p.mtiles) * 128 + row;
+      const int nbase = nt * p.ntile;
+      const bool sole = (c0 == c1);
       const long long local = t - t_first;
       float *dst = p.part + ((c * p.maxt + local) * p.ntile) * 128 + row;
       for (int n0 = 0; n0 < p.ntile; n0 += 16) {
@@ -185,11 +200,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld16_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
                             r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
+        for (int j = 0; j < 16; ++j) {
+          if (sole) {
+            const int n = nbase + n0 + j;
+            if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = __uint_as_float(r[j]);
+          } else {
+            dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
+          }
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(acc_empty));
+      if (!sole) {
+        __threadfence();
+        ptx::bar_sync(1, 128);  // the 4 epilogue warps
+        if (warp == 2 && lane == 0) {
+          const int old = atomicAdd(&p.counters[t], 1);
+          *s_last = (old == static_cast<int>(c1 - c0)) ? 1 : 0;
+        }
+        ptx::bar_sync(1, 128);
+        if (*reinterpret_cast<volatile int *>(s_last)) {
+          __threadfence();
+          for (int n0 = 0; n0 < p.ntile; ++n0) {
+            const int n = nbase + n0;
+            float acc = 0.f;
+            for (long long cc = c0; cc <= c1; ++cc) {
+              const long long lc = t - (cc * U / C) / KB;
+              acc += __ldcg(p.part + ((cc * p.maxt + lc) * p.ntile + n0) * 128 + row);
+            }
+            if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = acc;
+          }
+          if (warp == 2 && lane == 0) p.counters[t] = 0;
+        }
+        ptx::bar_sync(1, 128);
+      }
     }
   }
 
@@ -267,8 +312,13 @@ size_t gemm_partial_bytes(int M, int K, int Npad) {
   return static_cast<size_t>(s.ctas) * s.maxt * s.ntile * 128 * sizeof(float);
 }
 
+int gemm_num_tiles(int M, int Npad) {
+  const int ntile = Npad <= 256 ? Npad : 256;
+  return ((Npad + ntile - 1) / ntile) * ((M + 127) / 128);
+}
+
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
-                        GemmOut *out, bool pdl, cudaStream_t st) {
+                        float *y, int *counters, bool pdl, cudaStream_t st) {
   const int Npad = static_cast<int>(align_up(static_cast<size_t>(N), 16));
   const Schedule s = make_schedule(M, K, Npad);
   CUtensorMap tmW, tmX;
@@ -284,7 +334,11 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.maxt = s.maxt;
   p.stages = s.stages;
   p.units = s.units;
+  p.M = M;
+  p.N = N;
   p.part = part;
+  p.y = y;
+  p.counters = counters;
   p.idesc = ptx::idesc_bf16_f32(128, s.ntile);
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(s.ntile)) cols <<= 1;
@@ -293,7 +347,7 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.status = nullptr;
 
   const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
-                      (2 * s.stages + 3) * 8 + 16;
+                      (2 * s.stages + 3) * 8 + 32;
   if ((e = ensure_smem_limit(gemm_tc_kernel, kMaxSmem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -305,16 +359,7 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, p)) != cudaSuccess) return e;
-
-  out->part = part;
-  out->ntile = s.ntile;
-  out->mtiles = s.mtiles;
-  out->kblocks = s.kblocks;
-  out->ctas = s.ctas;
-  out->maxt = s.maxt;
-  out->units = s.units;
-  return cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, p);
 }
 
 }  // namespace dflash
