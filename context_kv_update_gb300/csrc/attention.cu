@@ -99,67 +99,52 @@ __global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p
 }  // namespace
 
 // ----------------------------------------------------------- merge
-// One CTA per output row (r, i, h), one thread per value dim.  Warp 0 turns
-// the segments' (m_s, l_s) into weights e^(m_s - M) (kept in shared memory)
-// and the denominator; then every thread sums its dim over the segments with
-// all loads of a batch of 8 segments in flight before their use.
-constexpr int kMergeMaxCachedSegs = 512;
-
+// One CTA per output row (r, i, h), one thread per value dim.  Segments are
+// merged in batches of 16 with a running maximum (online log-sum-exp): all
+// loads of a batch (m_s, l_s and the thread's O element) are issued before any
+// is used, so a row of up to 16 segments costs one memory round trip.  The
+// sink starts the running state as an extra logit with no value.  O of an
+// empty segment (m_s = -inf) is loaded but never used (selected away), so a
+// NaN there cannot leak.
 template <int DV>
 __global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
-  __shared__ float s_w[kMergeMaxCachedSegs];
-  __shared__ float s_M, s_den;
   griddep_launch();
   griddep_wait();
+  constexpr int kBatch = 16;
   const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
   const int d = threadIdx.x;
   const size_t base = static_cast<size_t>(row) * p.S;
   const int S = p.S;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const float sink = p.sinks ? p.sinks[h] : -INFINITY;
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, p.ws_m[base + s]);
-    M = fmaxf(warp_max(M), sink);
-    float den = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float ms = p.ws_m[base + s];
-      const float w = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-      if (s < kMergeMaxCachedSegs) s_w[s] = w;
-      if (w != 0.f) den += w * p.ws_l[base + s];
-    }
-    den = warp_sum(den);
-    if (lane == 0) {
-      s_M = M;
-      s_den = den + ((p.sinks && M != -INFINITY) ? __expf(sink - M) : 0.f);
-    }
-  }
-  __syncthreads();
-  const float M = s_M, den = s_den;
+  float M = p.sinks ? p.sinks[h] : -INFINITY;
+  float den = p.sinks ? 1.f : 0.f;
   float acc = 0.f;
-  if (M != -INFINITY) {
-    const float *o = p.ws_o + base * DV + d;
-    for (int s0 = 0; s0 < S; s0 += 8) {
-      float w[8], v[8];
+  for (int s0 = 0; s0 < S; s0 += kBatch) {
+    float mv[kBatch], lv[kBatch], ov[kBatch];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int s = s0 + j;
-        w[j] = 0.f;
-        if (s < S) {
-          if (s < kMergeMaxCachedSegs) {
-            w[j] = s_w[s];
-          } else {
-            const float ms = p.ws_m[base + s];
-            w[j] = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-          }
-        }
-        // empty segments (weight 0) were never written: their o is not read
-        v[j] = (w[j] != 0.f) ? __ldcg(o + static_cast<size_t>(s) * DV) : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc += w[j] * v[j];
+    for (int j = 0; j < kBatch; ++j) {
+      const int sj = s0 + j;
+      const bool in = sj < S;
+      mv[j] = in ? __ldcg(p.ws_m + base + sj) : -INFINITY;
+      lv[j] = in ? __ldcg(p.ws_l + base + sj) : 0.f;
+      ov[j] = in ? __ldcg(p.ws_o + (base + sj) * DV + d) : 0.f;
     }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) bm = fmaxf(bm, mv[j]);
+    const float Mn = fmaxf(M, bm);
+    if (Mn == -INFINITY) continue;
+    const float sc = (M == -INFINITY) ? 0.f : __expf(M - Mn);
+    acc *= sc;
+    den *= sc;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool live = mv[j] != -INFINITY;
+      const float w = live ? __expf(mv[j] - Mn) : 0.f;
+      den += live ? w * lv[j] : 0.f;
+      acc += live ? w * ov[j] : 0.f;
+    }
+    M = Mn;
   }
   p.out[static_cast<size_t>(row) * DV + d] = f32_to_bf16_rn(den > 0.f ? acc / den : 0.f);
 }

@@ -6,8 +6,8 @@
 // tcgen05.mma (one lane), warps 2-5 drain the TMEM accumulator (warp w reads
 // TMEM lanes 32*(w%4)..+31) and write fp32 partial tiles.  A ring of `stages`
 // shared-memory slots, each one 128x64 weight tile + one NTILEx64 activation
-// tile, is guarded by full/empty mbarriers; the accumulator by acc_full /
-// acc_empty.  Every wait is bounded (ptx::mbar_wait) so a broken pipeline
+// tile, is guarded by full/empty mbarriers; two TMEM accumulators by
+// acc_full / acc_empty, so the next tile's MMAs overlap the last one's drain.  Every wait is bounded (ptx::mbar_wait) so a broken pipeline
 // winds the kernel down instead of hanging it.
 #include "gemm_tc.cuh"
 
@@ -18,6 +18,7 @@ namespace dflash {
 namespace {
 
 constexpr int kThreads = 192;
+constexpr int kMaxParts = 160;  // CTAs sharing one output tile (<= kblocks + 1)
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
@@ -29,6 +30,7 @@ struct GemmParams {
   int *counters;  // one per output tile, zero between launches
   uint32_t idesc;
   uint32_t tmem_cols;
+  int acc_cols;  // TMEM columns per accumulator buffer
   int pdl_wait;
   int32_t *status;
 };
@@ -47,9 +49,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = sA + S * abytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * bbytes);
-  uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S, *acc_empty = bars + 2 * S + 1;
-  uint64_t *drain = bars + 2 * S + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 3);
+  // two accumulator buffers: the MMA fills one while the epilogue drains the other
+  uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S, *acc_empty = bars + 2 * S + 2;
+  uint64_t *drain = bars + 2 * S + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *consumed = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -59,8 +62,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(acc_full), 1);
-    ptx::mbar_init(ptx::smem_u32(acc_empty), 4);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_u32(&acc_full[b]), 1);
+      ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 4);
+    }
     ptx::mbar_init(ptx::smem_u32(drain), 1);
     *abort_flag = 0;
     *consumed = 0;
@@ -87,50 +92,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
+      // (t, kb, m, nt) and (stage, phase) advance incrementally: no divisions
+      // in the loop.
       const uint64_t pol_w = ptx::policy_evict_first();
-      long long issued = 0;
+      struct Cursor {
+        long long t;
+        int kb, m, nt;
+      };
+      const Cursor start{t_first, static_cast<int>(u_lo - t_first * KB),
+                         static_cast<int>(t_first % p.mtiles), static_cast<int>(t_first / p.mtiles)};
+      auto advance = [&](Cursor &q) {
+        if (++q.kb == p.kblocks) {
+          q.kb = 0;
+          ++q.t;
+          if (++q.m == p.mtiles) {
+            q.m = 0;
+            ++q.nt;
+          }
+        }
+      };
+      const int total = static_cast<int>(u_hi - u_lo);
+      const int pre = std::min(S, total);
       bool ok = true;
       // Prologue: weight tiles of the first ring slots do not depend on the
       // previous kernel, so they are in flight before the dependency wait.
-      const long long pre = std::min<long long>(S, u_hi - u_lo);
-      for (long long u = u_lo; u < u_lo + pre; ++u) {
-        const long long t = u / KB;
-        const int kb = static_cast<int>(u - t * KB);
-        const int m = static_cast<int>(t % p.mtiles);
-        const int s = static_cast<int>(u - u_lo);
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), abytes + bbytes);
-        ptx::tma_load_2d_hint(ptx::smem_u32(sA + s * abytes), &tmW, kb * 64, m * 128,
-                              ptx::smem_u32(&full[s]), pol_w);
+      Cursor q = start;
+      for (int i = 0; i < pre; ++i, advance(q)) {
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[i]), abytes + bbytes);
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + i * abytes), &tmW, q.kb * 64, q.m * 128,
+                              ptx::smem_u32(&full[i]), pol_w);
       }
       if (p.pdl_wait) griddep_wait();
-      for (long long u = u_lo; u < u_lo + pre; ++u) {
-        const long long t = u / KB;
-        const int kb = static_cast<int>(u - t * KB);
-        const int nt = static_cast<int>(t / p.mtiles);
-        const int s = static_cast<int>(u - u_lo);
-        ptx::tma_load_2d(ptx::smem_u32(sB + s * bbytes), &tmX, kb * 64, nt * p.ntile,
-                         ptx::smem_u32(&full[s]));
-      }
-      issued = pre;
-      for (long long u = u_lo + pre; u < u_hi; ++u) {
-        const long long it = u - u_lo;
-        const int s = static_cast<int>(it % S);
-        const uint32_t ph = static_cast<uint32_t>((it / S) & 1);
-        if (!ptx::mbar_wait(ptx::smem_u32(&empty[s]), ph ^ 1u, abort_flag)) { ok = false; break; }
-        const long long t = u / KB;
-        const int kb = static_cast<int>(u - t * KB);
-        const int m = static_cast<int>(t % p.mtiles);
-        const int nt = static_cast<int>(t / p.mtiles);
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[s]), abytes + bbytes);
-        ptx::tma_load_2d_hint(ptx::smem_u32(sA + s * abytes), &tmW, kb * 64, m * 128,
-                              ptx::smem_u32(&full[s]), pol_w);
-        ptx::tma_load_2d(ptx::smem_u32(sB + s * bbytes), &tmX, kb * 64, nt * p.ntile,
-                         ptx::smem_u32(&full[s]));
+      q = start;
+      for (int i = 0; i < pre; ++i, advance(q))
+        ptx::tma_load_2d(ptx::smem_u32(sB + i * bbytes), &tmX, q.kb * 64, q.nt * p.ntile,
+                         ptx::smem_u32(&full[i]));
+      int issued = pre;
+      int st = pre % S;
+      uint32_t ph = (pre / S) & 1;
+      for (int i = pre; i < total; ++i, advance(q)) {
+        if (!ptx::mbar_spin(ptx::smem_u32(&empty[st]), ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[st]), abytes + bbytes);
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + st * abytes), &tmW, q.kb * 64, q.m * 128,
+                              ptx::smem_u32(&full[st]), pol_w);
+        ptx::tma_load_2d(ptx::smem_u32(sB + st * bbytes), &tmX, q.kb * 64, q.nt * p.ntile,
+                         ptx::smem_u32(&full[st]));
         ++issued;
+        if (++st == S) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
       if (!ok) {
         // wind down: let the copies already issued land before the CTA exits
-        for (long long it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
+        for (int it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
           volatile int dummy = 0;
           ptx::mbar_wait(ptx::smem_u32(&full[it % S]), static_cast<uint32_t>((it / S) & 1), &dummy);
         }
@@ -139,31 +157,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      long long it = 0;
+      int it = 0, s = 0;
+      uint32_t ph = 0;
       int tile_i = 0;
       bool ok = true;
       for (long long t = t_first; t <= t_last && ok; ++t, ++tile_i) {
         const long long ua = std::max(u_lo, t * KB), ub = std::min(u_hi, (t + 1) * KB);
-        if (!ptx::mbar_wait(ptx::smem_u32(acc_empty), static_cast<uint32_t>(tile_i & 1) ^ 1u,
-                            abort_flag)) { ok = false; break; }
+        const int ab = tile_i & 1;
+        const uint32_t acc = tmem + static_cast<uint32_t>(ab * p.acc_cols);
+        if (!ptx::mbar_spin(ptx::smem_u32(&acc_empty[ab]),
+                            static_cast<uint32_t>((tile_i >> 1) & 1) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
         for (long long u = ua; u < ub; ++u, ++it) {
-          const int s = static_cast<int>(it % S);
-          const uint32_t ph = static_cast<uint32_t>((it / S) & 1);
-          if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), ph, abort_flag)) { ok = false; break; }
+          if (!ptx::mbar_spin(ptx::smem_u32(&full[s]), ph, abort_flag)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_base = ptx::smem_u32(sA + s * abytes);
           const uint32_t b_base = ptx::smem_u32(sB + s * bbytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            ptx::mma_bf16(tmem, ptx::desc_kmajor_sw128(a_base, k), ptx::desc_kmajor_sw128(b_base, k),
+            ptx::mma_bf16(acc, ptx::desc_kmajor_sw128(a_base, k), ptx::desc_kmajor_sw128(b_base, k),
                           p.idesc, (u > ua || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(ptx::smem_u32(&empty[s]));
-          *reinterpret_cast<volatile int *>(consumed) = static_cast<int>(it + 1);
+          *reinterpret_cast<volatile int *>(consumed) = it + 1;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
-        ptx::mma_commit(ptx::smem_u32(acc_full));
+        ptx::mma_commit(ptx::smem_u32(&acc_full[ab]));
       }
       if (!ok) {
         // make sure no MMA is still reading shared memory / writing TMEM
@@ -181,10 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     int *s_last = consumed + 1;  // shared flag written by the ticket holder
+    long long *s_base = reinterpret_cast<long long *>(consumed + 4);  // 8-byte aligned
     int tile_i = 0;
     for (long long t = t_first; t <= t_last; ++t, ++tile_i) {
-      const bool got = ptx::mbar_wait(ptx::smem_u32(acc_full), static_cast<uint32_t>(tile_i & 1),
-                                      abort_flag);
+      const int ab = tile_i & 1;
+      const uint32_t acc = tmem + static_cast<uint32_t>(ab * p.acc_cols);
+      const bool got = ptx::mbar_wait(ptx::smem_u32(&acc_full[ab]),
+                                      static_cast<uint32_t>((tile_i >> 1) & 1), abort_flag);
       if (ptx::bar_or(1, 128, !got)) break;  // the 4 epilogue warps leave together
       ptx::tc_fence_after();
       const long long c0 = ((t * KB + 1) * C - 1) / U;
@@ -197,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *dst = p.part + ((c * p.maxt + local) * p.ntile) * 128 + row;
       for (int n0 = 0; n0 < p.ntile; n0 += 16) {
         uint32_t r[16];
-        ptx::tmem_ld16_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
+        ptx::tmem_ld16_sync(acc + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
                             r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -211,24 +240,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(acc_empty));
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acc_empty[ab]));
       if (!sole) {
-        __threadfence();
-        ptx::bar_sync(1, 128);  // the 4 epilogue warps
+        ptx::bar_sync(1, 128);  // the 4 epilogue warps' partial stores are done
         if (warp == 2 && lane == 0) {
+          // one release fence covers the whole CTA's stores (ordered by the
+          // barrier above) before the ticket is taken
+          __threadfence();
           const int old = atomicAdd(&p.counters[t], 1);
           *s_last = (old == static_cast<int>(c1 - c0)) ? 1 : 0;
         }
         ptx::bar_sync(1, 128);
         if (*reinterpret_cast<volatile int *>(s_last)) {
           __threadfence();
+          // partial-tile offsets of the tile's CTAs, once per tile
+          const int cnt = static_cast<int>(c1 - c0 + 1);
+          for (int j = threadIdx.x - 64; j < cnt; j += 128) {
+            const long long cc = c0 + j;
+            s_base[j] = (cc * p.maxt + (t - (cc * U / C) / KB)) * p.ntile * 128;
+          }
+          ptx::bar_sync(1, 128);
           for (int n0 = 0; n0 < p.ntile; ++n0) {
             const int n = nbase + n0;
+            const long long off = static_cast<long long>(n0) * 128 + row;
             float acc = 0.f;
-            for (long long cc = c0; cc <= c1; ++cc) {
-              const long long lc = t - (cc * U / C) / KB;
-              acc += __ldcg(p.part + ((cc * p.maxt + lc) * p.ntile + n0) * 128 + row);
-            }
+            for (int j = 0; j < cnt; ++j) acc += __ldcg(p.part + s_base[j] + off);
             if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = acc;
           }
           if (warp == 2 && lane == 0) p.counters[t] = 0;
@@ -342,12 +378,13 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.idesc = ptx::idesc_bf16_f32(128, s.ntile);
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(s.ntile)) cols <<= 1;
-  p.tmem_cols = cols;
+  p.acc_cols = static_cast<int>(cols);
+  p.tmem_cols = 2 * cols;
   p.pdl_wait = 1;
   p.status = nullptr;
 
   const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
-                      (2 * s.stages + 3) * 8 + 32;
+                      (2 * s.stages + 5) * 8 + 32 + kMaxParts * 8;
   if ((e = ensure_smem_limit(gemm_tc_kernel, kMaxSmem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
