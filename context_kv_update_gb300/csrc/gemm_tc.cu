@@ -260,12 +260,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_base[j] = (cc * p.maxt + (t - (cc * U / C) / KB)) * p.ntile * 128;
           }
           ptx::bar_sync(1, 128);
-          for (int n0 = 0; n0 < p.ntile; ++n0) {
-            const int n = nbase + n0;
-            const long long off = static_cast<long long>(n0) * 128 + row;
-            float acc = 0.f;
-            for (int j = 0; j < cnt; ++j) acc += __ldcg(p.part + s_base[j] + off);
-            if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = acc;
+          // 16 rows at a time: the 16 loads of one partial tile are independent
+          // and in flight together; partials are added in CTA order
+          for (int n0 = 0; n0 < p.ntile; n0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+            for (int j = 0; j < cnt; ++j) {
+              const float *src = p.part + s_base[j] + static_cast<long long>(n0) * 128 + row;
+              float v[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[k] = __ldcg(src + k * 128);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) acc[k] += v[k];
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int n = nbase + n0 + k;
+              if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = acc[k];
+            }
           }
           if (warp == 2 && lane == 0) p.counters[t] = 0;
         }
