@@ -207,6 +207,16 @@ def make_events(n_layers, count):
             for _ in range(count)]
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's figure: every rank passes its own, all get the max."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world):
     import torch
     from context_kv_update_gb300 import build
@@ -270,11 +280,7 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     ms_total = start.elapsed_time(end)
-    ms_step = ms_total / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / args.steps, world, "cuda")
 
     # per-launch attention duration over the last replayed chunk
     attn_ms = None

@@ -96,7 +96,8 @@ typedef struct dflash_geom {
   int32_t d_model;         /* fc output width = drafter hidden size */
   int32_t hq;              /* query heads */
   int32_t nkv;             /* KV heads (GQA); 1 for MLA */
-  int32_t head_dim;        /* GQA head dim (64 or 128) */
+  int32_t head_dim;        /* GQA head dim: even multiple of 8 up to 256 for the
+                              update, 64 or 128 for the attention */
   int32_t latent_dim;      /* MLA latent width (512) */
   int32_t rope_dim;        /* MLA rotated width (64) */
   int32_t page_size;       /* P: tokens per page */
@@ -277,7 +278,8 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * (no sink term when sinks == NULL; out = 0 when no key is visible).
  * Key j lives at page block_table[r, j/P], slot j%P of layer `layer`.
  * The visible span [lo_0, hi_{Tq-1}] is cut into num_segments slices of whole
- * 128-key tiles; each (request, kv head, slice) CTA writes a partial
+ * 64-key tiles; each (request, kv head, slice) CTA -- one per 128 query rows
+ * of the kv head's group, rows being (token, head) pairs -- writes a partial
  * (max, sum, weighted values) to the workspace and a second pass merges them
  * (log-sum-exp) with the sink.
  *
@@ -291,10 +293,11 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * num_segments 0 = automatic, else >= 1.
  * workspace   device scratch >= dflash_attention_workspace_bytes(...), 16-byte
  *             aligned; clobbered.
- * Errors: DFLASH_ERR_INVALID_ARG, DFLASH_ERR_UNSUPPORTED_GEOM (hq not a
- * multiple of nkv, head_dim not 64 or 128, page_size not dividing 128 or a
- * multiple of 128, Tq * hq / nkv > 128 for GQA), DFLASH_ERR_WORKSPACE_TOO_SMALL,
- * DFLASH_ERR_CUDA.
+ * Errors: DFLASH_ERR_INVALID_ARG (also: scale not finite and > 0, window < 0,
+ * unknown mask_mode, a pointer not 16-byte aligned), DFLASH_ERR_UNSUPPORTED_GEOM
+ * (hq not a multiple of nkv, GQA head_dim not 64 or 128, MLA dims not 512 + 64,
+ * page_size not a multiple of 8 that divides 64 or is a multiple of 64, pool
+ * rows >= 2^31), DFLASH_ERR_WORKSPACE_TOO_SMALL, DFLASH_ERR_CUDA.
  * ------------------------------------------------------------------- */
 DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq, const void *q,
                            const void *q_rope, const void *kv_pool,
