@@ -10,20 +10,33 @@
 // are the query rows (token i, head h) of the KV head's group (G = hq / nkv
 // heads x Tq tokens; rows past G*Tq are zero padding).  Per 64-key tile:
 //   TMA   K and V pages of the tile -> shared memory ring (`nst` stages)
-//   MMA   S = Q K^T     (M=128, N=64, K=hd)  -> TMEM S buffer (2 buffers)
-//   warps 2-5: one thread per row: mask, online max with lazy rescale (the
-//         reference max only moves when the tile max exceeds it by 2^8, so O
-//         in TMEM is rarely rescaled), P = exp2(s - m) -> bf16 -> smem
-//   MMA   O += P V      (M=128, N=hd, K=64)  -> TMEM O accumulator
+//   MMA   S = Q K^T     (M=128, N=64, K=hd; Q from TMEM) -> TMEM S (2 buffers)
+//   softmax warps: mask, online max with lazy rescale (the reference max only
+//         moves when the tile max exceeds it by 2^8, so O in TMEM is rarely
+//         rescaled), P = exp2(s - m) -> bf16 -> TMEM
+//   MMA   O += P V      (M=128, N=hd, K=64; P from TMEM) -> TMEM O
 // and at the end each real row writes (m, l, O) of its segment to the
-// workspace for the merge kernel.
+// workspace for the merge kernel.  Both MMAs take their A operand (Q, P) from
+// tensor memory: with A in shared memory the tensor pipe spends most of its
+// time re-reading Q (a 64-key QK costs about as much as a 128-key one), and
+// keeping P out of shared memory also drops a store, a proxy fence and 16 KB
+// of shared memory per tile; the freed space deepens the KV ring.
 //
 // Roles (8 warps): warp 2 issues TMA, warp 3 issues tcgen05.mma and owns the
-// TMEM allocation, warps 4-7 run the softmax (warp w reads TMEM lanes
-// 32*(w%4)..+31), warps 0-1 only join the final barrier.  A warp's SM
-// sub-partition is w % 4, so the producer and the MMA issuer never share one
-// with the softmax warps of a compact (<= 64-row) group.  Every mbarrier wait is
-// bounded; a timeout raises DFLASH_DEV_WAIT_TIMEOUT and the CTA winds down.
+// TMEM allocation, warps 4-7 run the softmax (warp w reads and writes TMEM
+// lanes 32*(w%4)..+31, i.e. runs on SM sub-partition w%4), warps 0-1 only join
+// the final barrier.  When the group has at most 64 query rows (the decode
+// case: a 16-token block times a few heads per KV head), those rows are
+// loaded twice, as MMA rows r and r + 64: the tensor core then hands all four
+// sub-partitions a copy of the scores and each softmax warp takes half of a
+// row's 64 key columns, so the exp2 work spreads over all four SFU pipes
+// instead of two.  Row r's P then carries its first 32 keys (zeros after) and
+// row r + 64's its last 32 (zeros before), so O rows r and r + 64 hold the two
+// halves of the row's sum, added in the epilogue.
+//
+// Every wait is an mbarrier try_wait, which suspends the thread in hardware
+// rather than polling shared memory, and is bounded: a timeout raises
+// DFLASH_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <cuda.h>
 
 #include <algorithm>
@@ -40,23 +53,26 @@ namespace {
 constexpr int kKT = kAttnTileKeys;  // 64 keys per tile
 constexpr int kRows = 128;
 constexpr int kThreadsTC = 256;
-constexpr int kSmemBudget = 225 * 1024;
+constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory per CTA
 // V is the MMA's B operand stored N(=dim)-contiguous: 128-byte swizzled rows of
 // 64 dims, one row per key; next 64-dim chunk at kVChunk bytes, next 8 keys at
 // 1024 bytes.
 constexpr uint32_t kVChunk = kKT * 128;
+// Tensor memory columns (512 allocated; head_dim <= 128):
+constexpr uint32_t kColS = 0;    // two 64-column fp32 S buffers
+constexpr uint32_t kColO = 128;  // O accumulator, head_dim fp32 columns
+constexpr uint32_t kColQ = 256;  // Q, head_dim / 2 columns of bf16 pairs
+constexpr uint32_t kColP = 384;  // P, 32 columns of bf16 pairs (64 keys)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxAttnHeadDim = 128;
 
 struct TcParams {
   AttnParams a;
-  int GT, RT, box_rows, nst, chunks, compact;
-  uint32_t q_off, q_cs, p_off, kv_off, stage_bytes, k_bytes, bar_off;
-  uint32_t tmem_cols, idesc_qk, idesc_pv, v_lbo, v_sbo;
+  int GT, RT, box_rows, nst, chunks, split;
+  uint32_t stage_bytes, k_bytes, bar_off, x_off;
+  uint32_t idesc_qk, idesc_pv, v_lbo, v_sbo;
   float scale_log2;
 };
-
-__device__ __forceinline__ uint32_t sw128_off(int row, int unit16) {
-  return static_cast<uint32_t>(row * 128 + ((unit16 ^ (row & 7)) << 4));
-}
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const TcParams P) {
@@ -64,9 +80,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = sm + P.q_off;
-  uint8_t *sP = sm + P.p_off;
-  uint8_t *sKV = sm + P.kv_off;
+  uint8_t *sKV = sm;
   const int nst = P.nst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
   uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
@@ -86,20 +100,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&s_full[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&s_full[1]), 1);
-    // one arrival per softmax warp that owns at least one real row
+    // one arrival per softmax warp at work: all four in the split layout,
+    // else those owning at least one real row
     const int real_rows = min(kRows, P.GT - static_cast<int>(blockIdx.x % P.RT) * kRows);
-    ptx::mbar_init(ptx::smem_u32(p_full), static_cast<uint32_t>((real_rows + 31) / 32));
+    ptx::mbar_init(ptx::smem_u32(p_full),
+                   P.split ? 4u : static_cast<uint32_t>((real_rows + 31) / 32));
     ptx::mbar_init(ptx::smem_u32(o_done), 1);
     ptx::mbar_init(ptx::smem_u32(drain), 1);
-    // one arrival per warp that stores Q rows (2 in the compact layout)
-    ptx::mbar_init(ptx::smem_u32(q_full), P.compact ? 2u : 4u);
+    ptx::mbar_init(ptx::smem_u32(q_full), 4u);  // one arrival per softmax warp
     *abort_flag = 0;
     *consumed = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
   }
   if (warp == 3) {
-    ptx::tmem_alloc(ptx::smem_u32(tslot), P.tmem_cols);
+    ptx::tmem_alloc(ptx::smem_u32(tslot), kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -112,33 +127,55 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   griddep_wait();
   const SegRange sr = segment_range(p, r, s);
   const int ntiles = sr.t1 - sr.t0;
-  // Q rows of this tile -> shared memory (K-major, 128-byte swizzle), in
-  // parallel with the producer's first loads; the MMA issuer waits on q_full.
-  // In the compact layout only rows 0-63 exist; the MMA's rows 64-127 read
-  // whatever follows (the next chunk or the P buffer) and are never used.
-  const int q_rows = P.compact ? 64 : kRows;
-  if (warp >= 4 && ntiles > 0 && 32 * (warp & 3) < q_rows) {
-    const int row = 32 * (warp & 3) + lane;
+  const uint32_t tm_s = tmem + kColS;
+  const uint32_t tm_o = tmem + kColO;
+  const uint32_t tm_q = tmem + kColQ;
+  const uint32_t tm_p = tmem + kColP;
+
+  // Q rows of this tile -> TMEM (softmax warp w fills its own lane quarter),
+  // in parallel with the producer's first loads; the MMA issuer waits on
+  // q_full.  In the split layout lanes 64-127 repeat rows 0-63, and each warp
+  // zeroes the half of its P columns that it never writes.
+  if (warp >= 4 && ntiles > 0) {
+    const int q4 = warp & 3;
+    const int row = P.split ? 32 * (q4 & 1) + lane : 32 * q4 + lane;
     const int R = rt * kRows + row;
     const bool real = R < P.GT;
     const int i = real ? R / p.G : 0;
     const int h = kvh * p.G + (real ? R % p.G : 0);
     const uint4 *src = reinterpret_cast<const uint4 *>(
         p.q + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.dq);
-    for (int c = 0; c < P.chunks; ++c) {
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    uint4 v[kMaxAttnHeadDim / 8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint4 v = real ? src[c * 8 + u] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sQ + c * P.q_cs + sw128_off(row, u)) = v;
+    for (int u = 0; u < kMaxAttnHeadDim / 8; ++u)
+      v[u] = (real && u < p.dq / 8) ? src[u] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < kMaxAttnHeadDim / 32; ++c) {
+      if (c < p.dq / 32) {
+        uint32_t w16[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w16[4 * u] = v[4 * c + u].x;
+          w16[4 * u + 1] = v[4 * c + u].y;
+          w16[4 * u + 2] = v[4 * c + u].z;
+          w16[4 * u + 3] = v[4 * c + u].w;
+        }
+        ptx::tmem_st16(tm_q + lane_off + 16 * c, w16);
       }
     }
-    ptx::fence_proxy_async_smem();
+    if (P.split) {
+      uint32_t z[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      ptx::tmem_st16(tm_p + lane_off + (q4 < 2 ? 16 : 0), z);
+    }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(q_full));
   }
 
-  const uint32_t tm_s = tmem;          // S buffers: columns [0, 64) and [64, 128)
-  const uint32_t tm_o = tmem + 2 * kKT;  // O accumulator: hd columns
   const int boxes = kKT / P.box_rows;
 
   if (ntiles > 0 && warp == 2) {
@@ -175,7 +212,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int st = t % nst;
       bool got = true;
       if (lane == 0 && t >= nst)
-        got = ptx::mbar_spin(ptx::smem_u32(&kv_empty[st]),
+        got = ptx::mbar_wait(ptx::smem_u32(&kv_empty[st]),
                              static_cast<uint32_t>(((t / nst) & 1) ^ 1), abort_flag);
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
@@ -214,66 +251,207 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   } else if (ntiles > 0 && warp == 3) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer (warp 3)
-      // Issues S_t = Q K_t^T as soon as K_t has landed and S buffer t&1 is
-      // free (PV_{t-2} issued), and O += P_t V_t as soon as P_t is ready,
-      // whichever comes first; neither waits behind the other.
-      const uint32_t qb = ptx::smem_u32(sQ);
-      const uint32_t pb = ptx::smem_u32(sP);
-      int next_qk = 0, next_pv = 0;
-      bool ok = ptx::mbar_spin(ptx::smem_u32(q_full), 0u, abort_flag);
-      uint32_t idle = 0;
-      uint64_t t_idle = 0;
-      while (next_pv < ntiles) {
-        bool progressed = false;
-        if (next_qk < ntiles && next_qk <= next_pv + 1 &&
-            ptx::mbar_test(ptx::smem_u32(&kv_full[next_qk % nst]),
-                           static_cast<uint32_t>((next_qk / nst) & 1))) {
-          const int t = next_qk;
-          *consumed = t + 1;
-          ptx::tc_fence_after();
-          const uint32_t kb = ptx::smem_u32(sKV + (t % nst) * P.stage_bytes);
-          for (int ks = 0; ks < P.chunks * 4; ++ks) {
-            const int c = ks >> 2, j = ks & 3;
-            ptx::mma_bf16(tm_s + (t & 1) * kKT, ptx::desc_kmajor_sw128(qb + c * P.q_cs, j),
-                          ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk,
-                          ks > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
-          ++next_qk;
-          progressed = true;
+      // Per tile t: S_{t+1} = Q K_{t+1}^T (its S buffer was released when
+      // PV_{t-1} was issued), then O += P_t V_t once the softmax has written
+      // P_t.
+      auto issue_qk = [&](int t) {
+        *consumed = t + 1;
+        const uint32_t kb = ptx::smem_u32(sKV + (t % nst) * P.stage_bytes);
+        for (int ks = 0; ks < P.chunks * 4; ++ks) {
+          const int c = ks >> 2, j = ks & 3;
+          ptx::mma_bf16_ts(tm_s + (t & 1) * kKT, tm_q + ks * 8,
+                           ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk,
+                           ks > 0 ? 1u : 0u);
         }
-        if (next_pv < next_qk &&
-            ptx::mbar_test(ptx::smem_u32(p_full), static_cast<uint32_t>(next_pv & 1))) {
-          const int t = next_pv;
+        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
+      };
+      bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag) &&
+                ptx::mbar_wait(ptx::smem_u32(&kv_full[0]), 0u, abort_flag);
+      ptx::tc_fence_after();
+      if (ok) issue_qk(0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int tn = t + 1;
+        if (tn < ntiles) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&kv_full[tn % nst]),
+                              static_cast<uint32_t>((tn / nst) & 1), abort_flag);
+          if (!ok) break;
           ptx::tc_fence_after();
-          const int st = t % nst;
-          const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
+          issue_qk(tn);
+        }
+        ok = ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int st = t % nst;
+        const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
 #pragma unroll
-          for (int ks = 0; ks < kKT / 16; ++ks) {
-            ptx::mma_bf16(tm_o, ptx::desc_kmajor_sw128(pb, ks),
-                          ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
-                          P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-          }
-          ptx::mma_commit(ptx::smem_u32(o_done));
-          ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
-          ++next_pv;
-          progressed = true;
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+          ptx::mma_bf16_ts(tm_o, tm_p + ks * 8,
+                           ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
+                           P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
         }
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 1023u) == 0) {
-          if (idle == 1024u) t_idle = ptx::globaltimer_ns();
-          if (*abort_flag || ptx::globaltimer_ns() - t_idle > ptx::kWaitLimitNs) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-        }
+        ptx::mma_commit(ptx::smem_u32(o_done));
+        ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
       }
       if (!ok) {
         ptx::mma_commit(ptx::smem_u32(drain));
         volatile int dummy = 0;
         ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      }
+    }
+  } else if (warp >= 4 && P.split) {
+    // ------------------------------------------------ softmax, split layout
+    // Warp pair (q4, q4 ^ 2) shares query rows 32*(q4&1)..+31: warp q4 < 2
+    // takes key columns 0-31 from TMEM lanes of rows 0-63, warp q4 >= 2 takes
+    // columns 32-63 from the duplicate rows 64-127.  Row maxima are exchanged
+    // through shared memory behind a pair barrier (double-buffered by tile
+    // parity); every abort decision is made pair-uniform at that barrier, so
+    // both partners take identical rescale decisions and their O halves stay
+    // on one scale.
+    const int q4 = warp & 3;
+    const int half = q4 >> 1;
+    const int rrow = 32 * (q4 & 1) + lane;
+    const bool real = rrow < P.GT;
+    const int i = real ? rrow / p.G : 0;
+    const int h = kvh * p.G + (real ? rrow % p.G : 0);
+    int lo = 0, hi = -1;
+    if (real) row_key_range(p, sr.kv_len, i, &lo, &hi);
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t pair_bar = 2u + static_cast<uint32_t>(q4 & 1);
+    float *xmax = reinterpret_cast<float *>(sm + P.x_off);  // [2 parity][2 half][64 rows]
+    float *xl = xmax + 256;                                 // [64 rows]
+    float m_ref = -INFINITY, l = 0.f;
+    bool bad = false;
+    for (int t = 0; t < ntiles; ++t) {
+      const bool got = __all_sync(0xffffffffu,
+                                  ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
+                                                 static_cast<uint32_t>((t >> 1) & 1), abort_flag));
+      float sv[32];
+      if (got) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld32f_sync(tm_s + lane_off + (t & 1) * kKT + 32 * half, sv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = -INFINITY;
+      }
+      const int kbase = (sr.t0 + t) * kKT + 32 * half;
+      if (!(lo <= kbase && hi >= kbase + 31)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (kbase + c < lo || kbase + c > hi) sv[c] = -INFINITY;
+      }
+      float mx[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mx[c] = fmaxf(sv[c], sv[c + 16]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+      xmax[((t & 1) * 2 + half) * 64 + rrow] = mx[0];
+      if (ptx::bar_or(pair_bar, 64, bad || !got)) {
+        bad = true;
+        break;
+      }
+      const float tmax = fmaxf(mx[0], xmax[((t & 1) * 2 + (half ^ 1)) * 64 + rrow]) * P.scale_log2;
+      float corr = 1.f;
+      bool need = false;
+      if (m_ref == -INFINITY) {
+        m_ref = tmax;
+      } else if (tmax > m_ref + 8.f) {
+        corr = ptx::ex2(m_ref - tmax);
+        m_ref = tmax;
+        need = true;
+      }
+      uint32_t pk[16];
+      float sum = 0.f;
+      if (m_ref != -INFINITY) {
+        const float nm = -m_ref;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) mx[c] = sv[c] + sv[c + 16];
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) mx[c] += mx[c + w];
+        sum = mx[0];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+      }
+      l = l * corr + sum;
+      // PV of the previous tile must be done before O is rescaled and before
+      // the single P buffer is overwritten.
+      if (t > 0) {
+        const bool got_o = __all_sync(0xffffffffu,
+                                      ptx::mbar_wait(ptx::smem_u32(o_done),
+                                                     static_cast<uint32_t>((t - 1) & 1), abort_flag));
+        if (!got_o) {
+          bad = true;  // the next pair barrier (or the epilogue's) carries it
+          continue;
+        }
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          for (int c = 0; c < p.dv; c += 16) {
+            uint32_t ov[16];
+            ptx::tmem_ld16_sync(tm_o + lane_off + c, ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+            ptx::tmem_st16(tm_o + lane_off + c, ov);
+          }
+        }
+      }
+      ptx::tmem_st16(tm_p + lane_off + 16 * half, pk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
+    }
+    // epilogue: the half-1 warp hands its partial row sums and its O half to
+    // the half-0 warp (through the idle KV ring), which writes (m, l, O) of
+    // rows 0-63
+    bool okf = !bad && ntiles > 0;
+    if (okf) {
+      okf = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(o_done),
+                                                   static_cast<uint32_t>((ntiles - 1) & 1),
+                                                   abort_flag));
+      ptx::tc_fence_after();
+    }
+    float *xo = reinterpret_cast<float *>(sKV);  // [head_dim][64 rows]
+    if (half == 1) {
+      xl[rrow] = l;
+      if (okf) {
+        for (int c = 0; c < p.dv; c += 16) {
+          uint32_t ov[16];
+          ptx::tmem_ld16_sync(tm_o + lane_off + c, ov);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) xo[(c + e) * 64 + rrow] = __uint_as_float(ov[e]);
+        }
+      }
+    }
+    const bool pair_bad = ptx::bar_or(pair_bar, 64, !okf && ntiles > 0);
+    if (half == 0) {
+      const bool any = real && !pair_bad && ntiles > 0 && m_ref != -INFINITY;
+      const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
+      if (real) {
+        p.ws_m[wsi] = any ? m_ref * 0.69314718055994530942f : -INFINITY;
+        p.ws_l[wsi] = any ? l + xl[rrow] : 0.f;
+      }
+      if (__any_sync(0xffffffffu, any)) {
+        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wsi * p.dv);
+        for (int c = 0; c < p.dv; c += 16) {
+          uint32_t ov[16];
+          ptx::tmem_ld16_sync(tm_o + lane_off + c, ov);
+          if (any) {
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(ov[e]) + xo[(c + e) * 64 + rrow];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              dst[(c + e) / 4] = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          }
+        }
       }
     }
   } else if (warp >= 4) {
@@ -292,7 +470,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles && warp_active; ++t) {
-      const bool got_s = ptx::mbar_spin(ptx::smem_u32(&s_full[t & 1]),
+      const bool got_s = ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
                                         static_cast<uint32_t>((t >> 1) & 1), abort_flag);
       if (!__all_sync(0xffffffffu, got_s)) {
         ok = false;
@@ -349,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // PV of the previous tile must be done before O is rescaled and before
       // the single P buffer is overwritten.
       if (t > 0) {
-        const bool got_o = ptx::mbar_spin(ptx::smem_u32(o_done),
+        const bool got_o = ptx::mbar_wait(ptx::smem_u32(o_done),
                                           static_cast<uint32_t>((t - 1) & 1), abort_flag);
         if (!__all_sync(0xffffffffu, got_o)) {
           ok = false;
@@ -364,14 +542,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
             ptx::tmem_st16(tm_o + lane_off + c, ov);
           }
-          ptx::tmem_wait_st();
         }
       }
+      uint32_t p0[16], p1[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4 *>(sP + sw128_off(row, u)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      ptx::fence_proxy_async_smem();
+      for (int c = 0; c < 16; ++c) {
+        p0[c] = pk[c];
+        p1[c] = pk[16 + c];
+      }
+      ptx::tmem_st16(tm_p + lane_off, p0);
+      ptx::tmem_st16(tm_p + lane_off + 16, p1);
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
@@ -410,7 +591,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (threadIdx.x == 0 && *abort_flag) raise_status(p.st, DFLASH_DEV_WAIT_TIMEOUT);
   if (warp == 3) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, P.tmem_cols);
+    ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -419,28 +600,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s) {
   TcParams P;
   P.a = a;
-  const int hd = g.head_dim;
+  const int hd = g.head_dim;  // 64 or 128 (validated by the caller)
   P.chunks = hd / 64;
   P.GT = a.Tq * a.G;
   P.RT = (P.GT + kRows - 1) / kRows;
   P.box_rows = a.P < kKT ? a.P : kKT;
-  // Compact layout when the group's rows fit in 64: Q chunks of 64 rows
-  // (8 KB) back to back, leaving more room for the KV ring.
-  P.compact = P.GT <= 64 ? 1 : 0;
-  P.q_cs = P.compact ? 64 * 128 : kRows * 128;
-  const uint32_t q_bytes = P.chunks * P.q_cs;
-  const uint32_t p_bytes = kRows * 128;
+  // Split layout when a KV head's query rows fit in half the MMA rows.
+  P.split = P.GT <= 64 ? 1 : 0;
   P.k_bytes = P.chunks * kVChunk;
   P.stage_bytes = 2 * P.k_bytes;
-  P.q_off = 0;
-  P.p_off = q_bytes;
-  P.kv_off = q_bytes + p_bytes;
-  const int budget = kSmemBudget;
-  P.nst = std::max(2, std::min<int>(8, static_cast<int>((budget - q_bytes - p_bytes) /
+  const uint32_t x_bytes = 320 * 4;  // split-layout row maxima and row sums
+  const uint32_t bar_bytes = 8 * 8 * 2 + 7 * 8 + 16;
+  P.nst = std::max(2, std::min<int>(8, static_cast<int>((kSmemMax - 1024 - bar_bytes - x_bytes) /
                                                           P.stage_bytes)));
-  P.bar_off = P.kv_off + P.nst * P.stage_bytes;
-  const uint32_t smem = 1024 + P.bar_off + (2 * P.nst + 7) * 8 + 16;
-  P.tmem_cols = (2 * kKT + hd) <= 256 ? 256 : 512;
+  P.bar_off = P.nst * P.stage_bytes;
+  P.x_off = (P.bar_off + (2 * P.nst + 7) * 8 + 16 + 15) & ~15u;
+  const uint32_t smem = 1024 + P.x_off + x_bytes;
   P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);
   P.v_lbo = kVChunk;
@@ -452,7 +627,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit(attn_tc_kernel, 227 * 1024)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit(attn_tc_kernel, kSmemMax)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, a.nkv, a.B);
