@@ -8,19 +8,22 @@
 //
 // One CTA = (segment s, row tile rt) x KV head x request.  Its 128 MMA rows
 // are the query rows (token i, head h) of the KV head's group (G = hq / nkv
-// heads x Tq tokens; rows past G*Tq are zero padding).  Per 64-key tile:
+// heads x Tq tokens; rows past G*Tq are zero padding).  Per 128-key tile:
 //   TMA   K and V pages of the tile -> shared memory ring (`nst` stages)
-//   MMA   S = Q K^T     (M=128, N=64, K=hd; Q from TMEM) -> TMEM S (2 buffers)
+//   MMA   S = Q K^T     (M=128, N=128, K=hd; Q from TMEM) -> TMEM S (2 buffers)
 //   softmax warps: mask, online max with lazy rescale (the reference max only
 //         moves when the tile max exceeds it by 2^8, so O in TMEM is rarely
 //         rescaled), P = exp2(s - m) -> bf16 -> TMEM
-//   MMA   O += P V      (M=128, N=hd, K=64; P from TMEM) -> TMEM O
+//   MMA   O += P V      (M=128, N=hd, K=128; P from TMEM) -> TMEM O
 // and at the end each real row writes (m, l, O) of its segment to the
 // workspace for the merge kernel.  Both MMAs take their A operand (Q, P) from
 // tensor memory: with A in shared memory the tensor pipe spends most of its
-// time re-reading Q (a 64-key QK costs about as much as a 128-key one), and
-// keeping P out of shared memory also drops a store, a proxy fence and 16 KB
-// of shared memory per tile; the freed space deepens the KV ring.
+// time re-reading Q, and keeping P out of shared memory also drops a store, a
+// proxy fence and 32 KB of shared memory per tile.  The single issuing thread
+// is the critical resource here (each tcgen05.mma takes ~70 cycles to issue
+// whatever its N, and every commit and barrier wait adds to the same serial
+// stream), so tiles are 128 keys wide: per key that halves the QK
+// instructions and the waits and commits of a 64-key tile.
 //
 // Roles (8 warps): warp 2 issues TMA, warp 3 issues tcgen05.mma and owns the
 // TMEM allocation, warps 4-7 run the softmax (warp w reads and writes TMEM
@@ -29,9 +32,9 @@
 // case: a 16-token block times a few heads per KV head), those rows are
 // loaded twice, as MMA rows r and r + 64: the tensor core then hands all four
 // sub-partitions a copy of the scores and each softmax warp takes half of a
-// row's 64 key columns, so the exp2 work spreads over all four SFU pipes
-// instead of two.  Row r's P then carries its first 32 keys (zeros after) and
-// row r + 64's its last 32 (zeros before), so O rows r and r + 64 hold the two
+// row's 128 key columns, so the exp2 work spreads over all four SFU pipes
+// instead of two.  Row r's P then carries its first 64 keys (zeros after) and
+// row r + 64's its last 64 (zeros before), so O rows r and r + 64 hold the two
 // halves of the row's sum, added in the epilogue.
 //
 // Every wait is an mbarrier try_wait, which suspends the thread in hardware
@@ -50,7 +53,8 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, u
 
 namespace {
 
-constexpr int kKT = kAttnTileKeys;  // 64 keys per tile
+constexpr int kKT = kAttnTileKeys;  // 128 keys per tile
+static_assert(kKT == 128, "TMEM column plan below assumes 128-key tiles");
 constexpr int kRows = 128;
 constexpr int kThreadsTC = 256;
 constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory per CTA
@@ -58,11 +62,11 @@ constexpr int kSmemMax = 227 * 1024;  // dynamic shared memory per CTA
 // 64 dims, one row per key; next 64-dim chunk at kVChunk bytes, next 8 keys at
 // 1024 bytes.
 constexpr uint32_t kVChunk = kKT * 128;
-// Tensor memory columns (512 allocated; head_dim <= 128):
-constexpr uint32_t kColS = 0;    // two 64-column fp32 S buffers
-constexpr uint32_t kColO = 128;  // O accumulator, head_dim fp32 columns
-constexpr uint32_t kColQ = 256;  // Q, head_dim / 2 columns of bf16 pairs
-constexpr uint32_t kColP = 384;  // P, 32 columns of bf16 pairs (64 keys)
+// Tensor memory columns (all 512 allocated; head_dim <= 128):
+constexpr uint32_t kColS = 0;    // two 128-column fp32 S buffers
+constexpr uint32_t kColO = 256;  // O accumulator, head_dim fp32 columns
+constexpr uint32_t kColQ = 384;  // Q, head_dim / 2 columns of bf16 pairs
+constexpr uint32_t kColP = 448;  // P, 64 columns of bf16 pairs (128 keys)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxAttnHeadDim = 128;
 
@@ -168,7 +172,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint32_t z[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) z[e] = 0u;
-      ptx::tmem_st16(tm_p + lane_off + (q4 < 2 ? 16 : 0), z);
+      const uint32_t zc = tm_p + lane_off + (q4 < 2 ? 32 : 0);
+      ptx::tmem_st16(zc, z);
+      ptx::tmem_st16(zc + 16, z);
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
@@ -301,8 +307,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   } else if (warp >= 4 && P.split) {
     // ------------------------------------------------ softmax, split layout
     // Warp pair (q4, q4 ^ 2) shares query rows 32*(q4&1)..+31: warp q4 < 2
-    // takes key columns 0-31 from TMEM lanes of rows 0-63, warp q4 >= 2 takes
-    // columns 32-63 from the duplicate rows 64-127.  Row maxima are exchanged
+    // takes key columns 0-63 from TMEM lanes of rows 0-63, warp q4 >= 2 takes
+    // columns 64-127 from the duplicate rows 64-127.  Row maxima are exchanged
     // through shared memory behind a pair barrier (double-buffered by tile
     // parity); every abort decision is made pair-uniform at that barrier, so
     // both partners take identical rescale decisions and their O halves stay
@@ -325,25 +331,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const bool got = __all_sync(0xffffffffu,
                                   ptx::mbar_wait(ptx::smem_u32(&s_full[t & 1]),
                                                  static_cast<uint32_t>((t >> 1) & 1), abort_flag));
-      float sv[32];
+      float sv[64];
       if (got) {
         ptx::tc_fence_after();
-        ptx::tmem_ld32f_sync(tm_s + lane_off + (t & 1) * kKT + 32 * half, sv);
+        ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT + 64 * half, sv);
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = -INFINITY;
+        for (int c = 0; c < 64; ++c) sv[c] = -INFINITY;
       }
-      const int kbase = (sr.t0 + t) * kKT + 32 * half;
-      if (!(lo <= kbase && hi >= kbase + 31)) {
+      const int kbase = (sr.t0 + t) * kKT + 64 * half;
+      if (!(lo <= kbase && hi >= kbase + 63)) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < 64; ++c)
           if (kbase + c < lo || kbase + c > hi) sv[c] = -INFINITY;
       }
-      float mx[16];
+      float mx[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) mx[c] = fmaxf(sv[c], sv[c + 16]);
+      for (int c = 0; c < 32; ++c) mx[c] = fmaxf(sv[c], sv[c + 32]);
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
         for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
       xmax[((t & 1) * 2 + half) * 64 + rrow] = mx[0];
@@ -361,24 +367,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         m_ref = tmax;
         need = true;
       }
-      uint32_t pk[16];
+      uint32_t pk[32];
       float sum = 0.f;
       if (m_ref != -INFINITY) {
         const float nm = -m_ref;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
+        for (int c = 0; c < 64; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) mx[c] = sv[c] + sv[c + 16];
+        for (int c = 0; c < 32; ++c) mx[c] = sv[c] + sv[c + 32];
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
           for (int c = 0; c < w; ++c) mx[c] += mx[c + w];
         sum = mx[0];
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
       l = l * corr + sum;
       // PV of the previous tile must be done before O is rescaled and before
@@ -402,7 +408,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
         }
       }
-      ptx::tmem_st16(tm_p + lane_off + 16 * half, pk);
+      {
+        uint32_t p0[16], p1[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          p0[c] = pk[c];
+          p1[c] = pk[16 + c];
+        }
+        ptx::tmem_st16(tm_p + lane_off + 32 * half, p0);
+        ptx::tmem_st16(tm_p + lane_off + 32 * half + 16, p1);
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -477,24 +492,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         break;
       }
       ptx::tc_fence_after();
-      float sv[kKT];
-      static_assert(kKT == 64, "one 64-column TMEM load per tile");
-      ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT, sv);
       const int kbase = (sr.t0 + t) * kKT;
-      if (!(lo <= kbase && hi >= kbase + kKT - 1)) {  // a tile the row sees only in part
+      const bool partial = !(lo <= kbase && hi >= kbase + kKT - 1);  // row sees part of the tile
+      // pass 1: tile maximum of the raw scores over both 64-column halves
+      float raw_max = -INFINITY;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float sv[64];
+        ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT + 64 * hh, sv);
+        if (partial) {
 #pragma unroll
-        for (int c = 0; c < kKT; ++c)
-          if (kbase + c < lo || kbase + c > hi) sv[c] = -INFINITY;
+          for (int c = 0; c < 64; ++c)
+            if (kbase + 64 * hh + c < lo || kbase + 64 * hh + c > hi) sv[c] = -INFINITY;
+        }
+        float mx[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx[c] = fmaxf(sv[c], sv[c + 32]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+        raw_max = fmaxf(raw_max, mx[0]);
       }
-      // tile maximum of the raw scores (tree), then into the exp2 domain
-      float mx[kKT / 2];
-#pragma unroll
-      for (int c = 0; c < kKT / 2; ++c) mx[c] = fmaxf(sv[c], sv[c + kKT / 2]);
-#pragma unroll
-      for (int w = kKT / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-      const float tmax = mx[0] * P.scale_log2;
+      const float tmax = raw_max * P.scale_log2;
       float corr = 1.f;
       bool need = false;
       if (m_ref == -INFINITY) {
@@ -504,26 +524,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         m_ref = tmax;
         need = true;
       }
-      uint32_t pk[kKT / 2];
-      float sum = 0.f;
-      if (m_ref != -INFINITY) {
-        const float nm = -m_ref;
-#pragma unroll
-        for (int c = 0; c < kKT; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
-#pragma unroll
-        for (int c = 0; c < kKT / 2; ++c) pk[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
-#pragma unroll
-        for (int c = 0; c < kKT / 2; ++c) mx[c] = sv[c] + sv[c + kKT / 2];
-#pragma unroll
-        for (int w = kKT / 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) mx[c] += mx[c + w];
-        sum = mx[0];
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKT / 2; ++c) pk[c] = 0u;
-      }
-      l = l * corr + sum;
       // PV of the previous tile must be done before O is rescaled and before
       // the single P buffer is overwritten.
       if (t > 0) {
@@ -544,14 +544,43 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
         }
       }
-      uint32_t p0[16], p1[16];
+      // pass 2: P = exp2(s - m) per half, straight into TMEM
+      float sum = 0.f;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float sv[64];
+        ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT + 64 * hh, sv);
+        if (partial) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        p0[c] = pk[c];
-        p1[c] = pk[16 + c];
+          for (int c = 0; c < 64; ++c)
+            if (kbase + 64 * hh + c < lo || kbase + 64 * hh + c > hi) sv[c] = -INFINITY;
+        }
+        uint32_t p0[16], p1[16];
+        if (m_ref != -INFINITY) {
+          const float nm = -m_ref;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = ptx::ex2(fmaf(sv[c], P.scale_log2, nm));
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            p0[c] = ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
+            p1[c] = ptx::pack_bf16x2(sv[32 + 2 * c], sv[32 + 2 * c + 1]);
+          }
+          float mx[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx[c] = sv[c] + sv[c + 32];
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+            for (int c = 0; c < w; ++c) mx[c] += mx[c + w];
+          sum += mx[0];
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) p0[c] = p1[c] = 0u;
+        }
+        ptx::tmem_st16(tm_p + lane_off + 32 * hh, p0);
+        ptx::tmem_st16(tm_p + lane_off + 32 * hh + 16, p1);
       }
-      ptx::tmem_st16(tm_p + lane_off, p0);
-      ptx::tmem_st16(tm_p + lane_off + 16, p1);
+      l = l * corr + sum;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();

@@ -12,7 +12,7 @@ namespace dflash {
 
 // ------------------------------------------------------------ constants
 constexpr int kMaxHeadDim = 256;
-constexpr int kAttnTileKeys = 64;   // keys per attention tile
+constexpr int kAttnTileKeys = 128;  // keys per attention tile
 constexpr int kGemmTileM = 128;     // weight rows per GEMM tile
 constexpr int kGemmTileK = 64;      // reduction depth per pipeline stage (128 B of bf16)
 

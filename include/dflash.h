@@ -278,7 +278,7 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * (no sink term when sinks == NULL; out = 0 when no key is visible).
  * Key j lives at page block_table[r, j/P], slot j%P of layer `layer`.
  * The visible span [lo_0, hi_{Tq-1}] is cut into num_segments slices of whole
- * 64-key tiles; each (request, kv head, slice) CTA -- one per 128 query rows
+ * 128-key tiles; each (request, kv head, slice) CTA -- one per 128 query rows
  * of the kv head's group, rows being (token, head) pairs -- writes a partial
  * (max, sum, weighted values) to the workspace and a second pass merges them
  * (log-sum-exp) with the sink.
@@ -296,7 +296,7 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * Errors: DFLASH_ERR_INVALID_ARG (also: scale not finite and > 0, window < 0,
  * unknown mask_mode, a pointer not 16-byte aligned), DFLASH_ERR_UNSUPPORTED_GEOM
  * (hq not a multiple of nkv, GQA head_dim not 64 or 128, MLA dims not 512 + 64,
- * page_size not a multiple of 8 that divides 64 or is a multiple of 64, pool
+ * page_size not a multiple of 8 that divides 128 or is a multiple of 128, pool
  * rows >= 2^31), DFLASH_ERR_WORKSPACE_TOO_SMALL, DFLASH_ERR_CUDA.
  * ------------------------------------------------------------------- */
 DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq, const void *q,

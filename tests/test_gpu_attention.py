@@ -92,6 +92,21 @@ def test_attention_group_sizes_and_pages(dl, mode, hq, nkv, hd, P):
     assert_close(got, ref, f"hq={hq} nkv={nkv} hd={hd} P={P} mode={mode}")
 
 
+@pytest.mark.parametrize("hq,nkv,hd,Tq", [(32, 2, 128, 8), (24, 8, 128, 30), (32, 2, 64, 5),
+                                          (32, 2, 128, 16), (12, 1, 64, 20)])
+def test_attention_large_groups_and_row_tiles(dl, hq, nkv, hd, Tq):
+    # Tq * hq / nkv query rows per KV head above 64 (one thread per full row)
+    # and above 128 (several row tiles per KV head, the last one ragged).
+    kv_lens = [Tq, 333, 1500]
+    g, pool, tbl, q, sinks = _gqa_case(hq * 7 + Tq, kv_lens, hq=hq, nkv=nkv, hd=hd, P=64, Tq=Tq)
+    for mode in (0, 1):
+        ref = oracle.attention_gqa(g, 0, q, pool, tbl, np.array(kv_lens), window=700, sinks=sinks,
+                                   mask_mode=mode)
+        got, st = _run_gpu(dl, g, 0, q, pool, tbl, kv_lens, window=700, sinks=sinks, mask_mode=mode)
+        assert_close(got, ref, f"hq={hq} nkv={nkv} hd={hd} Tq={Tq} mode={mode}")
+        assert st == 0
+
+
 @pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 64, 1000])
 def test_attention_segment_counts(dl, S):
     kv_lens = [1500, 17, 640]
