@@ -37,9 +37,10 @@ UNIT = "us/step"
 WORKLOAD = "qwen3_8b"
 CTX = 32768
 
-# DRAM traffic per attention launch from the committed ncu capture, keyed by
+# DRAM traffic (read + write) of one attention call (main kernel + merge) from
+# the committed ncu capture, keyed by
 # the hash of the attention sources it was taken on (None = not captured).
-ATTN_TRAFFIC = {"sources_sha": None, "bytes_per_launch": None,
+ATTN_TRAFFIC = {"sources_sha": "a0df0090e9d86dd1", "bytes_per_launch": 143499008,
                 "profile": "profiles/attention_qwen3_8b_32k.md"}
 
 
