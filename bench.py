@@ -36,6 +36,52 @@ METRIC = "drafter step µs (ctx-KV update + block attn) at B=1, 32K ctx; attn HB
 UNIT = "us/step"
 WORKLOAD = "qwen3_8b"
 CTX = 32768
+WORKLOAD_TAG = "qwen3_8b_drafter_ctx32k"
+
+
+def workload_config(args):
+    """(tag, inputs config) of the run: the headline workload by default;
+    --workload/--ctx select another configuration (sliding_window, mla,
+    batch_sweep_<B>, tiny) for the measurement tables."""
+    name = getattr(args, "workload", None) or WORKLOAD
+    ctx = getattr(args, "ctx", None)
+    over = {}
+    if name in ("qwen3_8b", "mla"):
+        over["ctx"] = [ctx or CTX]
+    elif ctx and not name.startswith("batch_sweep_"):
+        over["ctx"] = [ctx]
+    window = getattr(args, "window", None)
+    if window is not None:
+        over["window"] = window
+    cfg = inputs.workload(name, **over)
+    if name == WORKLOAD and (ctx or CTX) == CTX and window is None:
+        return WORKLOAD_TAG, cfg
+    tag = name + (f"_ctx{over['ctx'][0]}" if "ctx" in over else "")
+    tag += f"_window{window}" if window is not None else ""
+    return tag, cfg
+
+
+def attention_work(prob):
+    """Algorithmic bytes and FLOPs of one attention call (one layer): every
+    visible key of every request read once; QK and PV for every query row."""
+    g = prob["g"]
+    T, B = g["T"], prob["B"]
+    A = np.asarray(prob["alloc_limit"], np.int64)
+    c = np.asarray(prob["ctx_len"], np.int64)
+    n = np.asarray(prob["n_acc"], np.int64)
+    kv = np.minimum(c + n, A) + T
+    w = int(prob["window"])
+    lo = np.maximum(0, kv - T - w + 1) if w > 0 else np.zeros_like(kv)
+    keys = int((kv - lo).sum())
+    rows = T * g["hq"]
+    if g["kind"] == "mla":
+        width = g["latent"] + g["rope_dim"]
+        nbytes = keys * width * 2
+        flops = 2 * keys * rows * (width + g["latent"])
+    else:
+        nbytes = keys * g["nkv"] * g["hd"] * 2 * 2
+        flops = 4 * keys * rows * g["hd"]
+    return nbytes, flops, int(kv.max())
 
 # DRAM traffic (read + write) of one attention call (main kernel + merge) from
 # the committed ncu capture, keyed by
@@ -58,8 +104,11 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         d = json.load(open(p))
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained",
+                                                     d["bf16_tflops"])),
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -136,9 +185,25 @@ class Step:
         self.hidden = td(prob["hidden"])
         self.weights = {k: td(prob[k]) for k in ("w_fc", "g_h", "w_kv", "g_k")}
         self.pool = td(prob["pool"])
-        self.q = td(prob["q"])
-        self.blk_k = td(prob["blk_k"])
-        self.blk_v = td(prob["blk_v"])
+        self.mla = g["kind"] == "mla"
+        if self.mla:
+            self.q = td(prob["q_lat"])
+            self.q_rope = td(prob["q_rope"])
+            self.blk_k = td(prob["blk_lat"])
+            self.blk_v = None
+            dv = g["latent"]
+            host = {"q_lat": self.q, "q_rope": self.q_rope, "blk_lat": self.blk_k}
+        else:
+            self.q = td(prob["q"])
+            self.q_rope = None
+            self.blk_k = td(prob["blk_k"])
+            self.blk_v = td(prob["blk_v"])
+            dv = g["hd"]
+            host = {"q": self.q, "blk_k": self.blk_k, "blk_v": self.blk_v}
+        # per-step inputs a caller would upload (prob key -> device tensor)
+        self.step_inputs = dict({"raw_offsets": self.raw_offsets, "acc": self.acc,
+                                 "n_acc": self.n_acc, "ctx_len": self.ctx_pre,
+                                 "hidden": self.hidden}, **host)
         self.sinks = td(prob["sinks"]) if prob["use_sinks"] else None
         M = g["max_pages"]
         self.outs = {}
@@ -152,7 +217,7 @@ class Step:
                                   device=dev)
         self.attn_ws = torch.empty(dl.dflash_attention_workspace_bytes(self.geom, B, T, 0),
                                    dtype=torch.uint8, device=dev)
-        self.attn_out = torch.empty((L, B, T, g["hq"], g["hd"]), dtype=torch.bfloat16, device=dev)
+        self.attn_out = torch.empty((L, B, T, g["hq"], dv), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if dev_status else None
         self.scale = inputs.attention_scale(g)
         self.launches_per_step = None
@@ -177,13 +242,15 @@ class Step:
                                 o["block_table"], None, self.weights, self.pool, self.ctx_ws,
                                 self.status)
         for layer in range(g["L"]):
-            dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer], self.blk_v[layer],
+            dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer],
+                                       None if self.mla else self.blk_v[layer],
                                        o["blk_page"], o["blk_slot"], o["blk_mask"], self.pool,
                                        self.status)
             if events is not None:
                 events[layer][0].record()
             dl.dflash_block_attention(self.geom, layer, self.q[layer], self.pool, o["block_table"],
                                       o["seq_lens"], self.attn_out[layer], self.attn_ws,
+                                      q_rope=None if self.q_rope is None else self.q_rope[layer],
                                       window=self.prob["window"], sinks=self.sinks,
                                       scale=self.scale, dev_status=self.status)
             if events is not None:
@@ -225,7 +292,7 @@ def run_ours(args, rank, world):
     import context_kv_update_gb300 as dl
     dl.load()
     torch.cuda.set_device(rank % max(1, torch.cuda.device_count()))
-    cfg = inputs.workload(WORKLOAD, ctx=[CTX])
+    _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=rank)
     g = prob["g"]
     step = Step(dl, prob)
@@ -309,16 +376,7 @@ def run_e2e(dl, step, stream, steps):
     and the outputs read back every step (copies inside the timed region)."""
     import torch
     prob, g = step.prob, step.g
-    host_in = {
-        "raw_offsets": (prob["raw_offsets"], step.raw_offsets),
-        "acc": (prob["acc"], step.acc),
-        "n_acc": (prob["n_acc"], step.n_acc),
-        "ctx_pre": (prob["ctx_len"], step.ctx_pre),
-        "hidden": (prob["hidden"], step.hidden),
-        "q": (prob["q"], step.q),
-        "blk_k": (prob["blk_k"], step.blk_k),
-        "blk_v": (prob["blk_v"], step.blk_v),
-    }
+    host_in = {k: (prob[k], d) for k, d in step.step_inputs.items()}
     pinned = {}
     for k, (a, d) in host_in.items():
         a = np.ascontiguousarray(a)
@@ -367,7 +425,8 @@ def run_kernel_only(args):
     build.build()
     import context_kv_update_gb300 as dl
     dl.load()
-    prob = inputs.make_problem(inputs.workload(WORKLOAD, ctx=[CTX]), seed=0)
+    _, cfg = workload_config(args)
+    prob = inputs.make_problem(cfg, seed=0)
     step = Step(dl, prob)
     step.run()
     torch.cuda.synchronize()
@@ -381,6 +440,7 @@ def run_kernel_only(args):
         if args.kernel == "attention":
             dl.dflash_block_attention(step.geom, layer, step.q[layer], step.pool, o["block_table"],
                                       o["seq_lens"], step.attn_out[layer], ws,
+                                      q_rope=None if step.q_rope is None else step.q_rope[layer],
                                       window=prob["window"], sinks=step.sinks, scale=step.scale,
                                       num_segments=args.segments, dev_status=step.status)
         else:
@@ -504,6 +564,12 @@ def main():
                     help="run only this call of the step, eagerly (for profiler captures)")
     ap.add_argument("--segments", type=int, default=0,
                     help="attention split count for --kernel attention (0 = automatic)")
+    ap.add_argument("--workload", default=None,
+                    help="qwen3_8b (default), sliding_window, mla, batch_sweep_<B>, tiny")
+    ap.add_argument("--ctx", type=int, default=None,
+                    help="context length for qwen3_8b / mla / sliding_window (default 32768)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="override the workload's sliding window (0 = full range)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -528,39 +594,57 @@ def main():
         return
     prob = res["prob"]
     g = prob["g"]
-    # attention reads every cached key of the step: c' + T keys (c' = c + n)
-    kv_len = int(min(prob["ctx_len"][0] + prob["n_acc"][0], prob["alloc_limit"][0])) + g["T"]
-    attn_bytes = kv_len * g["nkv"] * g["hd"] * 2 * 2
+    tag, _ = workload_config(args)
+    headline = tag == WORKLOAD_TAG
+    attn_bytes, attn_flops, kv_len = attention_work(prob)
     peaks = measured_peaks()
-    achieved = attn_bytes / (res["attn_ms"] * 1e-3) / 1e9
-    traffic = None
-    if ATTN_TRAFFIC["sources_sha"] == attention_sources_sha():
-        traffic = ATTN_TRAFFIC["bytes_per_launch"]
+    attn_s = res["attn_ms"] * 1e-3
     us = res["ms_step"] * 1000.0
+    # HBM-bound unless the call's arithmetic intensity is above the ridge point
+    if attn_flops / attn_bytes > peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9):
+        achieved = attn_flops / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": None,
+                "flops_per_launch": attn_flops,
+                "peak_source": peaks["source"] + " bf16_tflops_sustained (of "
+                               + peaks["source"] + ")"}
+    else:
+        achieved = attn_bytes / attn_s / 1e9
+        traffic = None
+        if headline and ATTN_TRAFFIC["sources_sha"] == attention_sources_sha():
+            traffic = ATTN_TRAFFIC["bytes_per_launch"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "bytes_per_launch": attn_bytes,
+                "peak_source": peaks["source"] + " hbm_gbs (of " + peaks["source"] + ")"}
+    roof.update({"kernel": "dflash_block_attention (split + merge)",
+                 "launch_ms": round(res["attn_ms"], 5)})
+    config = {"workload": tag, "B": prob["B"],
+              "ctx_len": CTX if headline else [int(x) for x in prob["ctx_len"][:8]],
+              "kv_len": kv_len, "layers": g["L"], "hq": g["hq"], "nkv": g["nkv"],
+              "hd": g["hd"], "block": g["T"], "page": g["P"], "d_model": g["D"],
+              "window": int(prob["window"]), "sinks": bool(prob["use_sinks"]),
+              "timing": "CUDA-graph replay of whole steps, CUDA events on the stream",
+              "l2": ("inputs larger than L2 (KV 640 MiB + weights 117 MB per step)" if headline
+                     else "per-step KV + weight bytes as the workload gives"),
+              "parallelism": "replicas" if world > 1 else "single GPU"}
+    if g["kind"] == "mla":
+        config.update({"latent": g["latent"], "rope_dim": g["rope_dim"]})
     line = {
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) hidden/q/KV, N(0,0.02) weights)",
-        "config": {"workload": "qwen3_8b_drafter_ctx32k", "B": 1, "ctx_len": CTX,
-                   "kv_len": kv_len, "layers": g["L"], "hq": g["hq"], "nkv": g["nkv"],
-                   "hd": g["hd"], "block": g["T"], "page": g["P"], "d_model": g["D"],
-                   "timing": "CUDA-graph replay of whole steps, CUDA events on the stream",
-                   "l2": "inputs larger than L2 (KV 640 MiB + weights 117 MB per step)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "attn_gbs": round(achieved, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "kernel": "dflash_block_attention (split + merge)",
-                     "bytes_per_launch": attn_bytes,
-                     "launch_ms": round(res["attn_ms"], 5),
-                     "peak_source": peaks["source"] + " hbm_gbs (of " + peaks["source"] + ")"},
+        "config": config,
+        "attn_gbs": round(attn_bytes / attn_s / 1e9, 1),
+        "roofline": roof,
         "clocks": res["clocks"],
         "e2e": res["e2e"],
         "gpu_launches": kernel_launches_per_step(g) * args.steps,
         "device_status": res["status"],
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and headline:
         line["cpu_baseline"] = cpu_baseline(prob)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -110,7 +110,9 @@ template <int DV>
 __global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
   griddep_launch();
   griddep_wait();
-  constexpr int kBatch = 16;
+  // one round trip for up to 32 segments (16 at the widest rows, within the
+  // register budget of a 512-thread block)
+  constexpr int kBatch = DV >= 512 ? 16 : 32;
   const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
   const int d = threadIdx.x;

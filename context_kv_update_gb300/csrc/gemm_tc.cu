@@ -260,19 +260,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_base[j] = (cc * p.maxt + (t - (cc * U / C) / KB)) * p.ntile * 128;
           }
           ptx::bar_sync(1, 128);
-          // 16 rows at a time: the 16 loads of one partial tile are independent
-          // and in flight together; partials are added in CTA order
+          // 16 rows at a time, up to 8 partials per batch: the 128 loads of a
+          // batch are independent and in flight together (one round trip for
+          // the usual handful of contributors); partials are still added in
+          // CTA order, so the sum does not depend on who finished last
+          constexpr int kPB = 8;
           for (int n0 = 0; n0 < p.ntile; n0 += 16) {
             float acc[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-            for (int j = 0; j < cnt; ++j) {
-              const float *src = p.part + s_base[j] + static_cast<long long>(n0) * 128 + row;
-              float v[16];
+            for (int j0 = 0; j0 < cnt; j0 += kPB) {
+              float v[kPB][16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] = __ldcg(src + k * 128);
+              for (int jj = 0; jj < kPB; ++jj) {
+                const bool in = j0 + jj < cnt;
+                const float *src =
+                    p.part + (in ? s_base[j0 + jj] : 0) + static_cast<long long>(n0) * 128 + row;
 #pragma unroll
-              for (int k = 0; k < 16; ++k) acc[k] += v[k];
+                for (int k = 0; k < 16; ++k) v[jj][k] = in ? __ldcg(src + k * 128) : 0.f;
+              }
+#pragma unroll
+              for (int jj = 0; jj < kPB; ++jj)
+#pragma unroll
+                for (int k = 0; k < 16; ++k) acc[k] += v[jj][k];
             }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
