@@ -18,91 +18,16 @@
 #include "attention_common.cuh"
 
 namespace dflash {
-namespace {
 
-// ----------------------------------------------------------- main (SIMT)
-// grid (S, nkv, B); 8 warps, warp w handles the group's query rows w, w+8, ...
-template <int QK_PER_LANE, int V_PER_LANE>
-__global__ void __launch_bounds__(256) attn_split_simt_kernel(const AttnParams p) {
-  griddep_launch();
-  const int s = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  SegRange sr = segment_range(p, r, s);
-  const int rows = p.Tq * p.G;
-  for (int rho = warp; rho < rows; rho += 8) {
-    const int i = rho / p.G, h = kvh * p.G + rho % p.G;
-    const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
-    int lo, hi;
-    row_key_range(p, sr.kv_len, i, &lo, &hi);
-    lo = max(lo, sr.k0);
-    hi = min(hi, sr.k1 - 1);
-    if (sr.k0 >= sr.k1 || hi < lo) {
-      if (lane == 0) {
-        p.ws_m[wsi] = -INFINITY;
-        p.ws_l[wsi] = 0.f;
-      }
-      continue;
-    }
-    float qv[QK_PER_LANE];
-    const uint16_t *qrow = p.q + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.dq;
-    const uint16_t *qrrow =
-        p.q_rope ? p.q_rope + ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.drope : nullptr;
-#pragma unroll
-    for (int e = 0; e < QK_PER_LANE; ++e) {
-      const int d = lane + 32 * e;
-      float v = 0.f;
-      if (d < p.dq) v = bf16_to_f32(qrow[d]);
-      else if (qrrow && d < p.dq + p.drope) v = bf16_to_f32(qrrow[d - p.dq]);
-      qv[e] = v;
-    }
-    float o[V_PER_LANE];
-#pragma unroll
-    for (int e = 0; e < V_PER_LANE; ++e) o[e] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    for (int j = lo; j <= hi; ++j) {
-      const uint16_t *krow, *vrow;
-      if (!key_rows(p, r, kvh, j, &krow, &vrow)) continue;
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < QK_PER_LANE; ++e) {
-        const int d = lane + 32 * e;
-        if (d < p.dqk) dot += qv[e] * bf16_to_f32(krow[d]);
-      }
-      dot = warp_sum(dot) * p.scale;
-      const float mn = fmaxf(m, dot);
-      const float corr = __expf(m - mn);
-      const float pj = __expf(dot - mn);
-      l = l * corr + pj;
-#pragma unroll
-      for (int e = 0; e < V_PER_LANE; ++e) {
-        const int d = lane + 32 * e;
-        const float vv = d < p.dv ? bf16_to_f32(vrow[d]) : 0.f;
-        o[e] = o[e] * corr + pj * vv;
-      }
-      m = mn;
-    }
-    if (lane == 0) {
-      p.ws_m[wsi] = m;
-      p.ws_l[wsi] = l;
-    }
-    if (m != -INFINITY) {
-      float *orow = p.ws_o + wsi * p.dv;
-#pragma unroll
-      for (int e = 0; e < V_PER_LANE; ++e) {
-        const int d = lane + 32 * e;
-        if (d < p.dv) orow[d] = o[e];
-      }
-    }
-  }
-}
-
-}  // namespace
+// The main kernels live in attention_tc.cu (GQA) and attention_mla_tc.cu
+// (MLA latent); this file holds the merge, the segment count and dispatch.
 
 // ----------------------------------------------------------- merge
 // One CTA per output row (r, i, h), one thread per value dim.  Segments are
-// merged in batches of 16 with a running maximum (online log-sum-exp): all
-// loads of a batch (m_s, l_s and the thread's O element) are issued before any
-// is used, so a row of up to 16 segments costs one memory round trip.  The
+// merged in batches of 32 (16 for 512-wide rows) with a running maximum
+// (online log-sum-exp): all loads of a batch (m_s, l_s and the thread's O
+// element) are issued before any is used, so a row of up to one batch of
+// segments costs one memory round trip.  The
 // sink starts the running state as an extra logit with no value.  O of an
 // empty segment (m_s = -inf) is loaded but never used (selected away), so a
 // NaN there cannot leak.
@@ -154,7 +79,9 @@ __global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
 int attention_num_segments(const dflash_geom &g, int B, int Tq) {
   const int heads = (g.kind == DFLASH_KIND_GQA) ? g.nkv : 1;
   const int rows = Tq * (g.hq / (heads > 0 ? heads : 1));
-  const int row_tiles = (rows + 127) / 128;
+  // query rows per CTA: 128 for GQA, 64 for the MLA latent (512-wide values)
+  const int tile_rows = (g.kind == DFLASH_KIND_GQA) ? 128 : mla_rows_per_cta();
+  const int row_tiles = (rows + tile_rows - 1) / tile_rows;
   // the tensor-core kernel runs one CTA per SM
   const long long slots = static_cast<long long>(device_sm_count());
   const long long ctas = static_cast<long long>(B) * heads * row_tiles;
@@ -185,12 +112,10 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
   AttnParams p = make_attn_params(g, B, layer, Tq, q, q_rope, pool, tbl, kv_len, window, sinks,
                                   scale, mask_mode, S, ws, out, st);
   cudaError_t e;
-  if (g.kind == DFLASH_KIND_GQA) {
+  if (g.kind == DFLASH_KIND_GQA)
     e = launch_attn_tc(p, g, s);
-  } else {
-    attn_split_simt_kernel<18, 16><<<dim3(S, 1, B), 256, 0, s>>>(p);
-    e = cudaGetLastError();
-  }
+  else
+    e = launch_attn_mla_tc(p, g, s);
   if (e != cudaSuccess) return e;
   return launch_attn_merge(p, s);
 }

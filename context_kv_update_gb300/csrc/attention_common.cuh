@@ -75,6 +75,8 @@ inline AttnParams make_attn_params(const dflash_geom &g, int B, int layer, int T
 
 cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s);
+cudaError_t launch_attn_mla_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s);
+int mla_rows_per_cta();
 
 // kv_len of request r, clamped to [0, M*P] (flagging out-of-range values).
 __device__ __forceinline__ int clamped_kv_len(const AttnParams &p, int r, bool report) {

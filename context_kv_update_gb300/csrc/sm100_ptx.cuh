@@ -315,9 +315,11 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t tile_addr, int k1
 // unless `b_mn_major` (B stored N-contiguous): D format bits 4-5 (1 = f32),
 // A format bits 7-9 and B format bits 10-12 (1 = bf16), B-major bit 16,
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false,
+                                                      bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
 }  // namespace ptx
