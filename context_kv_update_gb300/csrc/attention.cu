@@ -82,7 +82,7 @@ int attention_num_segments(const dflash_geom &g, int B, int Tq) {
   // query rows per CTA: 128 for GQA, 64 for the MLA latent (512-wide values)
   const int tile_rows = (g.kind == DFLASH_KIND_GQA) ? 128 : mla_rows_per_cta();
   const int row_tiles = (rows + tile_rows - 1) / tile_rows;
-  // the tensor-core kernel runs one CTA per SM
+  // the tensor-core kernels run one CTA per SM
   const long long slots = static_cast<long long>(device_sm_count());
   const long long ctas = static_cast<long long>(B) * heads * row_tiles;
   int S = static_cast<int>(slots / (ctas > 0 ? ctas : 1));

@@ -27,10 +27,14 @@
 // each thread accumulates its key's share of the row sums, reduced across
 // the 128 keys once at the end.
 //
-// A tile is loaded chunk by chunk: chunk c of tile t+1 is issued as soon as
-// the PV block that last read its slot has completed, and QK of tile t+1
-// starts on chunk 0 while the others are still landing.  Every wait is a
-// bounded mbarrier try_wait; a timeout raises DFLASH_DEV_WAIT_TIMEOUT.
+// A tile is loaded chunk by chunk: chunks 2b, 2b+1 of tile t+1 are issued as
+// soon as PV block b of tile t has released their slots (the rope chunk once
+// the whole PV is done), and QK of tile t+1 starts on chunk 0 while the
+// others are still landing.  The 18 TMA boxes of a tile (9 chunks x 2 pages
+// of 64 keys) are issued by 18 different lanes: copies issued by one thread
+// complete one after another, so a single issuing thread would cap the load
+// rate of the CTA far below what L2 delivers.  Every mbarrier wait is a
+// bounded try_wait; a timeout raises DFLASH_DEV_WAIT_TIMEOUT.
 #include <cuda.h>
 
 #include <algorithm>
@@ -58,7 +62,7 @@ constexpr uint32_t kSlotOff = kChunks * kQChunkBytes;
 constexpr uint32_t kBarOff = kSlotOff + kChunks * kChunkBytes;
 constexpr int kNumBars = 19;
 constexpr uint32_t kXOff = (kBarOff + kNumBars * 8 + 8 + 15) & ~15u;
-constexpr uint32_t kXBytes = (2 * 64 + 64 * 4 + 64 * 4) * 4;  // m_ref[2][64], xm, xl
+constexpr uint32_t kXBytes = (2 * 64 + 64 * 4 + 64 * 4) * 4 + 64 * 8;  // m_ref[2][64], xm, xl, roff
 constexpr uint32_t kSmemBytes = 1024 + kXOff + kXBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory plan");
 constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
@@ -77,18 +81,26 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int unit16) {
   return static_cast<uint32_t>(row * 128 + ((unit16 ^ (row & 7)) << 4));
 }
 
-// fp32 <-> int with the same order (for the integer warp max)
-__device__ __forceinline__ int ordered(float x) {
-  const int i = __float_as_int(x);
-  return i >= 0 ? i : i ^ 0x7fffffff;
-}
-__device__ __forceinline__ float unordered(int i) {
-  return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff);
-}
-__device__ __forceinline__ int warp_max_int(int v) {
-  int r;
-  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
+// Reduce 64 per-lane values across the warp, one row per value: after five
+// exchange steps (32 + 16 + 8 + 4 + 2 shuffles instead of 5 per row) lane L
+// holds the results of rows 2L and 2L + 1 in v[0], v[1] (at the step that
+// exchanges lane bit o, the lane with that bit set keeps the upper half).
+// MAX selects fmaxf, else addition.
+template <bool MAX>
+__device__ __forceinline__ void warp_transpose_reduce64(float (&v)[64], int lane) {
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int o = 16 >> st;      // lane bit exchanged at this step
+    const int half = 32 >> st;   // values kept per lane after the step
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = upper ? v[j] : v[j + half];
+      const float keep = upper ? v[j + half] : v[j];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -113,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *m_ref = reinterpret_cast<float *>(sm + kXOff);  // [2][64], log2 units
   float *xm = m_ref + 128;                              // [64 rows][4 warps]
   float *xl = xm + 256;                                 // [64 rows][4 warps]
+  long long *roff = reinterpret_cast<long long *>(xl + 256);  // [64 rows] workspace row
 
   const int s = blockIdx.x / P.RT, rg = blockIdx.x % P.RT;
   const int r = blockIdx.z;
@@ -202,22 +215,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt = fetch_page(t + tiles_per_batch);
       }
       const int kbase = (sr.t0 + t) * kKT;
-      for (int c = 0; c < kChunks; ++c) {
+      // groups of slots released together: chunks {0,1}, {2,3}, {4,5},
+      // {6,7} by PV blocks 0-3 of the previous tile, the rope chunk by its end
+      for (int grp = 0; grp < 5 && ok; ++grp) {
+        const int c_lo = 2 * grp, c_hi = grp < 4 ? 2 * grp + 2 : kChunks;
         bool got = true;
         if (lane == 0 && t > 0) {
-          // the slot was last read by PV block c/2 of tile t-1 (the rope
-          // slot, holding P^T, by the whole PV of tile t-1)
-          uint64_t *bar = (c == kRopeSlot) ? o_done : &blk_empty[c >> 1];
+          uint64_t *bar = grp < 4 ? &blk_empty[grp] : o_done;
           got = ptx::mbar_wait(ptx::smem_u32(bar), static_cast<uint32_t>((t - 1) & 1), abort_flag);
         }
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&ch_full[c]), kChunkBytes);
-        for (int b = 0; b < boxes; ++b) {
+        if (lane == 0)
+          for (int c = c_lo; c < c_hi; ++c)
+            ptx::mbar_arrive_expect_tx(ptx::smem_u32(&ch_full[c]), kChunkBytes);
+        __syncwarp();
+        // box j = c * boxes + b of the tile is issued by lane j % 32
+        for (int j = c_lo * boxes; j < c_hi * boxes; ++j) {
+          const int c = j / boxes, b = j % boxes;
           const int page = __shfl_sync(0xffffffffu, cur, tb * boxes + b);
-          if (lane == 0) {
+          if (lane == (j & 31)) {
             const int key0 = kbase + b * P.box_rows;
             const long long row0 =
                 (static_cast<long long>(p.layer) * p.NP + page) * p.P + key0 % p.P;
@@ -225,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              c * 64, static_cast<int32_t>(row0), ptx::smem_u32(&ch_full[c]));
           }
         }
-        last_fill[c] = t;
+        for (int c = c_lo; c < c_hi; ++c) last_fill[c] = t;
       }
     }
     if (!ok && lane == 0) {
@@ -327,7 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *mr = m_ref + 64 * cur;
       bool need = false;
 #pragma unroll
-      for (int c = 0; c < kRowsN; ++c) need |= sv[c] * P.scale_log2 > mr[c] + 8.f;
+      for (int c4 = 0; c4 < kRowsN / 4; ++c4) {
+        const float4 m4 = *reinterpret_cast<const float4 *>(mr + 4 * c4);
+        need |= sv[4 * c4] * P.scale_log2 > m4.x + 8.f;
+        need |= sv[4 * c4 + 1] * P.scale_log2 > m4.y + 8.f;
+        need |= sv[4 * c4 + 2] * P.scale_log2 > m4.z + 8.f;
+        need |= sv[4 * c4 + 3] * P.scale_log2 > m4.w + 8.f;
+      }
       if (ptx::bar_or(2, 128, need || !got)) {
         // ---- rebuild m_ref: exact tile maxima, rescale O^T and the row sums
         if (ptx::bar_or(3, 128, !got)) {
@@ -338,10 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t > 0)
           got_o = ptx::mbar_wait(ptx::smem_u32(o_done), static_cast<uint32_t>((t - 1) & 1),
                                  abort_flag);
+        {
+          float mx[kRowsN];
 #pragma unroll
-        for (int c = 0; c < kRowsN; ++c) {
-          const float m = unordered(warp_max_int(ordered(sv[c])));
-          if (lane == (c & 31)) xm[c * 4 + q4] = m;
+          for (int c = 0; c < kRowsN; ++c) mx[c] = sv[c];
+          warp_transpose_reduce64<true>(mx, lane);
+          const int row0 = 2 * lane;
+          xm[row0 * 4 + q4] = mx[0];
+          xm[(row0 + 1) * 4 + q4] = mx[1];
         }
         if (ptx::bar_or(2, 128, !got_o)) {
           bad = true;
@@ -349,12 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         float *mn = m_ref + 64 * (cur ^ 1);
-#pragma unroll 4
-        for (int c = 0; c < kRowsN; ++c) {
+        if (q4 < 2) {  // one row per thread
+          const int c = 32 * q4 + lane;
           const float4 w4 = *reinterpret_cast<const float4 *>(xm + c * 4);
           const float tmax = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w)) * P.scale_log2;
           const float old = mr[c];
-          mn[c] = (old == -INFINITY || tmax > old + 8.f) ? tmax : old;  // same value in every thread
+          mn[c] = (old == -INFINITY || tmax > old + 8.f) ? tmax : old;
         }
         ptx::bar_sync(2, 128);
 #pragma unroll
@@ -385,12 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint32_t pk[4];
+        const float4 ma = *reinterpret_cast<const float4 *>(m2 + 8 * u);
+        const float4 mb = *reinterpret_cast<const float4 *>(m2 + 8 * u + 4);
+        const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = 8 * u + 2 * e;
-          const float p0 = sv[c] == -INFINITY ? 0.f : ptx::ex2(fmaf(sv[c], P.scale_log2, -m2[c]));
-          const float p1 =
-              sv[c + 1] == -INFINITY ? 0.f : ptx::ex2(fmaf(sv[c + 1], P.scale_log2, -m2[c + 1]));
+          const float p0 =
+              sv[c] == -INFINITY ? 0.f : ptx::ex2(fmaf(sv[c], P.scale_log2, -mm[2 * e]));
+          const float p1 = sv[c + 1] == -INFINITY
+                               ? 0.f
+                               : ptx::ex2(fmaf(sv[c + 1], P.scale_log2, -mm[2 * e + 1]));
           lp[c] += p0;
           lp[c + 1] += p1;
           pk[e] = ptx::pack_bf16x2(p0, p1);
@@ -410,19 +444,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    abort_flag));
       ptx::tc_fence_after();
     }
-#pragma unroll
-    for (int c = 0; c < kRowsN; ++c) {
-      const float v = warp_sum(lp[c]);
-      if (lane == (c & 31)) xl[c * 4 + q4] = v;
+    warp_transpose_reduce64<false>(lp, lane);
+    {
+      const int row0 = 2 * lane;
+      xl[row0 * 4 + q4] = lp[0];
+      xl[(row0 + 1) * 4 + q4] = lp[1];
+    }
+    // per-row workspace offsets, computed once
+    if (q4 < 2) {
+      const int c = 32 * q4 + lane;
+      const int R = R0 + c;
+      long long off = -1;
+      if (R < P.GT) {
+        const int i = R / p.hq, h = R % p.hq;
+        off = static_cast<long long>(((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s);
+      }
+      roff[c] = off;
     }
     const bool any_bad = ptx::bar_or(2, 128, !okf && ntiles > 0);
     const float *mf = m_ref + 64 * cur;
     if (q4 < 2) {
       const int c = 32 * q4 + lane;
-      const int R = R0 + c;
-      if (R < P.GT) {
-        const int i = R / p.hq, h = R % p.hq;
-        const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
+      const long long wsi = roff[c];
+      if (wsi >= 0) {
         const bool any = !any_bad && ntiles > 0 && mf[c] != -INFINITY;
         const float4 l4 = *reinterpret_cast<const float4 *>(xl + c * 4);
         p.ws_m[wsi] = any ? mf[c] * kLn2 : -INFINITY;
@@ -430,21 +474,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!any_bad && ntiles > 0) {
+      // O^T (dims in lanes) -> O rows in the idle tile slots [64 rows][512]
+      // (bank-conflict-free: a warp writes 32 consecutive dims of one row),
+      // then every row leaves as coalesced 16-byte stores
+      float *stage = reinterpret_cast<float *>(sSlot);
       for (int b = 0; b < 4; ++b) {
-        const int d = b * 128 + 32 * q4 + lane;  // value dim of this TMEM lane
+        const int d = b * 128 + 32 * q4 + lane;
         for (int c0 = 0; c0 < kRowsN; c0 += 16) {
           uint32_t ov[16];
           ptx::tmem_ld16_sync(tm_o + lane_off + b * kRowsN + c0, ov);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c0 + e, R = R0 + c;
-            if (R < P.GT && mf[c] != -INFINITY) {
-              const int i = R / p.hq, h = R % p.hq;
-              const size_t wsi = ((static_cast<size_t>(r) * p.Tq + i) * p.hq + h) * p.S + s;
-              p.ws_o[wsi * kLat + d] = __uint_as_float(ov[e]);
-            }
-          }
+          for (int e = 0; e < 16; ++e) stage[(c0 + e) * kLat + d] = __uint_as_float(ov[e]);
         }
+      }
+      ptx::bar_sync(2, 128);
+      const int tid = threadIdx.x - 128;
+#pragma unroll 4
+      for (int q = tid; q < kRowsN * kLat / 4; q += 128) {
+        const int c = q / (kLat / 4), c4 = q % (kLat / 4);
+        const long long wsi = roff[c];
+        if (wsi >= 0 && mf[c] != -INFINITY)
+          reinterpret_cast<float4 *>(p.ws_o + wsi * kLat)[c4] =
+              reinterpret_cast<const float4 *>(stage)[q];
       }
     }
   }

@@ -225,24 +225,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         break;
       }
       if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
+      __syncwarp();
+      // The tile's boxes (page x K/V x 64-dim chunk) are issued by different
+      // lanes: copies issued by one thread complete one after another, so
+      // the number of issuing threads bounds the load rate of a CTA.
       const int kbase = (sr.t0 + t) * kKT;
       uint8_t *stage = sKV + st * P.stage_bytes;
-      for (int b = 0; b < boxes; ++b) {
+      const int nbox = boxes * 2 * P.chunks;
+      for (int j0 = 0; j0 < nbox; j0 += 32) {
+        const int j = j0 + lane;
+        const int b = (j < nbox) ? j / (2 * P.chunks) : 0;
         const int page = __shfl_sync(0xffffffffu, cur, tb * boxes + b);
-        if (lane == 0) {
+        if (j < nbox) {
+          const int kv = (j / P.chunks) & 1, c = j % P.chunks;
           const int key0 = kbase + b * P.box_rows;
-          const int slot0 = key0 % p.P;
-          for (int kv = 0; kv < 2; ++kv) {
-            const long long row0 =
-                ((((static_cast<long long>(p.layer) * p.NP + page) * 2 + kv) * p.nkv + kvh) * p.P) +
-                slot0;
-            for (int c = 0; c < P.chunks; ++c) {
-              const uint32_t dst = ptx::smem_u32(stage + kv * P.k_bytes + c * kVChunk +
-                                                 b * P.box_rows * 128);
-              ptx::tma_load_2d(dst, &tm, c * 64, static_cast<int32_t>(row0),
-                               ptx::smem_u32(&kv_full[st]));
-            }
-          }
+          const long long row0 =
+              ((((static_cast<long long>(p.layer) * p.NP + page) * 2 + kv) * p.nkv + kvh) * p.P) +
+              key0 % p.P;
+          const uint32_t dst =
+              ptx::smem_u32(stage + kv * P.k_bytes + c * kVChunk + b * P.box_rows * 128);
+          ptx::tma_load_2d(dst, &tm, c * 64, static_cast<int32_t>(row0), ptx::smem_u32(&kv_full[st]));
         }
       }
       ++issued;

@@ -90,68 +90,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long t_first = u_lo / KB, t_last = (u_hi - 1) / KB;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer
-      // (t, kb, m, nt) and (stage, phase) advance incrementally: no divisions
-      // in the loop.
-      const uint64_t pol_w = ptx::policy_evict_first();
-      struct Cursor {
-        long long t;
-        int kb, m, nt;
-      };
-      const Cursor start{t_first, static_cast<int>(u_lo - t_first * KB),
-                         static_cast<int>(t_first % p.mtiles), static_cast<int>(t_first / p.mtiles)};
-      auto advance = [&](Cursor &q) {
-        if (++q.kb == p.kblocks) {
-          q.kb = 0;
-          ++q.t;
-          if (++q.m == p.mtiles) {
-            q.m = 0;
-            ++q.nt;
-          }
+    // ---------------- TMA producer (warp 0)
+    // (t, kb, m, nt) and (stage, phase) advance incrementally: no divisions
+    // in the loop.  Lane 0 waits for free slots and arms the barriers; the
+    // two copies of unit i are issued by lanes 2(i%16) and 2(i%16)+1, since
+    // copies issued by one thread complete one after another.
+    const uint64_t pol_w = ptx::policy_evict_first();
+    struct Cursor {
+      long long t;
+      int kb, m, nt;
+    };
+    const Cursor start{t_first, static_cast<int>(u_lo - t_first * KB),
+                       static_cast<int>(t_first % p.mtiles), static_cast<int>(t_first / p.mtiles)};
+    auto advance = [&](Cursor &q) {
+      if (++q.kb == p.kblocks) {
+        q.kb = 0;
+        ++q.t;
+        if (++q.m == p.mtiles) {
+          q.m = 0;
+          ++q.nt;
         }
-      };
-      const int total = static_cast<int>(u_hi - u_lo);
-      const int pre = std::min(S, total);
-      bool ok = true;
-      // Prologue: weight tiles of the first ring slots do not depend on the
-      // previous kernel, so they are in flight before the dependency wait.
-      Cursor q = start;
-      for (int i = 0; i < pre; ++i, advance(q)) {
+      }
+    };
+    const int total = static_cast<int>(u_hi - u_lo);
+    const int pre = std::min(S, total);
+    bool ok = true;
+    // Prologue: weight tiles of the first ring slots do not depend on the
+    // previous kernel, so they are in flight before the dependency wait.
+    Cursor q = start;
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i)
         ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[i]), abytes + bbytes);
+    __syncwarp();
+    for (int i = 0; i < pre; ++i, advance(q))
+      if (lane == 2 * (i & 15))
         ptx::tma_load_2d_hint(ptx::smem_u32(sA + i * abytes), &tmW, q.kb * 64, q.m * 128,
                               ptx::smem_u32(&full[i]), pol_w);
-      }
-      if (p.pdl_wait) griddep_wait();
-      q = start;
-      for (int i = 0; i < pre; ++i, advance(q))
+    if (p.pdl_wait) griddep_wait();
+    q = start;
+    for (int i = 0; i < pre; ++i, advance(q))
+      if (lane == 2 * (i & 15) + 1)
         ptx::tma_load_2d(ptx::smem_u32(sB + i * bbytes), &tmX, q.kb * 64, q.nt * p.ntile,
                          ptx::smem_u32(&full[i]));
-      int issued = pre;
-      int st = pre % S;
-      uint32_t ph = (pre / S) & 1;
-      for (int i = pre; i < total; ++i, advance(q)) {
-        if (!ptx::mbar_spin(ptx::smem_u32(&empty[st]), ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[st]), abytes + bbytes);
+    int issued = pre;
+    int st = pre % S;
+    uint32_t ph = (pre / S) & 1;
+    for (int i = pre; i < total; ++i, advance(q)) {
+      bool got = true;
+      if (lane == 0) got = ptx::mbar_spin(ptx::smem_u32(&empty[st]), ph ^ 1u, abort_flag);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[st]), abytes + bbytes);
+      __syncwarp();
+      if (lane == 2 * (i & 15))
         ptx::tma_load_2d_hint(ptx::smem_u32(sA + st * abytes), &tmW, q.kb * 64, q.m * 128,
                               ptx::smem_u32(&full[st]), pol_w);
+      if (lane == 2 * (i & 15) + 1)
         ptx::tma_load_2d(ptx::smem_u32(sB + st * bbytes), &tmX, q.kb * 64, q.nt * p.ntile,
                          ptx::smem_u32(&full[st]));
-        ++issued;
-        if (++st == S) {
-          st = 0;
-          ph ^= 1u;
-        }
+      ++issued;
+      if (++st == S) {
+        st = 0;
+        ph ^= 1u;
       }
-      if (!ok) {
-        // wind down: let the copies already issued land before the CTA exits
-        for (int it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
-          volatile int dummy = 0;
-          ptx::mbar_wait(ptx::smem_u32(&full[it % S]), static_cast<uint32_t>((it / S) & 1), &dummy);
-        }
+    }
+    if (!ok && lane == 0) {
+      // wind down: let the copies already issued land before the CTA exits
+      for (int it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(&full[it % S]), static_cast<uint32_t>((it / S) & 1), &dummy);
       }
     }
   } else if (warp == 1) {

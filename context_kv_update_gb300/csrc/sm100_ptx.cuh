@@ -109,6 +109,17 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
 
 // 2-D tiled bulk tensor load global -> shared, completing on `bar`.
 // c0 is the innermost coordinate (elements), c1 the row.
+// 2-D tiled load into the same shared-memory offset of every CTA of the
+// cluster in `cta_mask`, completing on each CTA's mbarrier at offset `bar`.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *m,
+                                                      int32_t c0, int32_t c1, uint32_t bar,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, int32_t c0,
                                             int32_t c1, uint32_t bar) {
   asm volatile(
@@ -220,6 +231,27 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
+}
+// Arrive on the mbarrier at offset `bar` of every CTA of the cluster in
+// `cta_mask` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Cluster-wide barrier over every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns; thread t gets lane (base + t).
