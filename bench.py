@@ -258,9 +258,10 @@ class Step:
 
 
 def kernel_launches_per_step(g, hidden_is_f32=False) -> int:
-    # bookkeeping 1; update: prep, fc gemm, hidden norm, kv gemm, epilogue = 5;
-    # per layer: scatter 1 + attention (split + merge) 2
-    return 1 + 5 + g["L"] * 3
+    # bookkeeping 1; update: fc gemm, hidden norm, kv gemm, epilogue = 4 (+ the
+    # fp32 -> bf16 prep for fp32 hidden); per layer: scatter 1 + attention
+    # (split + merge) 2
+    return 1 + 4 + (1 if hidden_is_f32 else 0) + g["L"] * 3
 
 
 def make_events(n_layers, count):

@@ -1,14 +1,14 @@
 // bookkeeping.cu -- the per-step drafter bookkeeping in one launch.
 //
 // Follows TensorRT-LLM PR #20550 (Description, TLLM_DFLASH_FUSED_PROLOGUE:
-// "_refresh_ctx_block_tables: page counts and decoded table", the
-// gen-request prologue "bonus token, query and context positions, embedding
-// ids", the context-KV store's "rejected-row mask, clamp to the request's
-// allocation, page lookup", "the ctx_len advance with the clamp, dummy-slot
-// reset and advertised context length") and its follow-up commit
-// "spec_tail_kernels.py" (block-table decode of "clamped and divided
-// offsets"; destination pages / offsets / write mask; seq_lens;
-// DraftBlockPlacement for the block's own positions).
+// the page counts and decoded table of _refresh_ctx_block_tables; the
+// generation prologue's bonus token, query / context positions and embedding
+// ids; the context-KV store's mask of rejected rows, clamp to the request's
+// allocation and page lookup; the clamped ctx_len advance with dummy slots
+// reset and the advertised context length) and its follow-up commit
+// "spec_tail_kernels.py" (block-table decode from clamped, divided offsets;
+// destination pages / offsets / write mask; seq_lens; DraftBlockPlacement
+// for the block's own positions).
 //
 // One CTA per request: the table row is decoded by all threads with a block
 // reduction for the page count; the per-row outputs are one thread per row.

@@ -1,8 +1,8 @@
 // ctx_update.cu -- the per-step context-KV update.
 //
 // Follows TensorRT-LLM PR #20550 (Description, TLLM_DFLASH_OVERLAP_CONTEXT_
-// PROJECTION: "fc + hidden_norm + latent GEMM + RMSNorm/RoPE" on the gen
-// tokens, then the accepted-mask write) and PR #13995 ("migrate draft path to
+// PROJECTION: the fc projection, hidden norm, latent projection and norm +
+// RoPE of the generation tokens, then the masked write of the accepted rows) and PR #13995 ("migrate draft path to
 // per-layer cached K/V pool": one GEMM stacked across the drafter layers on
 // the newly accepted K+1 rows; "fuse cross-layer k_norm and avoid mask-mul
 // alloc": one RMSNorm over [N, L, nkv, hd] with stacked per-layer weights and
@@ -10,12 +10,14 @@
 // convention).
 //
 // Launch chain on the caller's stream:
-//   prep      ctx_len snapshot (+ fp32 -> bf16 of the hidden rows)
+//   prep      fp32 -> bf16 of the hidden rows (fp32 hidden only)
 //   gemm      Y1 = X W_fc^T            (weights streamed once)
-//   norm      hn = bf16(bf16(Y1) * gamma_h / rms)
+//   norm      hn = bf16(bf16(Y1) * gamma_h / rms), ctx_len snapshot
 //   gemm      Y2 = hn W_kv^T           (all layers' K/V rows in one pass)
 //   epilogue  k RMSNorm + RoPE (GQA) / latent RMSNorm + RoPE (MLA), masked
 //             paged bf16 store, ctx_len advance
+// Y1 and Y2 stay as the GEMMs' per-CTA partial tiles; the norm and the
+// epilogue add them up as they read (gemm_out_issue / gemm_out_finish).
 #include "dflash_internal.cuh"
 #include "gemm_tc.cuh"
 
@@ -25,14 +27,10 @@ namespace {
 // ----------------------------------------------------------- workspace map
 struct CtxWs {
   int32_t *ctx_snap;  // [B]
-  int *counters;      // stream-K tile tickets: fc tiles, then K/V tiles
-  int n_counters;
   uint16_t *x;        // [Npad, D_in] bf16 (fp32 hidden converted)
   uint16_t *hn;       // [Npad, D]    bf16
-  float *y1;          // [N, D]     fc output
-  float *y2;          // [N, Wrows] K/V (or latent) projection
-  float *part1;       // fc partial tiles
-  float *part2;       // K/V partial tiles
+  float *part1;       // fc partial tiles (Y1)
+  float *part2;       // K/V (or latent) partial tiles (Y2)
   size_t bytes;
 };
 
@@ -58,13 +56,6 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
   CtxWs w;
   w.ctx_snap = reinterpret_cast<int32_t *>(p + off);
   off = align_up(off + sizeof(int32_t) * (B > 0 ? B : 1), 256);
-  w.counters = reinterpret_cast<int *>(p + off);
-  w.n_counters = gemm_num_tiles(d.D, d.Npad) + gemm_num_tiles(d.Wrows, d.Npad);
-  off = align_up(off + sizeof(int) * w.n_counters, 256);
-  w.y1 = reinterpret_cast<float *>(p + off);
-  off = align_up(off + sizeof(float) * d.Npad * d.D, 256);
-  w.y2 = reinterpret_cast<float *>(p + off);
-  off = align_up(off + sizeof(float) * static_cast<size_t>(d.Npad) * d.Wrows, 256);
   w.x = reinterpret_cast<uint16_t *>(p + off);
   off = align_up(off + sizeof(uint16_t) * d.Npad * d.D_in, 256);
   w.hn = reinterpret_cast<uint16_t *>(p + off);
@@ -79,39 +70,85 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
 
 // ------------------------------------------------------------------ prep
 __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, int row_elems,
-                            int n_pad_rows, const int32_t *ctx_len, int32_t *ctx_snap, int B,
-                            int *counters, int n_counters) {
+                            int n_pad_rows) {
   griddep_launch();
   griddep_wait();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-  if (tid < B) ctx_snap[tid] = ctx_len[tid];
-  for (int k = tid; k < n_counters; k += gridDim.x * blockDim.x) counters[k] = 0;
-  if (hidden_f32 == nullptr) return;
   const int total = n_pad_rows * row_elems;
   for (int e = tid; e < total; e += gridDim.x * blockDim.x)
     x[e] = e < n_elems ? f32_to_bf16_rn(hidden_f32[e]) : static_cast<uint16_t>(0);
 }
 
 // ----------------------------------------------------- hidden RMSNorm
-// One CTA per row: h = bf16(sum of partials), hn = bf16(h * g / rms(h)).
-__global__ void __launch_bounds__(1024) hidden_norm_kernel(const float *y, const uint16_t *gamma,
-                                                           uint16_t *hn, int D, float eps) {
-  __shared__ float red[32];
-  extern __shared__ float hbuf[];  // [D]
+// hn = bf16(h * gamma_h / rms(h)), h = bf16(Y1 row).  A cluster of G CTAs
+// normalises one row, each CTA `cols` consecutive columns; the row's sum of
+// squares is added up across the cluster through distributed shared memory,
+// in rank order (deterministic).  Each thread issues the loads of all its
+// columns' partials before adding any.  The CTAs are small (128 threads), so
+// they share the SMs with the GEMMs: the K/V GEMM's CTAs start and prefetch
+// their weights while this kernel runs.  CTA (0, 0) also snapshots ctx_len
+// for the epilogue, which advances it.
+constexpr int kNormThreads = 128;
+constexpr int kNormMaxCols = 8 * kNormThreads;  // columns per CTA
+
+__global__ void __launch_bounds__(kNormThreads) hidden_norm_kernel(
+    const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, int cols, float eps,
+    const int32_t *ctx_len, int32_t *ctx_snap, int B) {
+  constexpr int E = kNormMaxCols / kNormThreads;
+  __shared__ float red[kNormThreads / 32];
+  __shared__ float s_part;
+  __shared__ int parts[E + 1];  // partial count of each 128-column tile the CTA covers
   griddep_launch();
-  griddep_wait();
-  const int n = blockIdx.x;
-  const float *row = y + static_cast<size_t>(n) * D;
-  float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const float h = bf16_to_f32(f32_to_bf16_rn(row[d]));
-    hbuf[d] = h;
-    ss += h * h;
+  const int x = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
+  const int c0 = x * cols, c1 = min(D, c0 + cols);
+  float gv[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int col = c0 + i * kNormThreads + tid;
+    gv[i] = col < c1 ? bf16_to_f32(gamma[col]) : 0.f;  // independent of the previous kernel
   }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / static_cast<float>(D) + eps);
-  for (int d = threadIdx.x; d < D; d += blockDim.x)
-    hn[static_cast<size_t>(n) * D + d] = f32_to_bf16_rn(hbuf[d] * inv * bf16_to_f32(gamma[d]));
+  griddep_wait();
+  if (n == 0 && x == 0)
+    for (int r = tid; r < B; r += kNormThreads) ctx_snap[r] = ctx_len[r];
+  const int nt = n / y.ntile, nr = n - nt * y.ntile;
+  const unsigned tb = static_cast<unsigned>(nt) * y.mtiles + static_cast<unsigned>(c0 >> 7);
+  if (c1 > c0 && tid <= ((c1 - 1) >> 7) - (c0 >> 7)) parts[tid] = gemm_tile_parts(y, tb + tid);
+  __syncthreads();
+  GemmOutLoad ld[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int col = c0 + i * kNormThreads + tid;
+    const int j = (col >> 7) - (c0 >> 7);
+    gemm_out_issue(y, tb + j, col < c1 ? parts[j] : 0, nr, col & 127, ld[i]);
+  }
+  float h[E], ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    h[i] = bf16_to_f32(f32_to_bf16_rn(gemm_out_finish(y, ld[i])));
+    ss += h[i] * h[i];
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kNormThreads / 32; ++w) t += red[w];
+    s_part = t;
+  }
+  ptx::cluster_sync();  // every CTA's s_part is written
+  // lane r reads CTA r's part (one round trip for all); the butterfly sum
+  // leaves the same total in every lane of every warp
+  const int lane = tid & 31;
+  const float tot =
+      warp_sum(lane < static_cast<int>(gridDim.x) ? ptx::ld_dsmem_f32(&s_part, lane) : 0.f);
+  ptx::cluster_arrive();  // done reading the other CTAs' s_part
+  const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int col = c0 + i * kNormThreads + tid;
+    if (col < c1) hn[static_cast<size_t>(n) * D + col] = f32_to_bf16_rn(h[i] * inv * gv[i]);
+  }
+  ptx::cluster_wait();  // no CTA leaves while another may still read its s_part
 }
 
 // ----------------------------------------------------------- write mask
@@ -128,12 +165,14 @@ struct MaskArgs {
 // Destination of context row (r, i), or false when the row is not written.
 __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, int *page, int *slot,
                                              int *pos, bool report) {
+  // the row's scalars are independent loads, issued together
   const int n = m.n_acc[r];
   const int c = m.ctx_snap[r];
+  const int A = m.alloc_limit[r];
   const bool live = m.valid ? (m.valid[r] != 0) : true;
   if (!live || n < 1 || n > m.T || c < 0 || i >= n) return false;
   const int p = c + i;
-  if (p >= m.alloc_limit[r]) return false;
+  if (p >= A) return false;
   const int lp = p / m.P;
   if (lp >= m.M) return false;
   const int pg = m.tbl[static_cast<int64_t>(r) * m.M + lp];
@@ -150,7 +189,7 @@ __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, in
 
 // ------------------------------------------------------ GQA epilogue
 // grid (N rows, L*2*nkv heads), block = head_dim threads.
-__global__ void epilogue_gqa_kernel(const float *y, int ldy, const MaskArgs m, const RopeFreqs rf,
+__global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_k, uint16_t *pool, int L, int nkv,
                                     int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
@@ -170,13 +209,20 @@ __global__ void epilogue_gqa_kernel(const float *y, int ldy, const MaskArgs m, c
       ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
     }
   }
+  // the Y2 loads go out first, overlapping the destination lookup
+  GemmOutLoad ld;
+  {
+    const int col = head * hd + d, nt = n / y.ntile;
+    const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
+    gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
+  }
   const int r = n / m.T, i = n % m.T;
   int page, slot, pos;
   if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && d == 0)) return;
   const int l = head / (2 * nkv);
   const int kv = (head / nkv) & 1;
   const int h = head % nkv;
-  float v = y[static_cast<size_t>(n) * ldy + head * hd + d];
+  float v = gemm_out_finish(y, ld);
   if (kv == 0) {
     const float ss = block_sum(v * v, red);
     const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
@@ -196,7 +242,7 @@ __global__ void epilogue_gqa_kernel(const float *y, int ldy, const MaskArgs m, c
 
 // ------------------------------------------------------ MLA epilogue
 // grid (N rows, L), block = lat + rope threads.
-__global__ void epilogue_mla_kernel(const float *y, int ldy, const MaskArgs m, const RopeFreqs rf,
+__global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_kv, uint16_t *pool, int L, int lat,
                                     int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
@@ -216,10 +262,16 @@ __global__ void epilogue_mla_kernel(const float *y, int ldy, const MaskArgs m, c
       ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
     }
   }
+  GemmOutLoad ld;
+  {
+    const int col = l * W + d, nt = n / y.ntile;
+    const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
+    gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
+  }
   const int r = n / m.T, i = n % m.T;
   int page, slot, pos;
   if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) return;
-  const float v = y[static_cast<size_t>(n) * ldy + l * W + d];
+  const float v = gemm_out_finish(y, ld);
   const float ss = block_sum(d < lat ? v * v : 0.f, red);
   float outv;
   if (d < lat) {
@@ -253,13 +305,12 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
   const CtxWs W = ctx_ws_map(g, B, ws);
   cudaError_t e;
 
-  // prep: ctx_len snapshot, fp32 hidden -> bf16
+  // prep: fp32 hidden -> bf16
   const bool f32 = hidden_dtype == DFLASH_DTYPE_F32;
-  {
+  if (f32) {
     const int threads = 256;
-    int blocks = f32 ? (d.Npad * d.D_in + threads - 1) / threads : 1;
+    int blocks = (d.Npad * d.D_in + threads - 1) / threads;
     if (blocks > 4 * device_sm_count()) blocks = 4 * device_sm_count();
-    if (blocks * threads < B) blocks = (B + threads - 1) / threads;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(blocks);
@@ -269,43 +320,47 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, prep_kernel,
-                                f32 ? static_cast<const float *>(hidden) : nullptr, W.x,
-                                d.N * d.D_in, d.D_in, d.Npad, ctx_len, W.ctx_snap, B, W.counters,
-                                W.n_counters)) !=
-        cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, prep_kernel, static_cast<const float *>(hidden), W.x,
+                                d.N * d.D_in, d.D_in, d.Npad)) != cudaSuccess)
       return e;
   }
   const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
 
   // fc GEMM
-  const int n_fc_tiles = gemm_num_tiles(d.D, d.Npad);
-  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, W.y1,
-                       W.counters, /*pdl=*/true, s)) != cudaSuccess)
+  GemmOut y1, y2;
+  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1,
+                       /*pdl=*/true, s, &y1)) != cudaSuccess)
     return e;
 
-  // hidden RMSNorm
+  // hidden RMSNorm: a cluster of G CTAs per row
   {
+    int G = (d.D + 511) / 512;
+    if (G > 8) G = 8;
+    const int cols = (d.D + G - 1) / G;  // <= kNormMaxCols, as d_model <= 8192
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(d.N);
-    cfg.blockDim = dim3(1024);
-    cfg.dynamicSmemBytes = sizeof(float) * d.D;
+    cudaLaunchAttribute attr[2];
+    cfg.gridDim = dim3(G, d.N);
+    cfg.blockDim = dim3(kNormThreads);
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = G;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if ((e = ensure_smem_limit(hidden_norm_kernel, 64 * 1024)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, static_cast<const float *>(W.y1),
-                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
-                                static_cast<float>(g.eps_hidden))) != cudaSuccess)
+    cfg.numAttrs = 2;
+    if (cols > kNormMaxCols) return cudaErrorInvalidValue;
+    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, y1,
+                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D, cols,
+                                static_cast<float>(g.eps_hidden), static_cast<const int32_t *>(ctx_len),
+                                W.ctx_snap, B)) != cudaSuccess)
       return e;
   }
 
   // stacked K/V (or latent) GEMM over every layer
   if ((e = launch_gemm(W.hn, d.N, d.D, static_cast<const uint16_t *>(w.w_kv), d.Wrows, W.part2,
-                       W.y2, W.counters + n_fc_tiles, /*pdl=*/true, s)) != cudaSuccess)
+                       /*pdl=*/true, s, &y2)) != cudaSuccess)
     return e;
 
   // epilogue
@@ -332,14 +387,14 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
     cfg.blockDim = dim3(g.head_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_kernel, static_cast<const float *>(W.y2), d.Wrows, m, rf,
+    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_kernel, y2, m, rf,
                            static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
                            g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else {
     fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers);
     cfg.blockDim = dim3(g.latent_dim + g.rope_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_mla_kernel, static_cast<const float *>(W.y2), d.Wrows, m, rf,
+    e = cudaLaunchKernelEx(&cfg, epilogue_mla_kernel, y2, m, rf,
                            static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
                            g.num_layers, g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k),
                            ctx_len, B);

@@ -7,8 +7,9 @@
 // TMEM lanes 32*(w%4)..+31) and write fp32 partial tiles.  A ring of `stages`
 // shared-memory slots, each one 128x64 weight tile + one NTILEx64 activation
 // tile, is guarded by full/empty mbarriers; two TMEM accumulators by
-// acc_full / acc_empty, so the next tile's MMAs overlap the last one's drain.  Every wait is bounded (ptx::mbar_wait) so a broken pipeline
-// winds the kernel down instead of hanging it.
+// acc_full / acc_empty, so the next tile's MMAs overlap the last one's drain.
+// Every wait is bounded (ptx::mbar_wait) so a broken pipeline winds the
+// kernel down instead of hanging it.
 #include "gemm_tc.cuh"
 
 #include <algorithm>
@@ -18,16 +19,12 @@ namespace dflash {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kMaxParts = 160;  // CTAs sharing one output tile (<= kblocks + 1)
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
-  int K, ntile, mtiles, kblocks, maxt, stages;
-  int M, N;  // output columns (weight rows) and rows (activation rows)
+  int K, ntile, mtiles, kblocks, maxc, stages;
   long long units;
-  float *part;
-  float *y;       // dense result [N, M] fp32
-  int *counters;  // one per output tile, zero between launches
+  float *part;  // [tiles][maxc][ntile][128]
   uint32_t idesc;
   uint32_t tmem_cols;
   int acc_cols;  // TMEM columns per accumulator buffer
@@ -208,15 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: TMEM -> dense result (stream-K fixup)
-    // A tile owned by one CTA is written straight to y.  A shared tile is
-    // written as a partial; the last of its CTAs to finish (per-tile ticket)
-    // sums every partial of the tile in CTA order -- the same order whoever
-    // is last -- and writes y, then resets the ticket for the next launch.
+    // ---------------- epilogue: TMEM -> this CTA's partial of each tile
+    // Tile t's partial j = c - c0(t) holds this CTA's K range of the tile;
+    // the reader adds the partials in CTA order.
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    int *s_last = consumed + 1;  // shared flag written by the ticket holder
-    long long *s_base = reinterpret_cast<long long *>(consumed + 4);  // 8-byte aligned
     int tile_i = 0;
     for (long long t = t_first; t <= t_last; ++t, ++tile_i) {
       const int ab = tile_i & 1;
@@ -226,83 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ptx::bar_or(1, 128, !got)) break;  // the 4 epilogue warps leave together
       ptx::tc_fence_after();
       const long long c0 = ((t * KB + 1) * C - 1) / U;
-      const long long c1 = ((t + 1) * KB * C - 1) / U;
-      const int nt = static_cast<int>(t / p.mtiles);
-      const int m = static_cast<int>(t % p.mtiles) * 128 + row;
-      const int nbase = nt * p.ntile;
-      const bool sole = (c0 == c1);
-      const long long local = t - t_first;
-      float *dst = p.part + ((c * p.maxt + local) * p.ntile) * 128 + row;
+      // c - c0 < maxc by the schedule's bound; checked so that a wrong bound
+      // can never write outside the partial buffer
+      const bool in = c - c0 < p.maxc;
+      float *dst = p.part + ((t * p.maxc + (c - c0)) * p.ntile) * 128 + row;
       for (int n0 = 0; n0 < p.ntile; n0 += 16) {
         uint32_t r[16];
         ptx::tmem_ld16_sync(acc + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
                             r);
+        if (in) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (sole) {
-            const int n = nbase + n0 + j;
-            if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = __uint_as_float(r[j]);
-          } else {
-            dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
-          }
+          for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(n0 + j) * 128] = __uint_as_float(r[j]);
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acc_empty[ab]));
-      if (!sole) {
-        ptx::bar_sync(1, 128);  // the 4 epilogue warps' partial stores are done
-        if (warp == 2 && lane == 0) {
-          // one release fence covers the whole CTA's stores (ordered by the
-          // barrier above) before the ticket is taken
-          __threadfence();
-          const int old = atomicAdd(&p.counters[t], 1);
-          *s_last = (old == static_cast<int>(c1 - c0)) ? 1 : 0;
-        }
-        ptx::bar_sync(1, 128);
-        if (*reinterpret_cast<volatile int *>(s_last)) {
-          __threadfence();
-          // partial-tile offsets of the tile's CTAs, once per tile
-          const int cnt = static_cast<int>(c1 - c0 + 1);
-          for (int j = threadIdx.x - 64; j < cnt; j += 128) {
-            const long long cc = c0 + j;
-            s_base[j] = (cc * p.maxt + (t - (cc * U / C) / KB)) * p.ntile * 128;
-          }
-          ptx::bar_sync(1, 128);
-          // 16 rows at a time, up to 8 partials per batch: the 128 loads of a
-          // batch are independent and in flight together (one round trip for
-          // the usual handful of contributors); partials are still added in
-          // CTA order, so the sum does not depend on who finished last
-          constexpr int kPB = 8;
-          for (int n0 = 0; n0 < p.ntile; n0 += 16) {
-            float acc[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-            for (int j0 = 0; j0 < cnt; j0 += kPB) {
-              float v[kPB][16];
-#pragma unroll
-              for (int jj = 0; jj < kPB; ++jj) {
-                const bool in = j0 + jj < cnt;
-                const float *src =
-                    p.part + (in ? s_base[j0 + jj] : 0) + static_cast<long long>(n0) * 128 + row;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[jj][k] = in ? __ldcg(src + k * 128) : 0.f;
-              }
-#pragma unroll
-              for (int jj = 0; jj < kPB; ++jj)
-#pragma unroll
-                for (int k = 0; k < 16; ++k) acc[k] += v[jj][k];
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int n = nbase + n0 + k;
-              if (n < p.N && m < p.M) p.y[static_cast<size_t>(n) * p.M + m] = acc[k];
-            }
-          }
-          if (warp == 2 && lane == 0) p.counters[t] = 0;
-        }
-        ptx::bar_sync(1, 128);
-      }
     }
   }
 
@@ -322,7 +254,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 struct Schedule {
-  int ntile, nt, mtiles, kblocks, ctas, maxt, stages;
+  int ntile, nt, mtiles, kblocks, ctas, maxc, stages;
   long long units;
 };
 
@@ -333,11 +265,13 @@ Schedule make_schedule(int M, int K, int Npad) {
   s.mtiles = (M + 127) / 128;
   s.kblocks = (K + 63) / 64;
   s.units = static_cast<long long>(s.nt) * s.mtiles * s.kblocks;
-  // one CTA per SM, capped so the consumers' partial-tile tables stay bounded
-  const long long sms = std::min(device_sm_count(), 160);
-  s.ctas = static_cast<int>(std::min<long long>(s.units, sms));
-  const long long per = (s.units + s.ctas - 1) / s.ctas;
-  s.maxt = static_cast<int>((per + s.kblocks - 1) / s.kblocks + 1);
+  // one CTA per SM
+  s.ctas = static_cast<int>(std::min<long long>(s.units, device_sm_count()));
+  // CTAs sharing one tile: every CTA holds at least q = floor(units / ctas)
+  // units, so at most floor(kblocks / q) lie inside the tile's kblocks units,
+  // plus one overlapping each end
+  const long long q = s.units / s.ctas;
+  s.maxc = static_cast<int>(std::min<long long>({s.ctas, s.kblocks, s.kblocks / q + 2}));
   const int stage_bytes = static_cast<int>(a_tile_bytes() + b_tile_bytes(s.ntile));
   s.stages = std::min(8, (kMaxSmem - 2048) / stage_bytes);
   return s;
@@ -377,18 +311,14 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, u
 
 size_t gemm_partial_bytes(int M, int K, int Npad) {
   const Schedule s = make_schedule(M, K, Npad);
-  return static_cast<size_t>(s.ctas) * s.maxt * s.ntile * 128 * sizeof(float);
-}
-
-int gemm_num_tiles(int M, int Npad) {
-  const int ntile = Npad <= 256 ? Npad : 256;
-  return ((Npad + ntile - 1) / ntile) * ((M + 127) / 128);
+  return static_cast<size_t>(s.nt) * s.mtiles * s.maxc * s.ntile * 128 * sizeof(float);
 }
 
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
-                        float *y, int *counters, bool pdl, cudaStream_t st) {
+                        bool pdl, cudaStream_t st, GemmOut *out) {
   const int Npad = static_cast<int>(align_up(static_cast<size_t>(N), 16));
   const Schedule s = make_schedule(M, K, Npad);
+  if (s.units * s.ctas >= (1ll << 32)) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&tmW, W, M, K, K, 128, 64)) != cudaSuccess) return e;
@@ -399,14 +329,10 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.ntile = s.ntile;
   p.mtiles = s.mtiles;
   p.kblocks = s.kblocks;
-  p.maxt = s.maxt;
+  p.maxc = s.maxc;
   p.stages = s.stages;
   p.units = s.units;
-  p.M = M;
-  p.N = N;
   p.part = part;
-  p.y = y;
-  p.counters = counters;
   p.idesc = ptx::idesc_bf16_f32(128, s.ntile);
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(s.ntile)) cols <<= 1;
@@ -416,7 +342,7 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.status = nullptr;
 
   const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
-                      (2 * s.stages + 5) * 8 + 32 + kMaxParts * 8;
+                      (2 * s.stages + 5) * 8 + 32;
   if ((e = ensure_smem_limit(gemm_tc_kernel, kMaxSmem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -428,6 +354,13 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  out->part = part;
+  out->units = static_cast<unsigned>(s.units);
+  out->ctas = s.ctas;
+  out->kblocks = s.kblocks;
+  out->mtiles = s.mtiles;
+  out->maxc = s.maxc;
+  out->ntile = s.ntile;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, p);
 }
 

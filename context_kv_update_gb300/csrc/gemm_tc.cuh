@@ -7,8 +7,12 @@
 // on its N side, so a decode-sized batch still fills the 128-row datapath.
 // The (N tile, M tile, 64-deep K block) units are spread evenly over one CTA
 // per SM (stream-K): each CTA streams exactly its share of the weights once.
-// A tile split between CTAs is finished by the last of them, which sums the
-// partials in CTA order (deterministic) into the dense fp32 result.
+//
+// The GEMM does not finish split tiles itself.  Every CTA that works on output
+// tile t writes its fp32 share as partial j = c - c0(t) (c0 = the tile's first
+// CTA), and the next kernel reads Y through gemm_out_issue / gemm_out_finish,
+// which add a tile's partials in CTA order: the same sum, bit for bit, whichever CTA ended first,
+// with no ticket, fence or extra pass at the GEMM's tail.
 #pragma once
 
 #include <cuda.h>
@@ -21,17 +25,62 @@ namespace dflash {
 using ptx::griddep_launch;
 using ptx::griddep_wait;
 
+// Where a GEMM's result lives: part[t][j][nr][mr] fp32, t = output tile
+// (nt * mtiles + m / 128), j < parts(t) the contributing CTA in order,
+// nr = n - nt * ntile, mr = m % 128.
+struct GemmOut {
+  const float *part;
+  unsigned units;  // (N tile, M tile, K block) units; units * ctas < 2^32
+  int ctas, kblocks, mtiles, maxc, ntile;
+};
+
+// Number of CTAs that wrote partials of output tile t.
+__device__ __forceinline__ int gemm_tile_parts(const GemmOut &g, unsigned t) {
+  const unsigned C = static_cast<unsigned>(g.ctas), U = g.units,
+                 KB = static_cast<unsigned>(g.kblocks);
+  const unsigned c0 = ((t * KB + 1u) * C - 1u) / U;
+  const unsigned c1 = ((t + 1u) * KB * C - 1u) / U;
+  const int n = static_cast<int>(c1 - c0) + 1;
+  return n < g.maxc ? n : g.maxc;
+}
+
+// Y[n, m] read in two halves, so that other loads can go out in between:
+// gemm_out_issue starts the loads of up to 8 partials of the element,
+// gemm_out_finish adds them (and any further ones) in CTA order.
+struct GemmOutLoad {
+  float v[8];
+  const float *src;
+  int cnt;
+};
+
+__device__ __forceinline__ void gemm_out_issue(const GemmOut &g, unsigned t, int cnt, int nr, int mr,
+                                               GemmOutLoad &ld) {
+  const size_t stride = static_cast<size_t>(g.ntile) * 128;
+  ld.src = g.part + static_cast<size_t>(t) * g.maxc * stride + static_cast<size_t>(nr) * 128 + mr;
+  ld.cnt = cnt;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ld.v[j] = j < cnt ? __ldcg(ld.src + j * stride) : 0.f;
+}
+
+__device__ __forceinline__ float gemm_out_finish(const GemmOut &g, const GemmOutLoad &ld) {
+  const size_t stride = static_cast<size_t>(g.ntile) * 128;
+  float acc = ld.v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < ld.cnt) acc += ld.v[j];
+  for (int j = 8; j < ld.cnt; ++j) acc += __ldcg(ld.src + j * stride);
+  return acc;
+}
+
 // Bytes of partial-tile storage a GEMM of this shape needs on this device.
 size_t gemm_partial_bytes(int M, int K, int Npad);
-// Output tiles (one stream-K ticket each) of a GEMM with M columns, Npad rows.
-int gemm_num_tiles(int M, int Npad);
 
-// Enqueue y = X W^T (fp32 [N, M], dense).  X: [N, K] bf16, W: [M, K] bf16.
-// `part` is partial-tile scratch (gemm_partial_bytes), `counters` one int per
-// output tile (gemm_num_tiles), zero on entry and left zero.  `pdl` launches
-// with programmatic stream serialization: the kernel prefetches weight tiles
-// before waiting on the previous kernel's output.
+// Enqueue Y = X W^T into `part` (gemm_partial_bytes) and describe it in *out.
+// X: [N, K] bf16, W: [M, K] bf16.  `pdl` launches with programmatic stream
+// serialization: the kernel prefetches weight tiles before waiting on the
+// previous kernel's output.  cudaErrorInvalidValue for a shape whose unit
+// count does not fit the reader's 32-bit arithmetic.
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
-                        float *y, int *counters, bool pdl, cudaStream_t s);
+                        bool pdl, cudaStream_t s, GemmOut *out);
 
 }  // namespace dflash

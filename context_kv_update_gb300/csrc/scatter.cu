@@ -1,11 +1,10 @@
 // scatter.cu -- per-layer block K/V (GQA) or block latent (MLA) scatter into
 // the paged pool at the DraftBlockPlacement.
 //
-// Follows TensorRT-LLM issue #20548 (Proposal: "a per-layer index_put of the
-// block latents into the pool") and PR #20550 (Description: "each layer's
-// block latents go into the pool with one scatter kernel instead of an
-// index_put"; the follow-up commit's DraftBlockPlacement supplies page, slot
-// and mask).  One CTA per block row; 16-byte vector copies.
+// Follows TensorRT-LLM issue #20548 (Proposal: each layer writes its block
+// latents into the pool) and PR #20550 (Description: that write becomes one
+// scatter kernel per layer in place of an index_put; the follow-up commit's
+// DraftBlockPlacement supplies page, slot and mask).  One CTA per block row; 16-byte vector copies.
 #include "dflash_internal.cuh"
 
 namespace dflash {

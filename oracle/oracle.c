@@ -14,8 +14,8 @@
  *  - TensorRT-LLM issue #20548 "DFlash / MLA DSpark decode spends ~0.2 ms per
  *    step in small bookkeeping kernels", Proposal: the bookkeeping groups.
  *  - TensorRT-LLM PR #20550, Description (TLLM_DFLASH_FUSED_PROLOGUE) and the
- *    follow-up commit "spec_tail_kernels.py": block-table decode ("clamped and
- *    divided offsets"), bonus token, query / RoPE positions, destination
+ *    follow-up commit "spec_tail_kernels.py": block-table decode (offsets
+ *    clamped, then divided), bonus token, query / RoPE positions, destination
  *    pages / offsets / write mask, ctx_len advance with the dummy slot
  *    emptied, advertised context length, seq_lens, DraftBlockPlacement.
  *  - TensorRT-LLM PR #13995 "DFlash performance optimizations", commits
@@ -27,7 +27,7 @@
  *    segments for small uniform q, sliding window with per-head sinks, the
  *    segment layout re-based on the visible window, the reduce over segments.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *  - n_pages counts the non-negative raw offsets of a row; the decoded table
  *    is max(offset, 0) / div with floor division.
  *  - alloc limit A = min(max_ctx, n_pages * P); advance c' = min(c + n, A).
