@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // The page ids of the segment are fetched warp-wide, one batch of 32
     // (tile, box) lookups ahead, so no table read sits between two TMA issues.
     const int tiles_per_batch = 32 / boxes;
+    // With one row tile per segment every K/V line is read exactly once:
+    // loading it evict-first keeps the stream from displacing what is reused
+    // (measured: 5 x (scatter + attention) of the 32K Qwen3-8B-shaped step,
+    // 197.6 -> 185.6 us).  Several row tiles re-read the segment, so they keep
+    // the normal policy.
+    const uint64_t pol = P.RT == 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
     auto fetch_page = [&](int t_batch) -> int {
       const int tt = t_batch + lane / boxes, b = lane % boxes;
       int page = 0;
@@ -244,7 +250,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               key0 % p.P;
           const uint32_t dst =
               ptx::smem_u32(stage + kv * P.k_bytes + c * kVChunk + b * P.box_rows * 128);
-          ptx::tma_load_2d(dst, &tm, c * 64, static_cast<int32_t>(row0), ptx::smem_u32(&kv_full[st]));
+          ptx::tma_load_2d_hint(dst, &tm, c * 64, static_cast<int32_t>(row0),
+                                ptx::smem_u32(&kv_full[st]), pol);
         }
       }
       ++issued;
