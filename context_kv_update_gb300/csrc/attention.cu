@@ -25,51 +25,48 @@ namespace dflash {
 // ----------------------------------------------------------- merge
 // One CTA per output row (r, i, h), one thread per value dim.  Segments are
 // merged in batches of 32 (16 for 512-wide rows) with a running maximum
-// (online log-sum-exp): all loads of a batch (m_s, l_s and the thread's O
-// element) are issued before any is used, so a row of up to one batch of
-// segments costs one memory round trip.  The
-// sink starts the running state as an extra logit with no value.  O of an
-// empty segment (m_s = -inf) is loaded but never used (selected away), so a
-// NaN there cannot leak.
+// (online log-sum-exp).  Lane j of every warp holds segment j's m and l, so
+// the batch maximum and the denominator are warp reductions and each thread
+// keeps only its own O elements: about 50 registers a thread, so the whole
+// grid is resident beside the main kernel from its launch and starts the
+// moment that kernel completes.  All loads of a batch are issued before any is
+// used (one memory round trip for up to one batch of segments).  The sink
+// starts the running state as an extra logit with no value.  O of an empty
+// segment (m_s = -inf) is loaded but never used (selected away), so a NaN
+// there cannot leak.
 template <int DV>
 __global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
   griddep_launch();
   griddep_wait();
-  // one round trip for up to 32 segments (16 at the widest rows, within the
-  // register budget of a 512-thread block)
   constexpr int kBatch = DV >= 512 ? 16 : 32;
   const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
-  const int d = threadIdx.x;
+  const int d = threadIdx.x, lane = d & 31;
   const size_t base = static_cast<size_t>(row) * p.S;
   const int S = p.S;
   float M = p.sinks ? p.sinks[h] : -INFINITY;
   float den = p.sinks ? 1.f : 0.f;
   float acc = 0.f;
   for (int s0 = 0; s0 < S; s0 += kBatch) {
-    float mv[kBatch], lv[kBatch], ov[kBatch];
+    const bool in = lane < kBatch && s0 + lane < S;
+    const float mj = in ? __ldcg(p.ws_m + base + s0 + lane) : -INFINITY;
+    const float lj = in ? __ldcg(p.ws_l + base + s0 + lane) : 0.f;
+    float ov[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int sj = s0 + j;
-      const bool in = sj < S;
-      mv[j] = in ? __ldcg(p.ws_m + base + sj) : -INFINITY;
-      lv[j] = in ? __ldcg(p.ws_l + base + sj) : 0.f;
-      ov[j] = in ? __ldcg(p.ws_o + (base + sj) * DV + d) : 0.f;
-    }
-    float bm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) bm = fmaxf(bm, mv[j]);
-    const float Mn = fmaxf(M, bm);
+    for (int j = 0; j < kBatch; ++j)
+      ov[j] = s0 + j < S ? __ldcg(p.ws_o + (base + s0 + j) * DV + d) : 0.f;
+    const float Mn = fmaxf(M, warp_max(mj));
     if (Mn == -INFINITY) continue;
     const float sc = (M == -INFINITY) ? 0.f : __expf(M - Mn);
+    const bool live = mj != -INFINITY;
+    const float wj = live ? __expf(mj - Mn) : 0.f;
+    const unsigned live_mask = __ballot_sync(0xffffffffu, live);
+    den = den * sc + warp_sum(wj * lj);
     acc *= sc;
-    den *= sc;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const bool live = mv[j] != -INFINITY;
-      const float w = live ? __expf(mv[j] - Mn) : 0.f;
-      den += live ? w * lv[j] : 0.f;
-      acc += live ? w * ov[j] : 0.f;
+      const float w = __shfl_sync(0xffffffffu, wj, j);
+      acc += ((live_mask >> j) & 1u) ? w * ov[j] : 0.f;
     }
     M = Mn;
   }

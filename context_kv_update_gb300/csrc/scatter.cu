@@ -4,43 +4,65 @@
 // Follows TensorRT-LLM issue #20548 (Proposal: each layer writes its block
 // latents into the pool) and PR #20550 (Description: that write becomes one
 // scatter kernel per layer in place of an index_put; the follow-up commit's
-// DraftBlockPlacement supplies page, slot and mask).  One CTA per block row; 16-byte vector copies.
+// DraftBlockPlacement supplies page, slot and mask).  One CTA per block row;
+// 16-byte vector copies.
 #include "dflash_internal.cuh"
 
 namespace dflash {
 namespace {
 
-__global__ void __launch_bounds__(256) block_scatter_kernel(
+constexpr int kScatterThreads = 256;
+constexpr int kScatterVecs = 4;  // 16-byte vectors a thread holds: rows up to 16 KB
+
+__global__ void __launch_bounds__(kScatterThreads) block_scatter_kernel(
     const uint4 *blk_k, const uint4 *blk_v, const int32_t *page, const int32_t *slot,
     const uint8_t *mask, uint16_t *pool, int kind, int nkv, int hd, int W, int P, int NP, int layer,
     int32_t *st) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x;  // r * T + i
+  const bool gqa = kind == DFLASH_KIND_GQA;
+  const int vph = hd / 8;                      // vectors per head row (GQA)
+  const int nv = gqa ? 2 * nkv * vph : W / 8;  // vectors of the block row
+  // source vector t of the row: GQA [K heads | V heads], MLA one latent row
+  auto src = [&](int t) -> uint4 {
+    if (!gqa) return blk_k[static_cast<size_t>(row) * nv + t];
+    const int kv = t / (nkv * vph);
+    const int rem = t - kv * nkv * vph;
+    return (kv == 0 ? blk_k : blk_v)[static_cast<size_t>(row) * nkv * vph + rem];
+  };
+  auto dst = [&](int t, int pg, int sl) -> uint4 * {
+    if (!gqa)
+      return reinterpret_cast<uint4 *>(pool + ((static_cast<size_t>(layer) * NP + pg) * P + sl) * W) + t;
+    const int kv = t / (nkv * vph);
+    const int rem = t - kv * nkv * vph;
+    const int h = rem / vph, e = rem % vph;
+    return reinterpret_cast<uint4 *>(
+               pool + ((((static_cast<size_t>(layer) * NP + pg) * 2 + kv) * nkv + h) * P + sl) * hd) +
+           e;
+  };
+  // The first vectors of the row are loaded before the destination is known:
+  // those loads do not depend on it, so they overlap the mask / page / slot
+  // lookups.
+  uint4 v[kScatterVecs];
+#pragma unroll
+  for (int u = 0; u < kScatterVecs; ++u) {
+    const int t = threadIdx.x + u * kScatterThreads;
+    if (t < nv) v[u] = src(t);
+  }
   if (!mask[row]) return;
   const int pg = page[row], sl = slot[row];
   if (pg < 0 || pg >= NP || sl < 0 || sl >= P) {
     if (threadIdx.x == 0) raise_status(st, DFLASH_DEV_BAD_PAGE);
     return;
   }
-  if (kind == DFLASH_KIND_GQA) {
-    const int vec_per_head = hd / 8;
-    const int total = 2 * nkv * vec_per_head;
-    for (int t = threadIdx.x; t < total; t += blockDim.x) {
-      const int kv = t / (nkv * vec_per_head);
-      const int rem = t - kv * nkv * vec_per_head;
-      const int h = rem / vec_per_head, e = rem % vec_per_head;
-      const uint4 *src = (kv == 0 ? blk_k : blk_v) + (static_cast<size_t>(row) * nkv + h) * vec_per_head + e;
-      uint4 *dst = reinterpret_cast<uint4 *>(
-          pool + ((((static_cast<size_t>(layer) * NP + pg) * 2 + kv) * nkv + h) * P + sl) * hd);
-      dst[e] = *src;
-    }
-  } else {
-    const int vec = W / 8;
-    uint4 *dst =
-        reinterpret_cast<uint4 *>(pool + ((static_cast<size_t>(layer) * NP + pg) * P + sl) * W);
-    for (int t = threadIdx.x; t < vec; t += blockDim.x) dst[t] = blk_k[static_cast<size_t>(row) * vec + t];
+#pragma unroll
+  for (int u = 0; u < kScatterVecs; ++u) {
+    const int t = threadIdx.x + u * kScatterThreads;
+    if (t < nv) *dst(t, pg, sl) = v[u];
   }
+  for (int t = threadIdx.x + kScatterVecs * kScatterThreads; t < nv; t += kScatterThreads)
+    *dst(t, pg, sl) = src(t);
 }
 
 }  // namespace
@@ -53,7 +75,7 @@ cudaError_t launch_block_scatter(const dflash_geom &g, int B, int layer, const v
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kScatterThreads);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
