@@ -177,37 +177,40 @@ class Step:
         B, T, L = prob["B"], g["T"], g["L"]
         dev = "cuda"
         td = self._td
-        self.raw_offsets = td(prob["raw_offsets"])
-        self.acc = td(prob["acc"])
-        self.n_acc = td(prob["n_acc"])
-        self.ctx_pre = td(prob["ctx_len"])
+        self.mla = g["kind"] == "mla"
+        # The per-step inputs a caller uploads live in one device buffer, each
+        # at a 256-byte aligned offset, so the end-to-end leg moves them with
+        # one host-to-device copy (prob key -> device view).
+        in_keys = ["raw_offsets", "acc", "n_acc", "ctx_len", "hidden"] + (
+            ["q_lat", "q_rope", "blk_lat"] if self.mla else ["q", "blk_k", "blk_v"])
+        self.in_buf, self.in_layout, self.step_inputs = self._pack(
+            {k: np.ascontiguousarray(prob[k]) for k in in_keys})
+        v = self.step_inputs
+        self.raw_offsets, self.acc, self.n_acc = v["raw_offsets"], v["acc"], v["n_acc"]
+        self.ctx_pre = v["ctx_len"]
         self.ctx_len = self.ctx_pre.clone()
-        self.hidden = td(prob["hidden"])
+        self.hidden = v["hidden"]
         self.weights = {k: td(prob[k]) for k in ("w_fc", "g_h", "w_kv", "g_k")}
         self.pool = td(prob["pool"])
-        self.mla = g["kind"] == "mla"
         if self.mla:
-            self.q = td(prob["q_lat"])
-            self.q_rope = td(prob["q_rope"])
-            self.blk_k = td(prob["blk_lat"])
-            self.blk_v = None
+            self.q, self.q_rope, self.blk_k, self.blk_v = v["q_lat"], v["q_rope"], v["blk_lat"], None
             dv = g["latent"]
-            host = {"q_lat": self.q, "q_rope": self.q_rope, "blk_lat": self.blk_k}
         else:
-            self.q = td(prob["q"])
-            self.q_rope = None
-            self.blk_k = td(prob["blk_k"])
-            self.blk_v = td(prob["blk_v"])
+            self.q, self.q_rope, self.blk_k, self.blk_v = v["q"], None, v["blk_k"], v["blk_v"]
             dv = g["hd"]
-            host = {"q": self.q, "blk_k": self.blk_k, "blk_v": self.blk_v}
-        # per-step inputs a caller would upload (prob key -> device tensor)
-        self.step_inputs = dict({"raw_offsets": self.raw_offsets, "acc": self.acc,
-                                 "n_acc": self.n_acc, "ctx_len": self.ctx_pre,
-                                 "hidden": self.hidden}, **host)
         self.sinks = td(prob["sinks"]) if prob["use_sinks"] else None
         M = g["max_pages"]
         self.outs = {}
+        # the outputs read back every step (attention output, advanced
+        # ctx_len) share one device buffer: one device-to-host copy
+        attn_shape = (L, B, T, g["hq"], dv)
+        self.out_buf, _, outv = self._pack(
+            {"attn_out": np.zeros(attn_shape, np.uint16), "ctx_len_new": np.zeros(B, np.int32)})
+        self.attn_out = outv["attn_out"]
         for k in dl.STEP_OUTPUT_FIELDS:
+            if k == "ctx_len_new":
+                self.outs[k] = outv[k]
+                continue
             shape = (B, M) if k == "block_table" else (B, T) if k in (
                 "emb_ids", "ctx_pos", "q_pos", "ctx_dst_page", "ctx_dst_slot", "ctx_wmask",
                 "blk_page", "blk_slot", "blk_mask") else (B,)
@@ -217,10 +220,31 @@ class Step:
                                   device=dev)
         self.attn_ws = torch.empty(dl.dflash_attention_workspace_bytes(self.geom, B, T, 0),
                                    dtype=torch.uint8, device=dev)
-        self.attn_out = torch.empty((L, B, T, g["hq"], dv), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if dev_status else None
         self.scale = inputs.attention_scale(g)
         self.launches_per_step = None
+
+    @staticmethod
+    def _pack(arrays):
+        """One uint8 device buffer holding `arrays` (name -> numpy array) at
+        256-byte aligned offsets; returns (buffer, {name: (offset, nbytes)},
+        {name: typed device view}).  uint16 arrays are bf16 data."""
+        import torch
+        layout, off = {}, 0
+        for k, a in arrays.items():
+            layout[k] = (off, a.nbytes)
+            off = (off + a.nbytes + 255) // 256 * 256
+        host = np.zeros(max(off, 256), np.uint8)
+        for k, a in arrays.items():
+            o, n = layout[k]
+            host[o:o + n] = np.frombuffer(a.tobytes(), np.uint8)
+        buf = torch.from_numpy(host).cuda()
+        views = {}
+        for k, a in arrays.items():
+            o, n = layout[k]
+            dt = torch.bfloat16 if a.dtype == np.uint16 else getattr(torch, a.dtype.name)
+            views[k] = buf[o:o + n].view(dt).view(a.shape)
+        return buf, layout, views
 
     @staticmethod
     def _td(a):
@@ -390,26 +414,20 @@ def run_e2e(dl, step, stream, steps):
     """Same step through the public API with inputs from pinned host memory
     and the outputs read back every step (copies inside the timed region)."""
     import torch
-    prob, g = step.prob, step.g
-    host_in = {k: (prob[k], d) for k, d in step.step_inputs.items()}
-    pinned = {}
-    for k, (a, d) in host_in.items():
-        a = np.ascontiguousarray(a)
-        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
-        if a.dtype == np.uint16:
-            t = t.view(torch.bfloat16)
-        pinned[k] = (t.pin_memory(), d)
-    out_host = torch.empty(step.attn_out.shape, dtype=torch.bfloat16).pin_memory()
-    ctx_host = torch.empty(step.outs["ctx_len_new"].shape, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t, _ in pinned.values())
-    d2h = out_host.numel() * 2 + ctx_host.numel() * 4
+    prob = step.prob
+    # the step's inputs, packed on the host as the device buffer holds them
+    host_in = torch.zeros(step.in_buf.numel(), dtype=torch.uint8).pin_memory()
+    hv = host_in.numpy()
+    for k, (o, n) in step.in_layout.items():
+        hv[o:o + n] = np.frombuffer(np.ascontiguousarray(prob[k]).tobytes(), np.uint8)
+    out_host = torch.empty(step.out_buf.numel(), dtype=torch.uint8).pin_memory()
+    h2d = host_in.numel()
+    d2h = out_host.numel()
 
     def one():
-        for t, d in pinned.values():
-            d.copy_(t, non_blocking=True)
+        step.in_buf.copy_(host_in, non_blocking=True)
         step.run()
-        out_host.copy_(step.attn_out, non_blocking=True)
-        ctx_host.copy_(step.outs["ctx_len_new"], non_blocking=True)
+        out_host.copy_(step.out_buf, non_blocking=True)
 
     with torch.cuda.stream(stream):
         one()
