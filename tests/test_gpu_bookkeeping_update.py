@@ -190,6 +190,28 @@ def test_update_qwen_shapes(dl, name, over):
     np.testing.assert_array_equal(ctx_gpu, ctx_ref)
 
 
+@pytest.mark.parametrize("D_in,D,nkv,hd,L,B,hidden", [
+    (1024, 2560, 4, 64, 2, 2, "bf16"),   # hidden norm: 5-CTA clusters of 512 columns
+    (2048, 6144, 2, 128, 1, 1, "f32"),   # 8 CTAs of 768 columns (6 of 8 slots a thread)
+    (512, 8192, 1, 128, 1, 3, "bf16"),   # 8 CTAs of 1024 columns; fc has 8 K blocks
+    (4096, 576, 2, 64, 1, 2, "f32"),     # 2 CTAs of 288 columns: tiles straddle CTAs
+    (64, 64, 1, 64, 1, 1, "bf16"),       # one 64-column CTA, one K block
+])
+def test_update_odd_widths(dl, D_in, D, nkv, hd, L, B, hidden):
+    """d_model / d_in / stacked K/V widths off the benchmark shapes: every
+    cluster layout of the hidden RMSNorm and GEMMs whose tiles are shared by
+    few or many CTAs, checked against the oracle."""
+    over = dict(D_in=D_in, D=D, nkv=nkv, hq=2 * nkv, hd=hd, L=L, B=B, T=16, hidden_dtype=hidden,
+                ctx=[100 + 7 * b for b in range(B)], n_acc=[16 - 3 * b for b in range(B)],
+                alloc_pages=[12] * B, pool_pages=16 * B, max_pages=16)
+    prob = inputs.make_problem(inputs.workload("tiny", **over), seed=11)
+    pool_ref, ctx_ref, pool_gpu, ctx_gpu, st = _update_both(dl, prob)
+    n = _check_pool(prob, pool_ref, pool_gpu)
+    assert n == sum(16 - 3 * b for b in range(B)) * 2 * nkv * L
+    np.testing.assert_array_equal(ctx_gpu, ctx_ref)
+    assert st == 0
+
+
 def test_update_dummies_bad_pages_and_ceiling(dl):
     prob = inputs.make_problem(inputs.workload("batch_sweep_8"), seed=5)
     valid = np.array([1, 0, 1, 1, 0, 1, 1, 1], np.uint8)
@@ -263,3 +285,28 @@ def test_block_scatter_bit_exact(dl, kind):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits(pool_d), pool_ref)
     assert (pool_ref != prob["pool"]).any()
+
+
+def test_block_scatter_wide_rows(dl):
+    """64 KV heads x 128 dims: 2048 16-byte vectors a block row, more than the
+    scatter keeps in registers (the rest go through its tail loop)."""
+    import torch
+    over = dict(nkv=64, hq=64, hd=128, L=2, B=2, T=8, ctx=[40, 90], n_acc=[5, 8],
+                alloc_pages=[12, 12], pool_pages=32, max_pages=16)
+    prob = inputs.make_problem(inputs.workload("tiny", **over), seed=6, with_weights=False)
+    g = prob["g"]
+    geom = dl.make_geom(g)
+    bk, _ = oracle.bookkeeping(prob["raw_offsets"], prob["acc"], prob["n_acc"], prob["ctx_len"],
+                               None, M=g["max_pages"], T=g["T"], P=g["P"], off_div=1,
+                               max_ctx=prob["max_ctx"], mask_id=prob["mask_id"])
+    pool_ref = prob["pool"].copy()
+    pool_d = to_dev(prob["pool"])
+    for layer in range(g["L"]):
+        oracle.block_kv_scatter_gqa(g, layer, prob["blk_k"][layer], prob["blk_v"][layer],
+                                    bk["blk_page"], bk["blk_slot"], bk["blk_mask"], pool_ref)
+        dl.dflash_block_kv_scatter(geom, layer, to_dev(prob["blk_k"][layer]),
+                                   to_dev(prob["blk_v"][layer]), to_dev(bk["blk_page"]),
+                                   to_dev(bk["blk_slot"]), to_dev(bk["blk_mask"]), pool_d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(pool_d), pool_ref)
+    assert (pool_ref != prob["pool"]).sum() > 0
