@@ -328,7 +328,7 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
 
   // fc GEMM
   GemmOut y1, y2;
-  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1,
+  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, st,
                        /*pdl=*/true, s, &y1)) != cudaSuccess)
     return e;
 
@@ -359,7 +359,7 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
   }
 
   // stacked K/V (or latent) GEMM over every layer
-  if ((e = launch_gemm(W.hn, d.N, d.D, static_cast<const uint16_t *>(w.w_kv), d.Wrows, W.part2,
+  if ((e = launch_gemm(W.hn, d.N, d.D, static_cast<const uint16_t *>(w.w_kv), d.Wrows, W.part2, st,
                        /*pdl=*/true, s, &y2)) != cudaSuccess)
     return e;
 

@@ -315,7 +315,7 @@ size_t gemm_partial_bytes(int M, int K, int Npad) {
 }
 
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
-                        bool pdl, cudaStream_t st, GemmOut *out) {
+                        int32_t *status, bool pdl, cudaStream_t st, GemmOut *out) {
   const int Npad = static_cast<int>(align_up(static_cast<size_t>(N), 16));
   const Schedule s = make_schedule(M, K, Npad);
   if (s.units * s.ctas >= (1ll << 32)) return cudaErrorInvalidValue;
@@ -339,7 +339,7 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   p.acc_cols = static_cast<int>(cols);
   p.tmem_cols = 2 * cols;
   p.pdl_wait = 1;
-  p.status = nullptr;
+  p.status = status;
 
   const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
                       (2 * s.stages + 5) * 8 + 32;

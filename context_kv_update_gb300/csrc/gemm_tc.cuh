@@ -76,11 +76,12 @@ __device__ __forceinline__ float gemm_out_finish(const GemmOut &g, const GemmOut
 size_t gemm_partial_bytes(int M, int K, int Npad);
 
 // Enqueue Y = X W^T into `part` (gemm_partial_bytes) and describe it in *out.
-// X: [N, K] bf16, W: [M, K] bf16.  `pdl` launches with programmatic stream
-// serialization: the kernel prefetches weight tiles before waiting on the
-// previous kernel's output.  cudaErrorInvalidValue for a shape whose unit
+// X: [N, K] bf16, W: [M, K] bf16.  A pipeline wait that times out ORs
+// DFLASH_DEV_WAIT_TIMEOUT into *status (when non-null).  `pdl` launches with
+// programmatic stream serialization: the kernel prefetches weight tiles
+// before waiting on the previous kernel's output.  cudaErrorInvalidValue for a shape whose unit
 // count does not fit the reader's 32-bit arithmetic.
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
-                        bool pdl, cudaStream_t s, GemmOut *out);
+                        int32_t *status, bool pdl, cudaStream_t s, GemmOut *out);
 
 }  // namespace dflash
