@@ -149,10 +149,10 @@ typedef struct dflash_step_outputs {
 
 /* ---------------------------------------------------------------------
  * dflash_step_bookkeeping -- one launch for the per-step bookkeeping groups
- * [TRT-20548 Proposal; TRT-20550 Description: "_refresh_ctx_block_tables",
- * "gen-request prologue", "ctx_len advance", and the follow-up commit:
- * block-table decode "clamped and divided offsets", bonus token, query and
- * RoPE positions, destination pages / offsets / write mask, ctx_len advance
+ * [TRT-20548 Proposal; TRT-20550 Description: the _refresh_ctx_block_tables
+ * group, the generation prologue and the ctx_len advance, and the follow-up
+ * commit: block-table decode from clamped, divided offsets, bonus token,
+ * query and RoPE positions, destination pages / offsets / write mask, ctx_len advance
  * with the dummy slot emptied, advertised context length, seq_lens,
  * DraftBlockPlacement].
  *
@@ -189,9 +189,10 @@ DFLASH_API size_t dflash_ctx_workspace_bytes(const dflash_geom *g, int B);
 /* ---------------------------------------------------------------------
  * dflash_ctx_kv_update -- the per-step context-KV update
  * [TRT-20548 Proposal: context-KV mask, clamp, paged write, ctx_len advance;
- * TRT-20550 Description "TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION": fc +
- * hidden_norm + latent GEMM + RMSNorm/RoPE; TRT-13995 "per-layer cached K/V
- * pool" (one GEMM stacked across drafter layers on the K+1 accepted rows),
+ * TRT-20550 Description, TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION: the fc
+ * projection, hidden norm, latent projection and norm + RoPE; TRT-13995
+ * "per-layer cached K/V pool" (one GEMM stacked across drafter layers on the
+ * K+1 accepted rows),
  * "fuse cross-layer k_norm" (one RMSNorm over [N, L, nkv, hd], mask
  * multiply), "match RoPE between context and query" (one cos/sin
  * convention)].
@@ -235,9 +236,8 @@ DFLASH_API int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
 /* ---------------------------------------------------------------------
  * dflash_block_kv_scatter -- write the block's own K/V (GQA) or latent rows
  * (MLA) of one layer into the pool at the DraftBlockPlacement
- * [TRT-20548 Proposal: "a per-layer index_put of the block latents into the
- * pool"; TRT-20550 Description: "each layer's block latents go into the pool
- * with one scatter kernel"].
+ * [TRT-20548 Proposal: each layer writes its block latents into the pool;
+ * TRT-20550 Description: that write is one scatter kernel per layer].
  *
  * blk_k    GQA: device bf16 [B, T, nkv, head_dim]; MLA: [B, T, latent+rope].
  * blk_v    GQA: device bf16 [B, T, nkv, head_dim]; MLA: must be NULL.
