@@ -4,10 +4,10 @@
 // small uniform query block (1 bonus + N drafts) runs the split-KV ("3D")
 // form: the KV range is cut into segments, each segment writes per-query-token
 // partial softmax state (max, sum, weighted values), and a reduce kernel
-// merges them; the segment layout is re-based on the visible window (a
-// sliding window lights only the last slices of an equal split of the whole
-// context) and shared by the main kernel and the reduce; per-head sink logits
-// join the merge.
+// merges them.  The segments split only the key range some query row can
+// see (with a sliding window, the last `window` keys rather than the whole
+// context, most of which no row would read), and the main kernel and the
+// reduce derive the same layout; per-head sink logits join the merge.
 //
 // Workspace (fp32): m[B, Tq, hq, S], l[B, Tq, hq, S], o[B, Tq, hq, S, dv],
 // with m in natural-log units of the scaled scores.  A segment with no visible

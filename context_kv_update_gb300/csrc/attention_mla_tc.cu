@@ -2,7 +2,7 @@
 // latent, on the 5th-generation tensor cores.
 //
 // Follows vLLM PR #54092 (Purpose item 2, Changes item 2) for the split-KV
-// form (per-segment partial softmax state, re-based segments, a separate
+// form (per-segment partial softmax state over the visible keys, a separate
 // reduce), applied to the absorbed-latent drafter attention: every query row
 // (token i, head h) scores one 512 + 64 wide latent row per key,
 //   s_j = scale * (<q_lat, c_j> + <q_rope, r_j>),  values c_j (512 wide).

@@ -3,8 +3,8 @@
 //
 // Follows vLLM PR #54092 (Purpose item 2, Changes item 2): small uniform query
 // blocks (1 bonus + N drafts) run split over KV segments with per-query-token
-// partial softmax state and a separate reduce; the segment layout is re-based
-// on the visible window; sinks join the reduce.
+// partial softmax state and a separate reduce; with a sliding window the
+// segments divide only the keys the window can see; sinks join the reduce.
 //
 // One CTA = (segment s, row tile rt) x KV head x request.  Its 128 MMA rows
 // are the query rows (token i, head h) of the KV head's group (G = hq / nkv

@@ -266,8 +266,8 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * layer over the paged cache, split over KV segments, with an optional
  * sliding window and per-head sink logits [VLLM-54092 Purpose 2 and
  * Changes 2: 3D split-KV for small uniform q (1 bonus + N drafts), per-query-
- * token segment buffers, the segment layout re-based on the visible window
- * and shared by the main kernel and the reduce; sinks].
+ * token segment buffers, segments over the keys the window leaves visible,
+ * one layout for the main kernel and the reduce; sinks].
  *
  * For request r, query token i < Tq and head h (kv head h / (hq/nkv)):
  *   p_i = kv_len[r] - Tq + i,

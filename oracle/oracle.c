@@ -25,7 +25,7 @@
  *    [N, L, nkv, hd] with stacked per-layer weights, shared eps).
  *  - vLLM PR #54092, Purpose item 2 and Changes item 2: split-KV over
  *    segments for small uniform q, sliding window with per-head sinks, the
- *    segment layout re-based on the visible window, the reduce over segments.
+ *    segments over the keys the window leaves visible, the reduce over them.
  *
  * Readings where the pages are silent:
  *  - n_pages counts the non-negative raw offsets of a row; the decoded table
