@@ -168,7 +168,7 @@ class ClockSampler:
 class Step:
     """Device buffers + the launch sequence of one drafter step."""
 
-    def __init__(self, dl, prob, dev_status=True):
+    def __init__(self, dl, prob, dev_status=True, split_update=False):
         import torch
         self.dl, self.prob = dl, prob
         g = prob["g"]
@@ -223,6 +223,15 @@ class Step:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if dev_status else None
         self.scale = inputs.attention_scale(g)
         self.launches_per_step = None
+        # split update: the projection half runs on an auxiliary stream, forked
+        # before the bookkeeping and joined before the commit
+        self.split_update = split_update
+        if split_update:
+            self.staged = torch.empty(dl.dflash_ctx_staged_bytes(self.geom, B), dtype=torch.uint8,
+                                      device=dev)
+            self.aux = torch.cuda.Stream()
+            self.fork_ev = torch.cuda.Event()
+            self.join_ev = torch.cuda.Event()
 
     @staticmethod
     def _pack(arrays):
@@ -257,14 +266,28 @@ class Step:
     def run(self, events=None):
         """Enqueue one step on the current stream.  events: optional list of
         (start, end) torch events recorded around each attention call."""
+        import torch
         dl, g, o = self.dl, self.g, self.outs
         self.ctx_len.copy_(self.ctx_pre)
+        if self.split_update:
+            main = torch.cuda.current_stream()
+            self.fork_ev.record(main)
+            self.aux.wait_event(self.fork_ev)
+            dl.dflash_ctx_kv_project(self.geom, self.hidden, self.ctx_len, self.weights,
+                                     self.staged, self.ctx_ws, self.status, stream=self.aux)
+            self.join_ev.record(self.aux)
         dl.dflash_step_bookkeeping(self.geom, self.raw_offsets, 1, self.acc, self.n_acc,
                                    self.ctx_pre, None, self.prob["max_ctx"], self.prob["mask_id"],
                                    o, self.status)
-        dl.dflash_ctx_kv_update(self.geom, self.hidden, self.n_acc, self.ctx_len, o["alloc_limit"],
-                                o["block_table"], None, self.weights, self.pool, self.ctx_ws,
-                                self.status)
+        if self.split_update:
+            main.wait_event(self.join_ev)
+            dl.dflash_ctx_kv_commit(self.geom, self.staged, self.n_acc, self.ctx_len,
+                                    o["alloc_limit"], o["block_table"], None, self.pool,
+                                    self.status)
+        else:
+            dl.dflash_ctx_kv_update(self.geom, self.hidden, self.n_acc, self.ctx_len,
+                                    o["alloc_limit"], o["block_table"], None, self.weights,
+                                    self.pool, self.ctx_ws, self.status)
         for layer in range(g["L"]):
             dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer],
                                        None if self.mla else self.blk_v[layer],
@@ -281,11 +304,11 @@ class Step:
                 events[layer][1].record()
 
 
-def kernel_launches_per_step(g, hidden_is_f32=False) -> int:
+def kernel_launches_per_step(g, hidden_is_f32=False, split_update=False) -> int:
     # bookkeeping 1; update: fc gemm, hidden norm, kv gemm, epilogue = 4 (+ the
-    # fp32 -> bf16 prep for fp32 hidden); per layer: scatter 1 + attention
-    # (split + merge) 2
-    return 1 + 4 + (1 if hidden_is_f32 else 0) + g["L"] * 3
+    # fp32 -> bf16 prep for fp32 hidden; + the commit when split); per layer:
+    # scatter 1 + attention (split + merge) 2
+    return 1 + 4 + (1 if hidden_is_f32 else 0) + (1 if split_update else 0) + g["L"] * 3
 
 
 def make_events(n_layers, count):
@@ -320,7 +343,7 @@ def run_ours(args, rank, world):
     _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=rank)
     g = prob["g"]
-    step = Step(dl, prob)
+    step = Step(dl, prob, split_update=args.split_update)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -603,6 +626,9 @@ def main():
                     help="context length for qwen3_8b / mla / sliding_window (default 32768)")
     ap.add_argument("--window", type=int, default=None,
                     help="override the workload's sliding window (0 = full range)")
+    ap.add_argument("--split-update", action="store_true",
+                    help="run the context update as project (on an auxiliary stream, beside "
+                         "the bookkeeping) + commit instead of the fused call")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -661,7 +687,9 @@ def main():
               "timing": "CUDA-graph replay of whole steps, CUDA events on the stream",
               "l2": ("inputs larger than L2 (KV 640 MiB + weights 117 MB per step)" if headline
                      else "per-step KV + weight bytes as the workload gives"),
-              "parallelism": "replicas" if world > 1 else "single GPU"}
+              "parallelism": "replicas" if world > 1 else "single GPU",
+              "update": ("split: project on an auxiliary stream, commit after the join"
+                         if args.split_update else "fused")}
     if g["kind"] == "mla":
         config.update({"latent": g["latent"], "rope_dim": g["rope_dim"]})
     line = {
@@ -674,7 +702,8 @@ def main():
         "roofline": roof,
         "clocks": res["clocks"],
         "e2e": res["e2e"],
-        "gpu_launches": kernel_launches_per_step(g) * args.steps,
+        "gpu_launches": kernel_launches_per_step(
+            g, prob["hidden"].dtype == np.float32, args.split_update) * args.steps,
         "device_status": res["status"],
     }
     if not args.no_cpu_baseline and headline:

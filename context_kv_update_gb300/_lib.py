@@ -39,7 +39,8 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_block_kv_scatter", "dflash_attention_num_segments",
            "dflash_attention_workspace_bytes", "dflash_block_attention", "dflash_status_string",
            "dflash_abi_version", "dflash_block_attention_noalloc",
-           "dflash_block_attention_noalloc_max_scratch_bytes")
+           "dflash_block_attention_noalloc_max_scratch_bytes", "dflash_ctx_staged_bytes",
+           "dflash_ctx_kv_project", "dflash_ctx_kv_commit")
 
 
 class DflashError(RuntimeError):
@@ -94,6 +95,11 @@ def load():
     lib.dflash_ctx_workspace_bytes.restype = sz
     lib.dflash_ctx_kv_update.argtypes = [G, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp, vp, vp,
                                          ctypes.POINTER(Weights), vp, vp, sz, vp, vp]
+    lib.dflash_ctx_staged_bytes.argtypes = [G, ctypes.c_int]
+    lib.dflash_ctx_staged_bytes.restype = sz
+    lib.dflash_ctx_kv_project.argtypes = [G, ctypes.c_int, vp, ctypes.c_int, vp,
+                                          ctypes.POINTER(Weights), vp, sz, vp, sz, vp, vp]
+    lib.dflash_ctx_kv_commit.argtypes = [G, ctypes.c_int, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dflash_block_kv_scatter.argtypes = [G, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                             vp, vp]
     lib.dflash_attention_num_segments.argtypes = [G, ctypes.c_int, ctypes.c_int]
@@ -112,7 +118,8 @@ def load():
     lib.dflash_status_string.restype = ctypes.c_char_p
     lib.dflash_abi_version.argtypes = []
     for name in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
-                 "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version"):
+                 "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version",
+                 "dflash_ctx_kv_project", "dflash_ctx_kv_commit"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -176,8 +183,7 @@ def dflash_ctx_kv_update(geom, hidden, n_accepted, ctx_len, alloc_limit, block_t
                          weights: dict, kv_pool, workspace, dev_status=None, stream=None):
     import torch
     lib = load()
-    w = Weights(w_fc=weights["w_fc"].data_ptr(), gamma_h=weights["g_h"].data_ptr(),
-                w_kv=weights["w_kv"].data_ptr(), gamma_k=weights["g_k"].data_ptr())
+    w = _weights(weights)
     dt = DTYPE_F32 if hidden.dtype == torch.float32 else DTYPE_BF16
     B = int(n_accepted.shape[0])
     _check("dflash_ctx_kv_update", lib.dflash_ctx_kv_update(
@@ -185,6 +191,42 @@ def dflash_ctx_kv_update(geom, hidden, n_accepted, ctx_len, alloc_limit, block_t
         _ptr(alloc_limit), _ptr(block_table), _ptr(valid), ctypes.byref(w), _ptr(kv_pool),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)))
+
+
+def _weights(weights: dict):
+    return Weights(w_fc=weights["w_fc"].data_ptr(), gamma_h=weights["g_h"].data_ptr(),
+                   w_kv=weights["w_kv"].data_ptr(), gamma_k=weights["g_k"].data_ptr())
+
+
+def dflash_ctx_staged_bytes(geom, B) -> int:
+    return int(load().dflash_ctx_staged_bytes(ctypes.byref(geom), B))
+
+
+def dflash_ctx_kv_project(geom, hidden, ctx_len, weights: dict, staged, workspace,
+                          dev_status=None, stream=None):
+    """Projection half of the split update: every row's stored values into
+    `staged` (uint8 CUDA tensor of dflash_ctx_staged_bytes bytes)."""
+    import torch
+    lib = load()
+    w = _weights(weights)
+    dt = DTYPE_F32 if hidden.dtype == torch.float32 else DTYPE_BF16
+    B = int(ctx_len.shape[0])
+    _check("dflash_ctx_kv_project", lib.dflash_ctx_kv_project(
+        ctypes.byref(geom), B, _ptr(hidden), dt, _ptr(ctx_len), ctypes.byref(w), _ptr(staged),
+        staged.numel() * staged.element_size(), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def dflash_ctx_kv_commit(geom, staged, n_accepted, ctx_len, alloc_limit, block_table, valid,
+                         kv_pool, dev_status=None, stream=None):
+    """Store half of the split update: masked paged store of the staged rows
+    and the ctx_len advance."""
+    lib = load()
+    B = int(n_accepted.shape[0])
+    _check("dflash_ctx_kv_commit", lib.dflash_ctx_kv_commit(
+        ctypes.byref(geom), B, _ptr(staged), staged.numel() * staged.element_size(),
+        _ptr(n_accepted), _ptr(ctx_len), _ptr(alloc_limit), _ptr(block_table), _ptr(valid),
+        _ptr(kv_pool), _ptr(dev_status), _stream(stream)))
 
 
 def dflash_block_kv_scatter(geom, layer, blk_k, blk_v, blk_page, blk_slot, blk_mask, kv_pool,

@@ -187,11 +187,26 @@ __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, in
   return true;
 }
 
+// Advance of ctx_len[r] from the pre-step length c (the snapshot).
+__device__ __forceinline__ void advance_ctx_len(const MaskArgs &m, int32_t *ctx_len, int B) {
+  for (int r = threadIdx.x; r < B; r += blockDim.x) {
+    const int nn = m.n_acc[r], c = m.ctx_snap[r];
+    const bool live = (m.valid ? (m.valid[r] != 0) : true) && nn >= 1 && nn <= m.T && c >= 0;
+    const long long s = static_cast<long long>(c) + nn;
+    const int A = m.alloc_limit[r];
+    ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
+  }
+}
+
 // ------------------------------------------------------ GQA epilogue
-// grid (N rows, L*2*nkv heads), block = head_dim threads.
+// grid (N rows, L*2*nkv heads), block = head_dim threads.  kStaged = false:
+// the fused update (write-masked paged store, ctx_len advance).  kStaged =
+// true: the projection half of a split update -- every row, RoPE at
+// c + i, the bf16 value to staged[n][col] (no mask, no store to the pool).
+template <bool kStaged>
 __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
-                                    const uint16_t *gamma_k, uint16_t *pool, int L, int nkv,
-                                    int hd, float eps, int32_t *ctx_len, int B) {
+                                    const uint16_t *gamma_k, uint16_t *pool, uint16_t *staged,
+                                    int L, int nkv, int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float kbuf[kMaxHeadDim];
   griddep_launch();
@@ -199,26 +214,23 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int n = blockIdx.x;
   const int head = blockIdx.y;  // ((l * 2 + kv) * nkv + h)
   const int d = threadIdx.x;
-  if (n == 0 && head == 0) {
-    // ctx_len advance; every reader of the pre-step value uses the snapshot.
-    for (int r = d; r < B; r += blockDim.x) {
-      const int nn = m.n_acc[r], c = m.ctx_snap[r];
-      const bool live = (m.valid ? (m.valid[r] != 0) : true) && nn >= 1 && nn <= m.T && c >= 0;
-      const long long s = static_cast<long long>(c) + nn;
-      const int A = m.alloc_limit[r];
-      ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
-    }
-  }
+  const int col = head * hd + d;
   // the Y2 loads go out first, overlapping the destination lookup
   GemmOutLoad ld;
   {
-    const int col = head * hd + d, nt = n / y.ntile;
+    const int nt = n / y.ntile;
     const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
     gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
   }
+  // ctx_len advance; every reader of the pre-step value uses the snapshot
+  if (!kStaged && n == 0 && head == 0) advance_ctx_len(m, ctx_len, B);
   const int r = n / m.T, i = n % m.T;
-  int page, slot, pos;
-  if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && d == 0)) return;
+  int page = 0, slot = 0, pos;
+  if (kStaged) {
+    pos = m.ctx_snap[r] + i;
+  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && d == 0)) {
+    return;
+  }
   const int l = head / (2 * nkv);
   const int kv = (head / nkv) & 1;
   const int h = head % nkv;
@@ -235,16 +247,21 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
     rope_cos_sin(pos, rf.f[j], &c, &s);
     v = d < half ? kn * c - kbuf[d + half] * s : kn * c + kbuf[d - half] * s;
   }
-  const size_t dst =
-      ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P + slot) * hd + d;
-  pool[dst] = f32_to_bf16_rn(v);
+  if (kStaged) {
+    staged[static_cast<size_t>(n) * L * 2 * nkv * hd + col] = f32_to_bf16_rn(v);
+  } else {
+    const size_t dst =
+        ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P + slot) * hd + d;
+    pool[dst] = f32_to_bf16_rn(v);
+  }
 }
 
 // ------------------------------------------------------ MLA epilogue
-// grid (N rows, L), block = lat + rope threads.
+// grid (N rows, L), block = lat + rope threads; kStaged as for GQA.
+template <bool kStaged>
 __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
-                                    const uint16_t *gamma_kv, uint16_t *pool, int L, int lat,
-                                    int rope, float eps, int32_t *ctx_len, int B) {
+                                    const uint16_t *gamma_kv, uint16_t *pool, uint16_t *staged,
+                                    int L, int lat, int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float rbuf[kMaxHeadDim];
   griddep_launch();
@@ -253,24 +270,21 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
   const int l = blockIdx.y;
   const int d = threadIdx.x;
   const int W = lat + rope;
-  if (n == 0 && l == 0) {
-    for (int r = d; r < B; r += blockDim.x) {
-      const int nn = m.n_acc[r], c = m.ctx_snap[r];
-      const bool live = (m.valid ? (m.valid[r] != 0) : true) && nn >= 1 && nn <= m.T && c >= 0;
-      const long long s = static_cast<long long>(c) + nn;
-      const int A = m.alloc_limit[r];
-      ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
-    }
-  }
+  const int col = l * W + d;
   GemmOutLoad ld;
   {
-    const int col = l * W + d, nt = n / y.ntile;
+    const int nt = n / y.ntile;
     const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
     gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
   }
+  if (!kStaged && n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
   const int r = n / m.T, i = n % m.T;
-  int page, slot, pos;
-  if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) return;
+  int page = 0, slot = 0, pos;
+  if (kStaged) {
+    pos = m.ctx_snap[r] + i;
+  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) {
+    return;
+  }
   const float v = gemm_out_finish(y, ld);
   const float ss = block_sum(d < lat ? v * v : 0.f, red);
   float outv;
@@ -288,21 +302,64 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
     rope_cos_sin(pos, rf.f[j], &c, &s);
     outv = e < half ? v * c - rbuf[e + half] * s : v * c + rbuf[e - half] * s;
   }
-  const size_t dst = ((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * W + d;
-  pool[dst] = f32_to_bf16_rn(outv);
+  if (kStaged)
+    staged[static_cast<size_t>(n) * L * W + col] = f32_to_bf16_rn(outv);
+  else
+    pool[((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * W + d] = f32_to_bf16_rn(outv);
+}
+
+// ------------------------------------------------------------ commit
+// The store half of a split update: staged rows -> pool at the write-masked
+// rows, then the ctx_len advance, both from the pre-step lengths the
+// projection recorded (so no CTA reads ctx_len while another writes it).
+// grid (N rows, L), 16-byte vectors of one layer's K and V rows (or latent).
+__global__ void commit_kernel(const uint4 *staged, const MaskArgs m, uint16_t *pool, int kind,
+                              int L, int nkv, int hd, int W, int32_t *ctx_len, int B) {
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x, l = blockIdx.y;
+  if (n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
+  const int r = n / m.T, i = n % m.T;
+  int page, slot, pos;
+  if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && threadIdx.x == 0)) return;
+  const bool gqa = kind == DFLASH_KIND_GQA;
+  const int vph = hd / 8;                            // vectors per head row (GQA)
+  const int lv = gqa ? 2 * nkv * vph : W / 8;        // vectors of one layer's row
+  const uint4 *src = staged + (static_cast<size_t>(n) * L + l) * lv;
+  uint4 *base = reinterpret_cast<uint4 *>(pool);
+  for (int t = threadIdx.x; t < lv; t += blockDim.x) {
+    size_t dst;
+    if (gqa) {
+      const int kv = t / (nkv * vph);
+      const int rem = t - kv * nkv * vph;
+      const int h = rem / vph, e = rem % vph;
+      dst = ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P + slot) * vph + e;
+    } else {
+      dst = ((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * (W / 8) + t;
+    }
+    base[dst] = src[t];
+  }
 }
 
 }  // namespace
 
 size_t ctx_workspace_bytes(const dflash_geom &g, int B) { return ctx_ws_map(g, B, nullptr).bytes; }
 
-cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,
-                                 const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
-                                 const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
-                                 void *pool, void *ws, int32_t *st, cudaStream_t s) {
-  if (B == 0) return cudaSuccess;
+namespace {
+
+// The launch chain prep -> fc GEMM -> hidden norm -> K/V GEMM -> epilogue.
+// staged == nullptr: the fused update.  Otherwise the projection half of a
+// split update: the norm records the pre-step ctx_len in staged_c and the
+// epilogue writes every row's values to staged (mask arguments unused).
+cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,
+                             const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
+                             const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
+                             void *pool, void *ws, int32_t *st, int32_t *staged_c,
+                             uint16_t *staged, cudaStream_t s) {
   const CtxDims d = ctx_dims(g, B);
   const CtxWs W = ctx_ws_map(g, B, ws);
+  const bool split = staged != nullptr;
+  int32_t *snap = split ? staged_c : W.ctx_snap;
   cudaError_t e;
 
   // prep: fp32 hidden -> bf16
@@ -354,7 +411,7 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
     if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_kernel, y1,
                                 static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D, cols,
                                 static_cast<float>(g.eps_hidden), static_cast<const int32_t *>(ctx_len),
-                                W.ctx_snap, B)) != cudaSuccess)
+                                snap, B)) != cudaSuccess)
       return e;
   }
 
@@ -366,7 +423,7 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
   // epilogue
   MaskArgs m;
   m.n_acc = n_acc;
-  m.ctx_snap = W.ctx_snap;
+  m.ctx_snap = snap;
   m.alloc_limit = alloc_limit;
   m.tbl = tbl;
   m.valid = valid;
@@ -383,23 +440,91 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.stream = s;
+  uint16_t *pool16 = static_cast<uint16_t *>(pool);
   if (g.kind == DFLASH_KIND_GQA) {
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
     cfg.blockDim = dim3(g.head_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_kernel, y2, m, rf,
-                           static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
+    e = cudaLaunchKernelEx(&cfg, split ? epilogue_gqa_kernel<true> : epilogue_gqa_kernel<false>, y2,
+                           m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
                            g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else {
     fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers);
     cfg.blockDim = dim3(g.latent_dim + g.rope_dim);
-    e = cudaLaunchKernelEx(&cfg, epilogue_mla_kernel, y2, m, rf,
-                           static_cast<const uint16_t *>(w.gamma_k), static_cast<uint16_t *>(pool),
+    e = cudaLaunchKernelEx(&cfg, split ? epilogue_mla_kernel<true> : epilogue_mla_kernel<false>, y2,
+                           m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
                            g.num_layers, g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k),
                            ctx_len, B);
   }
   return e;
+}
+
+// staged buffer: int32 pre-step ctx_len [B], then bf16 rows [B * T][Wrows]
+size_t staged_rows_offset(int B) { return align_up(sizeof(int32_t) * (B > 0 ? B : 1), 256); }
+
+}  // namespace
+
+cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,
+                                 const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
+                                 const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
+                                 void *pool, void *ws, int32_t *st, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  return launch_ctx_chain(g, B, hidden, hidden_dtype, n_acc, ctx_len, alloc_limit, tbl, valid, w,
+                          pool, ws, st, nullptr, nullptr, s);
+}
+
+size_t ctx_staged_bytes(const dflash_geom &g, int B) {
+  const CtxDims d = ctx_dims(g, B);
+  return staged_rows_offset(B) + sizeof(uint16_t) * static_cast<size_t>(d.N) * d.Wrows;
+}
+
+cudaError_t launch_ctx_kv_project(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,
+                                  const int32_t *ctx_len, const dflash_weights &w, void *staged,
+                                  void *ws, int32_t *st, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  char *sb = static_cast<char *>(staged);
+  return launch_ctx_chain(g, B, hidden, hidden_dtype, nullptr, const_cast<int32_t *>(ctx_len),
+                          nullptr, nullptr, nullptr, w, nullptr, ws, st,
+                          reinterpret_cast<int32_t *>(sb),
+                          reinterpret_cast<uint16_t *>(sb + staged_rows_offset(B)), s);
+}
+
+cudaError_t launch_ctx_kv_commit(const dflash_geom &g, int B, const void *staged,
+                                 const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
+                                 const int32_t *tbl, const uint8_t *valid, void *pool, int32_t *st,
+                                 cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  const CtxDims d = ctx_dims(g, B);
+  const char *sb = static_cast<const char *>(staged);
+  MaskArgs m;
+  m.n_acc = n_acc;
+  m.ctx_snap = reinterpret_cast<const int32_t *>(sb);
+  m.alloc_limit = alloc_limit;
+  m.tbl = tbl;
+  m.valid = valid;
+  m.T = g.block_size;
+  m.M = g.max_pages;
+  m.P = g.page_size;
+  m.NP = g.num_pool_pages;
+  m.st = st;
+  const bool gqa = g.kind == DFLASH_KIND_GQA;
+  const int W = g.latent_dim + g.rope_dim;
+  const int lv = gqa ? 2 * g.nkv * (g.head_dim / 8) : W / 8;
+  int threads = lv < 256 ? ((lv + 31) / 32) * 32 : 256;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(d.N, g.num_layers);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, commit_kernel,
+                            reinterpret_cast<const uint4 *>(sb + staged_rows_offset(B)), m,
+                            static_cast<uint16_t *>(pool), static_cast<int>(g.kind), g.num_layers,
+                            g.nkv, g.head_dim, W, ctx_len, B);
 }
 
 }  // namespace dflash

@@ -92,18 +92,12 @@ extern "C" size_t dflash_ctx_workspace_bytes(const dflash_geom *g, int B) {
   return ctx_workspace_bytes(*g, B);
 }
 
-extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hidden,
-                                    int hidden_dtype, const int32_t *n_accepted, int32_t *ctx_len,
-                                    const int32_t *alloc_limit, const int32_t *block_table,
-                                    const uint8_t *valid, const dflash_weights *w, void *kv_pool,
-                                    void *workspace, size_t ws_bytes, int32_t *dev_status,
-                                    dflash_stream_t stream) {
-  if (!geom_ok(g) || B < 0 || !w) return DFLASH_ERR_INVALID_ARG;
-  if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
-    return DFLASH_ERR_INVALID_ARG;
+namespace {
+
+// Geometry the context update (fused or split) supports.
+int update_geom_status(const dflash_geom *g) {
   if (g->d_in % 64 != 0 || g->d_model % 64 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
-  // partial-sum tables of the projection hold up to 64 output tiles per row
-  // and d/64 + 1 contributors per tile
+  // the hidden RMSNorm spreads a row over at most 8 CTAs of 1024 columns
   if (g->d_in > 8192 || g->d_model > 8192) return DFLASH_ERR_UNSUPPORTED_GEOM;
   if (g->kind == DFLASH_KIND_GQA) {
     if (g->head_dim % 8 != 0 || g->head_dim > kMaxHeadDim || g->head_dim % 2 != 0)
@@ -113,17 +107,78 @@ extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
         (g->latent_dim + g->rope_dim) % 8 != 0)
       return DFLASH_ERR_UNSUPPORTED_GEOM;
   }
+  return DFLASH_OK;
+}
+
+bool weights_ok(const dflash_weights *w) {
+  return w->w_fc && w->gamma_h && w->w_kv && w->gamma_k && aligned16(w->w_fc) && aligned16(w->w_kv);
+}
+
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+}  // namespace
+
+extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hidden,
+                                    int hidden_dtype, const int32_t *n_accepted, int32_t *ctx_len,
+                                    const int32_t *alloc_limit, const int32_t *block_table,
+                                    const uint8_t *valid, const dflash_weights *w, void *kv_pool,
+                                    void *workspace, size_t ws_bytes, int32_t *dev_status,
+                                    dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || !w) return DFLASH_ERR_INVALID_ARG;
+  if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
+    return DFLASH_ERR_INVALID_ARG;
+  if (const int gs = update_geom_status(g)) return gs;
   if (B == 0) return DFLASH_OK;
   if (!hidden || !n_accepted || !ctx_len || !alloc_limit || !block_table || !kv_pool || !workspace)
     return DFLASH_ERR_INVALID_ARG;
-  if (!w->w_fc || !w->gamma_h || !w->w_kv || !w->gamma_k) return DFLASH_ERR_INVALID_ARG;
-  if (!aligned16(hidden) || !aligned16(w->w_fc) || !aligned16(w->w_kv) || !aligned16(kv_pool) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+  if (!weights_ok(w) || !aligned16(hidden) || !aligned16(kv_pool) || !aligned256(workspace))
     return DFLASH_ERR_INVALID_ARG;
   if (ws_bytes < ctx_workspace_bytes(*g, B)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
   return cuda_status(launch_ctx_kv_update(*g, B, hidden, hidden_dtype, n_accepted, ctx_len,
                                           alloc_limit, block_table, valid, *w, kv_pool, workspace,
                                           dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t dflash_ctx_staged_bytes(const dflash_geom *g, int B) {
+  if (!geom_ok(g) || B < 0) return 0;
+  return ctx_staged_bytes(*g, B);
+}
+
+extern "C" int dflash_ctx_kv_project(const dflash_geom *g, int B, const void *hidden,
+                                     int hidden_dtype, const int32_t *ctx_len,
+                                     const dflash_weights *w, void *staged, size_t staged_bytes,
+                                     void *workspace, size_t ws_bytes, int32_t *dev_status,
+                                     dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || !w) return DFLASH_ERR_INVALID_ARG;
+  if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
+    return DFLASH_ERR_INVALID_ARG;
+  if (const int gs = update_geom_status(g)) return gs;
+  if (B == 0) return DFLASH_OK;
+  if (!hidden || !ctx_len || !staged || !workspace) return DFLASH_ERR_INVALID_ARG;
+  if (!weights_ok(w) || !aligned16(hidden) || !aligned256(staged) || !aligned256(workspace))
+    return DFLASH_ERR_INVALID_ARG;
+  if (ws_bytes < ctx_workspace_bytes(*g, B) || staged_bytes < ctx_staged_bytes(*g, B))
+    return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_ctx_kv_project(*g, B, hidden, hidden_dtype, ctx_len, *w, staged,
+                                           workspace, dev_status,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_ctx_kv_commit(const dflash_geom *g, int B, const void *staged,
+                                    size_t staged_bytes, const int32_t *n_accepted,
+                                    int32_t *ctx_len, const int32_t *alloc_limit,
+                                    const int32_t *block_table, const uint8_t *valid,
+                                    void *kv_pool, int32_t *dev_status, dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0) return DFLASH_ERR_INVALID_ARG;
+  if (const int gs = update_geom_status(g)) return gs;
+  if (B == 0) return DFLASH_OK;
+  if (!staged || !n_accepted || !ctx_len || !alloc_limit || !block_table || !kv_pool)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!aligned256(staged) || !aligned16(kv_pool)) return DFLASH_ERR_INVALID_ARG;
+  if (staged_bytes < ctx_staged_bytes(*g, B)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_ctx_kv_commit(*g, B, staged, n_accepted, ctx_len, alloc_limit,
+                                          block_table, valid, kv_pool, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int dflash_block_kv_scatter(const dflash_geom *g, int B, int layer, const void *blk_k,

@@ -109,6 +109,15 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
                                  const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
                                  const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
                                  void *pool, void *ws, int32_t *st, cudaStream_t s);
+// split update: projection into a staged buffer, then the masked store
+size_t ctx_staged_bytes(const dflash_geom &g, int B);
+cudaError_t launch_ctx_kv_project(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,
+                                  const int32_t *ctx_len, const dflash_weights &w, void *staged,
+                                  void *ws, int32_t *st, cudaStream_t s);
+cudaError_t launch_ctx_kv_commit(const dflash_geom &g, int B, const void *staged,
+                                 const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
+                                 const int32_t *tbl, const uint8_t *valid, void *pool, int32_t *st,
+                                 cudaStream_t s);
 
 cudaError_t launch_block_scatter(const dflash_geom &g, int B, int layer, const void *blk_k,
                                  const void *blk_v, const int32_t *page, const int32_t *slot,

@@ -234,6 +234,48 @@ DFLASH_API int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
                          dflash_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * Split context update: dflash_ctx_kv_project + dflash_ctx_kv_commit
+ * [TRT-20550 Description, TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION: the
+ * context projection of the generation tokens is forked onto an auxiliary
+ * stream before sampling / acceptance and joined before the accepted-mask
+ * write; it reads only the target hidden states and the pre-step ctx_len].
+ *
+ * dflash_ctx_kv_project computes, for EVERY row (r, i < T), the values
+ * dflash_ctx_kv_update would store -- GQA bf16(k'), bf16(v) of every layer
+ * and KV head, MLA the bf16 latent row -- with RoPE at c_r + i, and writes
+ * them to `staged` together with the c_r it used.  n_accepted, the masks and
+ * the pool are not needed, so it can run before acceptance.
+ * dflash_ctx_kv_commit then does the write-masked paged store of the staged
+ * rows and the ctx_len advance, exactly as dflash_ctx_kv_update: the pool and
+ * ctx_len after project + commit are bit-identical to the fused call's.  The
+ * advance starts from the c_r recorded by the projection.
+ *
+ * staged       device scratch of dflash_ctx_staged_bytes(g, B) bytes,
+ *              256-byte aligned, owned by the caller: int32 c [B] at offset
+ *              0, then bf16 rows [B * T][W] at offset round_up(4 B, 256),
+ *              W = L * 2 * nkv * head_dim (GQA, per row [L][K|V][nkv][hd])
+ *              or L * (latent_dim + rope_dim) (MLA, [L][latent | rope]).
+ *              Written by project, read by commit; nothing else may write it
+ *              in between.
+ * workspace    (project) as for dflash_ctx_kv_update; a project and a fused
+ *              update must not share a workspace concurrently.
+ * ctx_len      project reads it (the pre-step lengths); commit overwrites it
+ *              with c'.
+ * Other arguments and errors as for dflash_ctx_kv_update;
+ * DFLASH_ERR_WORKSPACE_TOO_SMALL also when staged_bytes is short.
+ * ------------------------------------------------------------------- */
+DFLASH_API size_t dflash_ctx_staged_bytes(const dflash_geom *g, int B);
+DFLASH_API int dflash_ctx_kv_project(const dflash_geom *g, int B, const void *hidden,
+                          int hidden_dtype, const int32_t *ctx_len, const dflash_weights *w,
+                          void *staged, size_t staged_bytes, void *workspace, size_t ws_bytes,
+                          int32_t *dev_status, dflash_stream_t stream);
+DFLASH_API int dflash_ctx_kv_commit(const dflash_geom *g, int B, const void *staged,
+                         size_t staged_bytes, const int32_t *n_accepted, int32_t *ctx_len,
+                         const int32_t *alloc_limit, const int32_t *block_table,
+                         const uint8_t *valid, void *kv_pool, int32_t *dev_status,
+                         dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * dflash_block_kv_scatter -- write the block's own K/V (GQA) or latent rows
  * (MLA) of one layer into the pool at the DraftBlockPlacement
  * [TRT-20548 Proposal: each layer writes its block latents into the pool;

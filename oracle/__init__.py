@@ -236,6 +236,55 @@ def ctx_kv_update_mla(g, hidden, n_acc, ctx_in, alloc_limit, tbl, valid, w_fc, g
     return ctx_out
 
 
+# ------------------------------------------------- split context update
+
+
+def ctx_kv_project(g, hidden, ctx_in, w_fc, g_h, w_kv, g_k):
+    """Projection half of the split update (every row, RoPE at c + i).
+    Returns (staged_c int32 [B], staged uint16 [B * T, W]) with W the
+    per-row width: GQA L * 2 * nkv * hd ([L][K|V][nkv][hd]), MLA L * 576."""
+    lib = _load()
+    B, T = hidden.shape[0], hidden.shape[1]
+    is_f32 = hidden.dtype == np.float32
+    hid = _c(hidden, np.float32 if is_f32 else np.uint16)
+    gqa = g["kind"] == "gqa"
+    W = g["L"] * (2 * g["nkv"] * g["hd"] if gqa else g["latent"] + g["rope_dim"])
+    staged_c = np.empty(B, np.int32)
+    staged = np.empty((B * T, W), np.uint16)
+    common = [ctypes.c_int(B), ctypes.c_int(T), ctypes.c_int(g["L"]), ctypes.c_int(g["D_in"]),
+              ctypes.c_int(g["D"])]
+    dims = ([ctypes.c_int(g["nkv"]), ctypes.c_int(g["hd"])] if gqa else
+            [ctypes.c_int(g["latent"]), ctypes.c_int(g["rope_dim"])])
+    fn = lib.oracle_ctx_kv_project_gqa if gqa else lib.oracle_ctx_kv_project_mla
+    rc = fn(*common, *dims, ctypes.c_double(g["rope_theta"]), ctypes.c_double(g["eps_h"]),
+            ctypes.c_double(g["eps_k"]), _p(hid), ctypes.c_int(int(is_f32)),
+            _p(_c(ctx_in, np.int32)), _p(_c(w_fc, np.uint16)), _p(_c(g_h, np.uint16)),
+            _p(_c(w_kv, np.uint16)), _p(_c(g_k, np.uint16)), _p(staged_c), _p(staged))
+    assert rc == 0
+    return staged_c, staged
+
+
+def ctx_kv_commit(g, staged_c, staged, n_acc, alloc_limit, tbl, valid, pool):
+    """Store half of the split update: in-place masked store into ``pool``;
+    returns ctx_out."""
+    lib = _load()
+    B = staged_c.shape[0]
+    assert pool.dtype == np.uint16 and pool.flags.c_contiguous
+    gqa = g["kind"] == "gqa"
+    tbl = _c(tbl, np.int32)
+    ctx_out = np.empty(B, np.int32)
+    rc = lib.oracle_ctx_kv_commit(
+        ctypes.c_int(0 if gqa else 1), ctypes.c_int(B), ctypes.c_int(g["T"]), ctypes.c_int(g["L"]),
+        ctypes.c_int(g["nkv"] if gqa else 1), ctypes.c_int(g["hd"] if gqa else 0),
+        ctypes.c_int(0 if gqa else g["latent"] + g["rope_dim"]), ctypes.c_int(g["P"]),
+        ctypes.c_int(tbl.shape[1]), ctypes.c_int(g["num_pool_pages"]),
+        _p(_c(staged_c, np.int32)), _p(_c(staged, np.uint16)), _p(_c(n_acc, np.int32)),
+        _p(ctx_out), _p(_c(alloc_limit, np.int32)), _p(tbl),
+        _p(None if valid is None else _c(valid, np.uint8)), _p(pool))
+    assert rc == 0
+    return ctx_out
+
+
 # ----------------------------------------------------------- scatter
 
 

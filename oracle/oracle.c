@@ -383,6 +383,141 @@ int oracle_ctx_kv_update_mla(int B, int T, int L, int D_in, int D, int lat, int 
   return 0;
 }
 
+/* ------------------------------------------- split context-KV update */
+/* TensorRT-LLM PR #20550, Description (TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION):
+ * the context projection (fc, hidden norm, latent / K-V projection, norm and
+ * RoPE) runs before acceptance, from the target hidden states and the
+ * pre-step ctx_len alone; the accepted-mask write follows after the join.
+ * Projection half: for EVERY row (no write mask) the values the update would
+ * store, RoPE at c + i; staged_c[r] = the c used.  Staged row layout:
+ * GQA [L][2][nkv][hd], MLA [L][lat + rope], bf16 bits. */
+int oracle_ctx_kv_project_gqa(int B, int T, int L, int D_in, int D, int nkv, int hd,
+                              double theta, double eps_h, double eps_k, const void *hidden,
+                              int hidden_is_f32, const int32_t *ctx_in, const uint16_t *w_fc,
+                              const uint16_t *g_h, const uint16_t *w_kv, const uint16_t *g_k,
+                              int32_t *staged_c, uint16_t *staged) {
+  size_t esz = hidden_is_f32 ? 4 : 2;
+  size_t row_w = (size_t)L * 2 * nkv * hd;
+  for (int r = 0; r < B; ++r) staged_c[r] = ctx_in[r];
+#pragma omp parallel
+  {
+    double *x = malloc(sizeof(double) * D_in);
+    double *h = malloc(sizeof(double) * D);
+    double *g = malloc(sizeof(double) * D);
+    double *hn = malloc(sizeof(double) * D);
+    double *t = malloc(sizeof(double) * hd);
+    double *kn = malloc(sizeof(double) * hd);
+    double *kr = malloc(sizeof(double) * hd);
+    double *gk = malloc(sizeof(double) * hd);
+#pragma omp for schedule(dynamic, 1)
+    for (int rt = 0; rt < B * T; ++rt) {
+      int r = rt / T, i = rt % T;
+      const char *row = (const char *)hidden + (size_t)rt * D_in * esz;
+      fc_hidden_norm(row, hidden_is_f32, D_in, D, w_fc, g_h, eps_h, x, h, g, hn);
+      double pos = (double)ctx_in[r] + i;
+      for (int l = 0; l < L; ++l) {
+        for (int d = 0; d < hd; ++d) gk[d] = oracle_bf16_to_double(g_k[(size_t)l * hd + d]);
+        for (int kv = 0; kv < 2; ++kv) {
+          for (int hh = 0; hh < nkv; ++hh) {
+            const uint16_t *Wh = w_kv + ((((size_t)l * 2 + kv) * nkv + hh) * hd) * (size_t)D;
+            oracle_matvec_bf16(Wh, hd, D, hn, t);
+            uint16_t *dst = staged + (size_t)rt * row_w + (((size_t)l * 2 + kv) * nkv + hh) * hd;
+            if (kv == 0) {
+              oracle_rmsnorm(t, gk, hd, eps_k, kn);
+              oracle_rope_neox(kn, hd, pos, theta, kr);
+              for (int d = 0; d < hd; ++d) dst[d] = oracle_double_to_bf16(kr[d]);
+            } else {
+              for (int d = 0; d < hd; ++d) dst[d] = oracle_double_to_bf16(t[d]);
+            }
+          }
+        }
+      }
+    }
+    free(x); free(h); free(g); free(hn); free(t); free(kn); free(kr); free(gk);
+  }
+  return 0;
+}
+
+int oracle_ctx_kv_project_mla(int B, int T, int L, int D_in, int D, int lat, int rope,
+                              double theta, double eps_h, double eps_k, const void *hidden,
+                              int hidden_is_f32, const int32_t *ctx_in, const uint16_t *w_fc,
+                              const uint16_t *g_h, const uint16_t *w_dkv, const uint16_t *g_kv,
+                              int32_t *staged_c, uint16_t *staged) {
+  size_t esz = hidden_is_f32 ? 4 : 2;
+  int W = lat + rope;
+  for (int r = 0; r < B; ++r) staged_c[r] = ctx_in[r];
+#pragma omp parallel
+  {
+    double *x = malloc(sizeof(double) * D_in);
+    double *h = malloc(sizeof(double) * D);
+    double *g = malloc(sizeof(double) * D);
+    double *hn = malloc(sizeof(double) * D);
+    double *cc = malloc(sizeof(double) * W);
+    double *ln = malloc(sizeof(double) * lat);
+    double *gl = malloc(sizeof(double) * lat);
+    double *rr = malloc(sizeof(double) * rope);
+#pragma omp for schedule(dynamic, 1)
+    for (int rt = 0; rt < B * T; ++rt) {
+      int r = rt / T, i = rt % T;
+      const char *row = (const char *)hidden + (size_t)rt * D_in * esz;
+      fc_hidden_norm(row, hidden_is_f32, D_in, D, w_fc, g_h, eps_h, x, h, g, hn);
+      double pos = (double)ctx_in[r] + i;
+      for (int l = 0; l < L; ++l) {
+        oracle_matvec_bf16(w_dkv + (size_t)l * W * D, W, D, hn, cc);
+        for (int d = 0; d < lat; ++d) gl[d] = oracle_bf16_to_double(g_kv[(size_t)l * lat + d]);
+        oracle_rmsnorm(cc, gl, lat, eps_k, ln);
+        oracle_rope_neox(cc + lat, rope, pos, theta, rr);
+        uint16_t *dst = staged + ((size_t)rt * L + l) * W;
+        for (int d = 0; d < lat; ++d) dst[d] = oracle_double_to_bf16(ln[d]);
+        for (int d = 0; d < rope; ++d) dst[lat + d] = oracle_double_to_bf16(rr[d]);
+      }
+    }
+    free(x); free(h); free(g); free(hn); free(cc); free(ln); free(gl); free(rr);
+  }
+  return 0;
+}
+
+/* Store half (after the join): the write-masked paged store of the staged
+ * rows and the ctx_len advance, both from the c the projection recorded.
+ * kind 0 = GQA (pool [L][NP][2][nkv][P][hd]), 1 = MLA (pool [L][NP][P][W]). */
+int oracle_ctx_kv_commit(int kind, int B, int T, int L, int nkv, int hd, int W, int P, int M,
+                         int num_pool_pages, const int32_t *staged_c, const uint16_t *staged,
+                         const int32_t *n_acc, int32_t *ctx_out, const int32_t *alloc_limit,
+                         const int32_t *tbl, const uint8_t *valid, uint16_t *pool) {
+  size_t row_w = kind == 0 ? (size_t)L * 2 * nkv * hd : (size_t)L * W;
+  for (int rt = 0; rt < B * T; ++rt) {
+    int r = rt / T, i = rt % T;
+    int n = n_acc[r], c = staged_c[r];
+    int ok = row_valid(valid, r, n, c, T);
+    int page, slot;
+    if (!ctx_row_dest(ok, i, n, c, alloc_limit[r], tbl + (int64_t)r * M, M, P, num_pool_pages,
+                      &page, &slot))
+      continue;
+    const uint16_t *src = staged + (size_t)rt * row_w;
+    for (int l = 0; l < L; ++l) {
+      if (kind == 0) {
+        for (int kv = 0; kv < 2; ++kv)
+          for (int hh = 0; hh < nkv; ++hh) {
+            uint16_t *dst =
+                pool + (((((size_t)l * num_pool_pages + page) * 2 + kv) * nkv + hh) * P + slot) *
+                           (size_t)hd;
+            memcpy(dst, src + (((size_t)l * 2 + kv) * nkv + hh) * hd, sizeof(uint16_t) * hd);
+          }
+      } else {
+        uint16_t *dst = pool + (((size_t)l * num_pool_pages + page) * P + slot) * (size_t)W;
+        memcpy(dst, src + (size_t)l * W, sizeof(uint16_t) * W);
+      }
+    }
+  }
+  for (int r = 0; r < B; ++r) {
+    int n = n_acc[r], c = staged_c[r];
+    int ok = row_valid(valid, r, n, c, T);
+    long long s = (long long)c + n;
+    ctx_out[r] = ok ? (int)(s < alloc_limit[r] ? s : alloc_limit[r]) : 0;
+  }
+  return 0;
+}
+
 /* --------------------------------------------------- block KV scatter */
 
 /* GQA: blk_k / blk_v [B, T, nkv, hd] -> pool layer `layer` at the placement. */

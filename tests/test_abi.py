@@ -25,7 +25,8 @@ def test_header_declares_the_entry_points():
     names = set(_declared())
     for n in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
               "dflash_block_attention", "dflash_ctx_workspace_bytes",
-              "dflash_attention_workspace_bytes", "dflash_attention_num_segments"):
+              "dflash_attention_workspace_bytes", "dflash_attention_num_segments",
+              "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes"):
         assert n in names
 
 
@@ -99,6 +100,27 @@ def test_validation_rejects_without_launching(lib):
     w0 = _lib.Weights(0x1000, None, 0x1000, 0x1000)
     assert lib.dflash_ctx_kv_update(G, 1, p, 0, p, p, p, p, null, ctypes.byref(w0), p, p, 1 << 30,
                                     null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    # split update: staged bytes cover c [B] + rows; short or misaligned staged
+    # buffers, bad dtype and missing arguments are rejected before any launch
+    T, L, nkv, hd = g.block_size, g.num_layers, g.nkv, g.head_dim
+    assert lib.dflash_ctx_staged_bytes(G, 3) == 256 + 3 * T * L * 2 * nkv * hd * 2
+    assert lib.dflash_ctx_staged_bytes(None, 3) == 0
+    assert lib.dflash_ctx_kv_project(G, 1, p, 9, p, ctypes.byref(w), p, 1 << 30, p, 1 << 30,
+                                     null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_project(G, 1, p, 0, p, ctypes.byref(w), p, 16, p, 1 << 30,
+                                     null, null) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    assert lib.dflash_ctx_kv_project(G, 1, p, 0, p, ctypes.byref(w), odd, 1 << 30, p, 1 << 30,
+                                     null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_project(G, 1, p, 0, null, ctypes.byref(w), p, 1 << 30, p, 1 << 30,
+                                     null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_project(G, 0, null, 0, null, ctypes.byref(w), null, 0, null, 0,
+                                     null, null) == _lib.DFLASH_OK
+    assert lib.dflash_ctx_kv_commit(G, 1, p, 16, p, p, p, p, null, p, null,
+                                    null) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    assert lib.dflash_ctx_kv_commit(G, 1, odd, 1 << 30, p, p, p, p, null, p, null,
+                                    null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_commit(G, 1, p, 1 << 30, null, p, p, p, null, p, null,
+                                    null) == _lib.DFLASH_ERR_INVALID_ARG
     # bookkeeping: off_div < 1, stride below the row width
     outs = _lib.StepOutputs(*([0x1000] * 15))
     assert lib.dflash_step_bookkeeping(G, 1, p, 16, 0, p, 4, p, p, null, 100, 7,
