@@ -285,6 +285,27 @@ def ctx_kv_commit(g, staged_c, staged, n_acc, alloc_limit, tbl, valid, pool):
     return ctx_out
 
 
+# ------------------------------------------------------------ query side
+
+
+def q_norm_rope(q_in, gamma, pos, theta, eps):
+    """q_in uint16 [..., heads, dim] (rows = leading dims), gamma uint16 [dim]
+    or None (rotation only), pos int32 [rows].  Returns uint16 like q_in."""
+    lib = _load()
+    q = _c(q_in, np.uint16)
+    dim, heads = q.shape[-1], q.shape[-2]
+    rows = q.size // (dim * heads)
+    pos = _c(np.asarray(pos).reshape(rows), np.int32)
+    out = np.empty_like(q)
+    rc = lib.oracle_q_norm_rope(ctypes.c_int(rows), ctypes.c_int(heads), ctypes.c_int(dim),
+                                ctypes.c_int(0 if gamma is None else 1), ctypes.c_double(theta),
+                                ctypes.c_double(eps), _p(q),
+                                _p(None if gamma is None else _c(gamma, np.uint16)), _p(pos),
+                                _p(out))
+    assert rc == 0
+    return out
+
+
 # ----------------------------------------------------------- scatter
 
 

@@ -518,6 +518,36 @@ int oracle_ctx_kv_commit(int kind, int B, int T, int L, int nkv, int hd, int W, 
   return 0;
 }
 
+/* ------------------------------------------------------- query side */
+/* TensorRT-LLM PR #13995, commits "use fused qk-norm+rope on non-YaRN draft"
+ * and "match RoPE between context and query": the drafter's query rows get
+ * RMSNorm (gain gamma, eps) and the same rotate-half RoPE as the context keys,
+ * at the query positions.  q_in / q_out [rows][heads][dim] bf16 bits,
+ * pos [rows]; do_norm = 0 applies the rotation only (the MLA rope part). */
+int oracle_q_norm_rope(int rows, int heads, int dim, int do_norm, double theta, double eps,
+                       const uint16_t *q_in, const uint16_t *gamma, const int32_t *pos,
+                       uint16_t *q_out) {
+  double *x = malloc(sizeof(double) * dim);
+  double *g = malloc(sizeof(double) * dim);
+  double *n = malloc(sizeof(double) * dim);
+  double *o = malloc(sizeof(double) * dim);
+  for (int d = 0; d < dim; ++d) g[d] = do_norm ? oracle_bf16_to_double(gamma[d]) : 1.0;
+  for (int r = 0; r < rows; ++r) {
+    for (int h = 0; h < heads; ++h) {
+      size_t base = ((size_t)r * heads + h) * dim;
+      for (int d = 0; d < dim; ++d) x[d] = oracle_bf16_to_double(q_in[base + d]);
+      if (do_norm)
+        oracle_rmsnorm(x, g, dim, eps, n);
+      else
+        memcpy(n, x, sizeof(double) * dim);
+      oracle_rope_neox(n, dim, (double)pos[r], theta, o);
+      for (int d = 0; d < dim; ++d) q_out[base + d] = oracle_double_to_bf16(o[d]);
+    }
+  }
+  free(x); free(g); free(n); free(o);
+  return 0;
+}
+
 /* --------------------------------------------------- block KV scatter */
 
 /* GQA: blk_k / blk_v [B, T, nkv, hd] -> pool layer `layer` at the placement. */
