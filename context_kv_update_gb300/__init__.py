@@ -10,6 +10,6 @@ from ._lib import (DflashError, Geom, StepOutputs, Weights, STEP_OUTPUT_FIELDS, 
                    dflash_block_attention, dflash_block_attention_noalloc,
                    dflash_block_attention_noalloc_max_scratch_bytes, dflash_block_kv_scatter,
                    dflash_ctx_kv_commit, dflash_ctx_kv_project, dflash_ctx_kv_update,
-                   dflash_ctx_staged_bytes, dflash_ctx_workspace_bytes, dflash_step_bookkeeping,
-                   load, make_geom,
+                   dflash_ctx_staged_bytes, dflash_ctx_workspace_bytes, dflash_q_norm_rope,
+                   dflash_step_bookkeeping, load, make_geom,
                    KIND_GQA, KIND_MLA, MASK_CAUSAL_TAIL, MASK_BLOCK_BIDIR)

@@ -40,7 +40,7 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_attention_workspace_bytes", "dflash_block_attention", "dflash_status_string",
            "dflash_abi_version", "dflash_block_attention_noalloc",
            "dflash_block_attention_noalloc_max_scratch_bytes", "dflash_ctx_staged_bytes",
-           "dflash_ctx_kv_project", "dflash_ctx_kv_commit")
+           "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope")
 
 
 class DflashError(RuntimeError):
@@ -100,6 +100,7 @@ def load():
     lib.dflash_ctx_kv_project.argtypes = [G, ctypes.c_int, vp, ctypes.c_int, vp,
                                           ctypes.POINTER(Weights), vp, sz, vp, sz, vp, vp]
     lib.dflash_ctx_kv_commit.argtypes = [G, ctypes.c_int, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dflash_q_norm_rope.argtypes = [G, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp]
     lib.dflash_block_kv_scatter.argtypes = [G, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                             vp, vp]
     lib.dflash_attention_num_segments.argtypes = [G, ctypes.c_int, ctypes.c_int]
@@ -119,7 +120,7 @@ def load():
     lib.dflash_abi_version.argtypes = []
     for name in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
                  "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version",
-                 "dflash_ctx_kv_project", "dflash_ctx_kv_commit"):
+                 "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -227,6 +228,16 @@ def dflash_ctx_kv_commit(geom, staged, n_accepted, ctx_len, alloc_limit, block_t
         ctypes.byref(geom), B, _ptr(staged), staged.numel() * staged.element_size(),
         _ptr(n_accepted), _ptr(ctx_len), _ptr(alloc_limit), _ptr(block_table), _ptr(valid),
         _ptr(kv_pool), _ptr(dev_status), _stream(stream)))
+
+
+def dflash_q_norm_rope(geom, q_in, gamma_q, q_pos, q_out, dev_status=None, stream=None):
+    """q_in / q_out bf16 CUDA tensors [B, Tq, hq, dim] (may be the same tensor),
+    gamma_q [head_dim] (GQA) or None (MLA rope part), q_pos int32 [B, Tq]."""
+    lib = load()
+    B, Tq = int(q_pos.shape[0]), int(q_pos.shape[1])
+    _check("dflash_q_norm_rope", lib.dflash_q_norm_rope(
+        ctypes.byref(geom), B, Tq, _ptr(q_in), _ptr(gamma_q), _ptr(q_pos), _ptr(q_out),
+        _ptr(dev_status), _stream(stream)))
 
 
 def dflash_block_kv_scatter(geom, layer, blk_k, blk_v, blk_page, blk_slot, blk_mask, kv_pool,

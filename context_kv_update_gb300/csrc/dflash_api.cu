@@ -181,6 +181,25 @@ extern "C" int dflash_ctx_kv_commit(const dflash_geom *g, int B, const void *sta
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" int dflash_q_norm_rope(const dflash_geom *g, int B, int Tq, const void *q_in,
+                                  const void *gamma_q, const int32_t *q_pos, void *q_out,
+                                  int32_t *dev_status, dflash_stream_t stream) {
+  (void)dev_status;  // nothing in the rows can be out of range
+  if (!geom_ok(g) || B < 0 || Tq < 1) return DFLASH_ERR_INVALID_ARG;
+  const bool gqa = g->kind == DFLASH_KIND_GQA;
+  const int dim = gqa ? g->head_dim : g->rope_dim;
+  if (dim < 2 || dim % 2 != 0 || dim > kMaxHeadDim) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  // GQA: norm + rotation of the head rows; MLA: rotation of the rope part only
+  if (gqa != (gamma_q != nullptr)) return DFLASH_ERR_INVALID_ARG;
+  if (B == 0) return DFLASH_OK;
+  if (!q_in || !q_pos || !q_out) return DFLASH_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_in) | reinterpret_cast<uintptr_t>(q_out) |
+       reinterpret_cast<uintptr_t>(gamma_q)) & 1u)
+    return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(launch_q_norm_rope(*g, B * Tq, q_in, gamma_q, q_pos, q_out,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int dflash_block_kv_scatter(const dflash_geom *g, int B, int layer, const void *blk_k,
                                        const void *blk_v, const int32_t *blk_page,
                                        const int32_t *blk_slot, const uint8_t *blk_mask,

@@ -119,6 +119,11 @@ cudaError_t launch_ctx_kv_commit(const dflash_geom &g, int B, const void *staged
                                  const int32_t *tbl, const uint8_t *valid, void *pool, int32_t *st,
                                  cudaStream_t s);
 
+// query rows: RMSNorm (gamma non-null) + RoPE at pos[row], [rows][hq][dim]
+cudaError_t launch_q_norm_rope(const dflash_geom &g, int rows, const void *q_in,
+                               const void *gamma, const int32_t *pos, void *q_out,
+                               cudaStream_t s);
+
 cudaError_t launch_block_scatter(const dflash_geom &g, int B, int layer, const void *blk_k,
                                  const void *blk_v, const int32_t *page, const int32_t *slot,
                                  const uint8_t *mask, void *pool, int32_t *st, cudaStream_t s);

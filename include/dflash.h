@@ -276,6 +276,34 @@ DFLASH_API int dflash_ctx_kv_commit(const dflash_geom *g, int B, const void *sta
                          dflash_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * dflash_q_norm_rope -- the query side of one drafter layer
+ * [TRT-13995 "use fused qk-norm+rope on non-YaRN draft", "match RoPE between
+ * context and query": query norm and rotation in one kernel, with the cos/sin
+ * the context keys are rotated with].
+ *
+ * GQA: for every request r, query token i < Tq and head h,
+ *   q_out[r, i, h] = bf16(RoPE(q * gamma_q / sqrt(mean(q^2) + eps_k),
+ *                               q_pos[r, i]))   over head_dim,
+ * q = q_in[r, i, h]; eps is the geometry's eps_k and the rotation the
+ * rotate-half RoPE of dflash_ctx_kv_update (same frequency table and angle
+ * code, so a query and a context key at the same position get the same
+ * cos/sin).  MLA: gamma_q must be NULL and only the rotation is applied, to
+ * the rope part of the query (rows of rope_dim).
+ *
+ * q_in, q_out  device bf16 [B, Tq, hq, head_dim] (MLA: [B, Tq, hq, rope_dim]);
+ *              q_out may equal q_in.
+ * gamma_q      device bf16 [head_dim] (the layer's query-norm gain), or NULL
+ *              for MLA.
+ * q_pos        device int32 [B, Tq] (e.g. dflash_step_outputs.q_pos).
+ * Errors: DFLASH_ERR_INVALID_ARG (null / odd pointers, gamma_q given for MLA
+ * or missing for GQA), DFLASH_ERR_UNSUPPORTED_GEOM (an odd or > 256 rotated
+ * width), DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_q_norm_rope(const dflash_geom *g, int B, int Tq, const void *q_in,
+                       const void *gamma_q, const int32_t *q_pos, void *q_out,
+                       int32_t *dev_status, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * dflash_block_kv_scatter -- write the block's own K/V (GQA) or latent rows
  * (MLA) of one layer into the pool at the DraftBlockPlacement
  * [TRT-20548 Proposal: each layer writes its block latents into the pool;

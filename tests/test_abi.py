@@ -26,7 +26,8 @@ def test_header_declares_the_entry_points():
     for n in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
               "dflash_block_attention", "dflash_ctx_workspace_bytes",
               "dflash_attention_workspace_bytes", "dflash_attention_num_segments",
-              "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes"):
+              "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes",
+              "dflash_q_norm_rope"):
         assert n in names
 
 
@@ -121,6 +122,16 @@ def test_validation_rejects_without_launching(lib):
                                     null) == _lib.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_ctx_kv_commit(G, 1, p, 1 << 30, null, p, p, p, null, p, null,
                                     null) == _lib.DFLASH_ERR_INVALID_ARG
+    # query norm + RoPE (every case here is rejected before any launch): GQA
+    # without the gain, Tq < 1, a pointer off the 2-byte grid; B == 0 is a no-op
+    odd1 = ctypes.c_void_p(0x1001)
+    assert lib.dflash_q_norm_rope(G, 1, 4, p, null, p, p, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_q_norm_rope(G, 1, 0, p, p, p, p, null, null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_q_norm_rope(G, 1, 4, odd1, p, p, p, null,
+                                  null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_q_norm_rope(G, 1, 4, p, p, null, p, null,
+                                  null) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_q_norm_rope(G, 0, 4, null, p, null, null, null, null) == _lib.DFLASH_OK
     # bookkeeping: off_div < 1, stride below the row width
     outs = _lib.StepOutputs(*([0x1000] * 15))
     assert lib.dflash_step_bookkeeping(G, 1, p, 16, 0, p, 4, p, p, null, 100, 7,
