@@ -285,6 +285,36 @@ def ctx_kv_commit(g, staged_c, staged, n_acc, alloc_limit, tbl, valid, pool):
     return ctx_out
 
 
+# ------------------------------------------------ either side of the path
+
+
+def strict_accept(draft, target):
+    """draft int32 [B, K], target int32 [B, K + 1] -> (n_acc [B], accepted
+    [B, K + 1] with -1 past n_acc)."""
+    lib = _load()
+    d = _c(draft, np.int32)
+    t = _c(target, np.int32)
+    B, K = d.shape
+    assert t.shape == (B, K + 1)
+    n_acc = np.empty(B, np.int32)
+    acc = np.empty((B, K + 1), np.int32)
+    assert lib.oracle_strict_accept(ctypes.c_int(B), ctypes.c_int(K), _p(d), _p(t), _p(n_acc),
+                                    _p(acc)) == 0
+    return n_acc, acc
+
+
+def embedding_gather(ids, table):
+    """ids int32 [...], table uint16 [V, D] -> (uint16 [..., D], any id out of range)."""
+    lib = _load()
+    i = _c(ids, np.int32)
+    tb = _c(table, np.uint16)
+    V, D = tb.shape
+    out = np.empty(i.shape + (D,), np.uint16)
+    bad = lib.oracle_embedding_gather(ctypes.c_int(i.size), ctypes.c_int(V), ctypes.c_int(D),
+                                      _p(i), _p(tb), _p(out))
+    return out, bool(bad)
+
+
 # ------------------------------------------------------------ query side
 
 

@@ -518,6 +518,45 @@ int oracle_ctx_kv_commit(int kind, int B, int T, int L, int nkv, int hd, int W, 
   return 0;
 }
 
+/* ------------------------------------------ either side of the path */
+/* TensorRT-LLM PR #20550, follow-up commit "spec_tail_kernels.py": strict
+ * acceptance of a uniform-width draft.  Request r drafted K tokens
+ * draft[r, 0..K-1]; the target produced K + 1 tokens target[r, 0..K] at the
+ * same positions.  Drafts are accepted while they equal the target's token;
+ * the target's token at the first disagreement (or after the last draft) is
+ * the bonus.  n_acc[r] = 1 + (leading matches) in [1, K + 1];
+ * accepted[r, i] = target[r, i] for i < n_acc[r], -1 after. */
+int oracle_strict_accept(int B, int K, const int32_t *draft, const int32_t *target,
+                         int32_t *n_acc, int32_t *accepted) {
+  for (int r = 0; r < B; ++r) {
+    int m = 0;
+    while (m < K && draft[(size_t)r * K + m] == target[(size_t)r * (K + 1) + m]) ++m;
+    n_acc[r] = m + 1;
+    for (int i = 0; i <= K; ++i)
+      accepted[(size_t)r * (K + 1) + i] = i <= m ? target[(size_t)r * (K + 1) + i] : -1;
+  }
+  return 0;
+}
+
+/* TensorRT-LLM PR #13995, commit "fuse query-input build in pure Torch +
+ * fused embedding lookup": the noise block's input rows are one embedding
+ * lookup over its ids ([bonus, mask_id, ...]).  out[k, :] = table[ids[k], :]
+ * for k < n (bf16 bits); an id outside [0, V) gives a zero row and returns 1. */
+int oracle_embedding_gather(int n, int V, int D, const int32_t *ids, const uint16_t *table,
+                            uint16_t *out) {
+  int bad = 0;
+  for (int k = 0; k < n; ++k) {
+    int id = ids[k];
+    if (id < 0 || id >= V) {
+      memset(out + (size_t)k * D, 0, sizeof(uint16_t) * D);
+      bad = 1;
+      continue;
+    }
+    memcpy(out + (size_t)k * D, table + (size_t)id * D, sizeof(uint16_t) * D);
+  }
+  return bad;
+}
+
 /* ------------------------------------------------------- query side */
 /* TensorRT-LLM PR #13995, commits "use fused qk-norm+rope on non-YaRN draft"
  * and "match RoPE between context and query": the drafter's query rows get
