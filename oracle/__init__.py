@@ -12,7 +12,10 @@ bf16 tensors travel as ``uint16`` arrays holding the bf16 bit patterns.
 Pins (tests/test_oracle_*.py): brute-force dense attention on tiny inputs,
 split-count invariance of the split-KV form, RMSNorm / RoPE closed forms,
 numpy float64 matmul for the projection, a hand-worked bookkeeping case
-(tests/golden/bookkeeping_tiny.json) and bookkeeping invariants.
+(tests/golden/bookkeeping_tiny.json) and bookkeeping invariants; the split
+update against the fused one; the query RMSNorm + RoPE against numpy RMSNorm
+and RoPE's position-difference and length invariants; strict acceptance by
+hand cases and brute force; the embedding lookup as a one-hot product.
 """
 from __future__ import annotations
 

@@ -41,6 +41,12 @@
  *  - CAUSAL_TAIL: query i of Tq sits at p_i = kv_len - Tq + i and sees keys
  *    j <= p_i; BLOCK_BIDIR: it sees every key j < kv_len.  A window W > 0
  *    further restricts to p_i - j < W.  An empty key set yields 0.
+ *  - split update: the projection covers every row of the block at c + i
+ *    and records c; the commit masks and advances from the recorded c.
+ *  - the query norm uses the key norm's eps; MLA rotates only the rope part.
+ *  - strict acceptance compares each draft with the target's token at the
+ *    same position; the first mismatch (or the position after the last
+ *    draft) supplies the bonus, accepted[n - 1].
  */
 #include <math.h>
 #include <stdint.h>
