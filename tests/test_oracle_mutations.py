@@ -7,7 +7,10 @@ import subprocess
 import pytest
 
 import oracle
+import tests.test_oracle_accept_gather as accept_pins
 import tests.test_oracle_pins as pins
+import tests.test_oracle_q_rope as q_pins
+import tests.test_oracle_split_update as split_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -33,6 +36,14 @@ MUTATIONS = [
     ("kv_head_swap", "oracle_matvec_bf16(W, hd, D, hn, t);",
      "oracle_matvec_bf16(W + (kv == 0 ? (size_t)nkv * hd * D : 0), hd, D, hn, t);",
      [pins.test_update_v_is_plain_projection_and_k_is_normed_rotation]),
+    # the next rows' functions
+    ("accept_off_by_one", "n_acc[r] = m + 1;", "n_acc[r] = m;",
+     [accept_pins.test_strict_accept_hand_cases]),
+    ("q_norm_dropped", "oracle_rmsnorm(x, g, dim, eps, n);", "memcpy(n, x, sizeof(double) * dim);",
+     [q_pins.test_position_zero_is_plain_rmsnorm]),
+    ("commit_kv_swap", "memcpy(dst, src + (((size_t)l * 2 + kv) * nkv + hh) * hd, sizeof(uint16_t) * hd);",
+     "memcpy(dst, src + (((size_t)l * 2 + (1 - kv)) * nkv + hh) * hd, sizeof(uint16_t) * hd);",
+     [lambda: split_pins.test_split_update_equals_fused(*split_pins._cases()[1])]),
 ]
 
 
