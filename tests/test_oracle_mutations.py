@@ -44,6 +44,14 @@ MUTATIONS = [
     ("commit_kv_swap", "memcpy(dst, src + (((size_t)l * 2 + kv) * nkv + hh) * hd, sizeof(uint16_t) * hd);",
      "memcpy(dst, src + (((size_t)l * 2 + (1 - kv)) * nkv + hh) * hd, sizeof(uint16_t) * hd);",
      [lambda: split_pins.test_split_update_equals_fused(*split_pins._cases()[1])]),
+    ("latent_scatter_layer_stride",
+     "memcpy(pool + (((size_t)layer * num_pool_pages + pg) * P + sl) * (size_t)W,",
+     "memcpy(pool + (((size_t)num_pool_pages + pg) * P + sl) * (size_t)W,",
+     [pins.test_block_latent_scatter_places_rows]),
+    ("latent_scatter_row_stride",
+     "blk_lat + (size_t)k * W, sizeof(uint16_t) * W);",
+     "blk_lat + (size_t)i * W, sizeof(uint16_t) * W);",
+     [pins.test_block_latent_scatter_places_rows]),
 ]
 
 

@@ -517,3 +517,30 @@ def test_block_scatter_places_rows():
                 exp[1, page[r, i], 0, :, slot[r, i]] = bk[r, i]
                 exp[1, page[r, i], 1, :, slot[r, i]] = bv[r, i]
     np.testing.assert_array_equal(pool, exp)
+
+
+def test_block_latent_scatter_places_rows():
+    # MLA block scatter: each placed row's whole latent (latent + rope part)
+    # lands at (layer, page, slot); masked and unplaced rows, every other
+    # slot and every other layer plane keep their nonzero contents.
+    rng = np.random.default_rng(31)
+    B, T, W, P, NP, L = 3, 4, 24, 4, 7, 3
+    g = dict(P=P, num_pool_pages=NP)
+    pool0 = rng.integers(1, 65535, size=(L, NP, P, W)).astype(np.uint16)
+    blk = rng.integers(1, 65535, size=(B, T, W)).astype(np.uint16)
+    page = np.array([[2, 2, 6, 0], [3, 3, 3, -1], [5, 1, -1, -1]], np.int32)
+    slot = np.array([[0, 3, 1, 2], [1, 2, 0, -1], [3, 0, -1, -1]], np.int32)
+    mask = np.array([[1, 1, 1, 0], [1, 1, 1, 0], [1, 1, 0, 0]], np.uint8)
+    for layer in (0, L - 1):
+        pool = pool0.copy()
+        oracle.block_latent_scatter_mla(g, layer, blk, page, slot, mask, pool)
+        exp = pool0.copy()
+        for r in range(B):
+            for i in range(T):
+                if mask[r, i]:
+                    exp[layer, page[r, i], slot[r, i]] = blk[r, i]
+        np.testing.assert_array_equal(pool, exp)
+        # exactly the placed rows changed, and only in this layer's plane
+        changed = np.argwhere(np.any(pool != pool0, axis=-1))
+        assert len(changed) == int(mask.sum())
+        assert set(changed[:, 0].tolist()) == {layer}
