@@ -153,54 +153,183 @@ def test_attention_kv_len_out_of_range_flags(dl):
 
 
 # ---------------------------------------------------------- full sizes
+#
+# With N(0,1) keys and values, outputs at 32K+ keys are ~1/sqrt(keys) in size
+# and the absolute tolerance alone would pass a kernel that dropped a segment.
+# So every full-size case also bounds the relative RMS error, and runs a
+# "peaked" variant: half of the query rows are set to 1.5 x one visible key
+# (spread uniformly over the visible range, so every segment holds some
+# row's key); those rows' outputs are ~ that key's value, O(1), and a dropped
+# or misplaced segment moves them by O(1).
+
+REL_RMS = 1e-2
+
+
+def _peak_gqa(q, pool, tbl, kv_len, g, layer, window, seed, frac=0.5, gain=1.5):
+    rng = np.random.default_rng(seed)
+    q = q.copy()
+    B, Tq, hq, hd = q.shape
+    G, P = hq // g["nkv"], g["P"]
+    n = 0
+    for r in range(B):
+        for i in range(Tq):
+            p = int(kv_len[r]) - Tq + i
+            lo = max(0, p - window + 1) if window > 0 else 0
+            for h in range(hq):
+                if p < lo or rng.random() >= frac:
+                    continue
+                j = int(rng.integers(lo, p + 1))
+                k = bf16_f64(pool[layer, tbl[r, j // P], 0, h // G, j % P])
+                q[r, i, h] = inputs.f32_to_bf16_bits((gain * k).astype(np.float32))
+                n += 1
+    return q, n
+
+
+def _check_full(got, ref, what):
+    assert_close(got, ref, what)
+    err = rel_rms_err(got, ref)
+    assert err < REL_RMS, f"{what}: relative RMS error {err:.3e}"
 
 
 def test_attention_sliding_window_full_size(dl):
     """Sliding-window drafter workload: hq=32, hkv=2, Tq=3, window 1024 + sinks,
-    kv_len 131072, page 64 (and the same read with the window off)."""
+    kv_len 131072, page 64 (and the same read with the window off, plain and
+    peaked)."""
     cfg = inputs.workload("sliding_window")
     prob = inputs.make_problem(cfg, seed=0, with_weights=False)
     g = prob["g"]
     kv_len = np.array([131072], np.int32)
     q = prob["q"][0]
-    for window in (1024, 0):
-        ref = oracle.attention_gqa(g, 0, q, prob["pool"], prob["pages"], kv_len, window=window,
+    qp, n = _peak_gqa(q, prob["pool"], prob["pages"], kv_len, g, 0, 0, seed=21)
+    assert n > 20
+    for window, qq, tag in ((1024, q, ""), (0, q, ""), (0, qp, " peaked")):
+        ref = oracle.attention_gqa(g, 0, qq, prob["pool"], prob["pages"], kv_len, window=window,
                                    sinks=prob["sinks"][0])
-        got, st = _run_gpu(dl, g, 0, q, prob["pool"], prob["pages"], kv_len, window=window,
+        got, st = _run_gpu(dl, g, 0, qq, prob["pool"], prob["pages"], kv_len, window=window,
                            sinks=prob["sinks"][0])
-        assert_close(got, ref, f"sliding window={window}")
+        _check_full(got, ref, f"sliding window={window}{tag}")
         assert st == 0
+        if tag:
+            assert np.sqrt(np.mean(ref ** 2)) > 0.3
 
 
 def test_attention_qwen_32k_full_size_one_layer(dl):
     """Qwen3-8B-shaped drafter at 32K context: all 16 queries x 32 heads of a
-    layer, in the launch configuration the benchmark uses (automatic split)."""
+    layer, in the launch configuration the benchmark uses (automatic split),
+    with plain and peaked queries."""
     prob = inputs.make_problem(inputs.workload("qwen3_8b"), seed=0, with_weights=False)
     g = prob["g"]
     kv_len = np.array([32768 + 16], np.int32)
     layer = 3
     q = prob["q"][layer]
-    ref = oracle.attention_gqa(g, layer, q, prob["pool"], prob["pages"], kv_len)
-    got, st = _run_gpu(dl, g, layer, q, prob["pool"], prob["pages"], kv_len)
-    assert_close(got, ref, "qwen 32k")
-    assert st == 0
+    qp, n = _peak_gqa(q, prob["pool"], prob["pages"], kv_len, g, layer, 0, seed=22)
+    assert n > 200
+    for qq, tag in ((q, ""), (qp, " peaked")):
+        ref = oracle.attention_gqa(g, layer, qq, prob["pool"], prob["pages"], kv_len)
+        got, st = _run_gpu(dl, g, layer, qq, prob["pool"], prob["pages"], kv_len)
+        _check_full(got, ref, "qwen 32k" + tag)
+        assert st == 0
+        if tag:
+            assert np.sqrt(np.mean(ref ** 2)) > 0.3
 
 
-@pytest.mark.parametrize("ctx,mode,window", [(300, 0, 0), (4096, 0, 0), (2500, 1, 700)])
-def test_attention_mla(dl, ctx, mode, window):
+@pytest.mark.parametrize("B", [16, 64])
+def test_attention_batch_sweep_fed_by_gpu_bookkeeping(dl, B):
+    """Batch sweep (per-request contexts U[1K, 8K], 10% at the allocation
+    ceiling): the GPU bookkeeping's decoded table and seq_lens feed the GPU
+    attention; the oracle runs on its own bookkeeping (bit-exact with the
+    GPU's, checked here too)."""
+    import torch
+    cfg = inputs.workload(f"batch_sweep_{B}", L=1)
+    prob = inputs.make_problem(cfg, seed=B, with_weights=False)
+    g = prob["g"]
+    geom = dl.make_geom(g)
+    T, M = g["T"], g["max_pages"]
+    outs = {}
+    for k in dl.STEP_OUTPUT_FIELDS:
+        shape = (B, M) if k == "block_table" else (B, T) if k in (
+            "emb_ids", "ctx_pos", "q_pos", "ctx_dst_page", "ctx_dst_slot", "ctx_wmask", "blk_page",
+            "blk_slot", "blk_mask") else (B,)
+        outs[k] = torch.zeros(shape, dtype=torch.uint8 if k in ("ctx_wmask", "blk_mask")
+                              else torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dl.dflash_step_bookkeeping(geom, to_dev(prob["raw_offsets"]), 1, to_dev(prob["acc"]),
+                               to_dev(prob["n_acc"]), to_dev(prob["ctx_len"]), None,
+                               prob["max_ctx"], prob["mask_id"], outs, st)
+    bk, _ = oracle.bookkeeping(prob["raw_offsets"], prob["acc"], prob["n_acc"], prob["ctx_len"],
+                               None, M=M, T=T, P=g["P"], off_div=1, max_ctx=prob["max_ctx"],
+                               mask_id=prob["mask_id"])
+    for k in ("block_table", "seq_lens"):
+        np.testing.assert_array_equal(outs[k].cpu().numpy(), bk[k], err_msg=k)
+    q = prob["q"][0]
+    ws = torch.empty(dl.dflash_attention_workspace_bytes(geom, B, T, 0), dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0xFF)
+    out = torch.full((B, T, g["hq"], g["hd"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dl.dflash_block_attention(geom, 0, to_dev(q), to_dev(prob["pool"]), outs["block_table"],
+                              outs["seq_lens"], out, ws, dev_status=st)
+    torch.cuda.synchronize()
+    ref = oracle.attention_gqa(g, 0, q, prob["pool"], bk["block_table"], bk["seq_lens"])
+    _check_full(bf16_f64(bits(out)), ref, f"batch sweep B={B}")
+    assert int(st.item()) == 0
+
+
+def _peak_mla(ql, qr, pool, tbl, kv_len, g, layer, window, seed, frac=0.5, gain=0.5):
+    rng = np.random.default_rng(seed)
+    ql, qr = ql.copy(), qr.copy()
+    B, Tq, hq, lat = ql.shape
+    P = g["P"]
+    for r in range(B):
+        for i in range(Tq):
+            p = int(kv_len[r]) - Tq + i
+            lo = max(0, p - window + 1) if window > 0 else 0
+            for h in range(hq):
+                if p < lo or rng.random() >= frac:
+                    continue
+                j = int(rng.integers(lo, p + 1))
+                c = bf16_f64(pool[layer, tbl[r, j // P], j % P]) * gain
+                ql[r, i, h] = inputs.f32_to_bf16_bits(c[:lat].astype(np.float32))
+                qr[r, i, h] = inputs.f32_to_bf16_bits(c[lat:].astype(np.float32))
+    return ql, qr
+
+
+@pytest.mark.parametrize("ctx,mode,window,sinks,heads,peaked", [
+    (300, 0, 0, False, None, False),
+    (4096, 0, 0, False, None, False),
+    (2500, 1, 700, True, None, False),
+    (32768, 0, 0, False, None, False),
+    (32768, 1, 0, True, None, True),
+    (131072, 1, 4096, True, [0, 17, 40, 63], False),
+    (131072, 0, 0, False, [5, 30, 45, 62], True),
+    (393216, 0, 0, True, [3, 33, 48, 60], True),
+    (393216, 1, 100000, False, [1, 22], False),
+])
+def test_attention_mla(dl, ctx, mode, window, sinks, heads, peaked):
     """Absorbed-latent attention of the MLA drafter (hq = 64, one shared
-    512 + 64 latent per token)."""
-    cfg = inputs.workload("mla", ctx=[ctx])
-    prob = inputs.make_problem(cfg, seed=ctx, with_weights=False)
+    512 + 64 latent per token) from 300 to 393K keys, both mask modes, windows
+    and sinks.  The GPU always runs all 64 heads; at 128K+ the oracle checks a
+    sample of heads (every head reads the same latents, so a head subset is
+    the same computation on fewer query rows)."""
+    L = 1 if ctx > 32768 else 3
+    cfg = inputs.workload("mla", ctx=[ctx], L=L)
+    prob = inputs.make_problem(cfg, seed=ctx % 1000, with_weights=False)
     g = prob["g"]
     kv_len = np.array([ctx + g["T"]], np.int32)
-    layer = 1
+    layer = L - 1
     ql, qr = prob["q_lat"][layer], prob["q_rope"][layer]
-    sinks = prob["sinks"][layer] if mode == 1 else None
+    if peaked:
+        ql, qr = _peak_mla(ql, qr, prob["pool"], prob["pages"], kv_len, g, layer, window,
+                           seed=ctx + 1)
+    sk = prob["sinks"][layer] if sinks else None
     scale = inputs.attention_scale(g)
-    ref = oracle.attention_mla(g, layer, ql, qr, prob["pool"], prob["pages"], kv_len,
-                               window=window, sinks=sinks, scale=scale, mask_mode=mode)
     got, st = _run_gpu(dl, g, layer, ql, prob["pool"], prob["pages"], kv_len, window=window,
-                       sinks=sinks, mask_mode=mode, q_rope=qr, scale=scale)
-    assert_close(got, ref, f"mla ctx={ctx}")
+                       sinks=sk, mask_mode=mode, q_rope=qr, scale=scale)
+    hs = list(range(g["hq"])) if heads is None else heads
+    ref = oracle.attention_mla(dict(g, hq=len(hs)), layer, np.ascontiguousarray(ql[:, :, hs]),
+                               np.ascontiguousarray(qr[:, :, hs]), prob["pool"], prob["pages"],
+                               kv_len, window=window, sinks=None if sk is None else sk[hs],
+                               scale=scale, mask_mode=mode)
+    _check_full(got[:, :, hs], ref, f"mla ctx={ctx} mode={mode} window={window}")
     assert st == 0
+    if peaked:
+        assert np.sqrt(np.mean(ref ** 2)) > 0.2

@@ -229,8 +229,11 @@ def test_update_dummies_bad_pages_and_ceiling(dl):
     assert st & 8  # DFLASH_DEV_BAD_PAGE
 
 
-def test_update_mla(dl):
-    prob = inputs.make_problem(inputs.workload("mla", ctx=[2048]), seed=2)
+@pytest.mark.parametrize("ctx", [2048, 32768, 131072 + 5])
+def test_update_mla(dl, ctx):
+    """MLA latent update; the long contexts put the rope part's angles at
+    positions past 32K and 128K."""
+    prob = inputs.make_problem(inputs.workload("mla", ctx=[ctx], n_acc=[8]), seed=2)
     pool_ref, ctx_ref, pool_gpu, ctx_gpu, st = _update_both(dl, prob)
     n = _check_pool(prob, pool_ref, pool_gpu)
     assert n == prob["g"]["L"] * int(prob["n_acc"][0])
