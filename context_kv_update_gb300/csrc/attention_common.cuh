@@ -108,9 +108,10 @@ __device__ __forceinline__ void row_key_range(const AttnParams &p, int kv_len, i
 struct SegRange {
   int kv_len, k0, k1, t0, t1;
 };
-__device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, int s) {
+// The same from a given (already clamped) kv_len.
+__device__ __forceinline__ SegRange segment_range_for(const AttnParams &p, int kv_len, int s) {
   SegRange sr;
-  sr.kv_len = clamped_kv_len(p, r, s == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+  sr.kv_len = kv_len;
   sr.k0 = sr.k1 = sr.t0 = sr.t1 = 0;
   if (sr.kv_len <= 0) return sr;
   int lo0, hi0;
@@ -128,6 +129,10 @@ __device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, in
   sr.k0 = max(lo0, sr.t0 * kAttnTileKeys);
   sr.k1 = min(sr.kv_len, sr.t1 * kAttnTileKeys);
   return sr;
+}
+__device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, int s) {
+  return segment_range_for(p, clamped_kv_len(p, r, s == 0 && blockIdx.y == 0 && threadIdx.x == 0),
+                           s);
 }
 
 // Cache rows of key j (GQA: K and V of head kvh; MLA: the latent row twice).

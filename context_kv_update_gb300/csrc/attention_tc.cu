@@ -126,6 +126,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tslot;
   griddep_launch();
+  if (warp == 2) {
+    // While the preceding grid finishes, pull this segment's first ring-full
+    // of K/V into L2.  kv_len and the table may still be changing, so they
+    // are read with relaxed loads and used for nothing but this hint: L2 is
+    // the point of coherence, so a prefetched line never hides a later write
+    // from the copies below, and a wrong guess only costs bandwidth.
+    int kl = ptx::ld_relaxed_s32(p.kv_len + r);
+    const long long cap = static_cast<long long>(p.M) * p.P;
+    kl = kl < 0 ? 0 : (kl > cap ? static_cast<int>(cap) : kl);
+    const SegRange g = segment_range_for(p, kl, s);
+    const int boxes = kKT / P.box_rows;
+    const int nbox = boxes * 2 * P.chunks;
+    const int npre = min(g.t1 - g.t0, P.nst) * nbox;
+    for (int j = lane; j < npre; j += 32) {
+      const int tt = j / nbox, jb = j % nbox;
+      const int b = jb / (2 * P.chunks), kv = (jb / P.chunks) & 1, c = jb % P.chunks;
+      const int key0 = (g.t0 + tt) * kKT + b * P.box_rows;
+      const int lp = key0 / p.P;
+      if (lp < p.M && key0 < g.kv_len) {
+        const int page = ptx::ld_relaxed_s32(p.tbl + static_cast<int64_t>(r) * p.M + lp);
+        if (page >= 0 && page < p.NP) {
+          const long long row0 =
+              ((((static_cast<long long>(p.layer) * p.NP + page) * 2 + kv) * p.nkv + kvh) * p.P) +
+              key0 % p.P;
+          ptx::tma_prefetch_2d(&tm, c * 64, static_cast<int32_t>(row0));
+        }
+      }
+    }
+  }
   // Everything above overlaps the previous kernel's tail; inputs are read
   // only after it has completed.
   griddep_wait();
@@ -284,14 +313,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 ptx::mbar_wait(ptx::smem_u32(&kv_full[0]), 0u, abort_flag);
       ptx::tc_fence_after();
       if (ok) issue_qk(0);
+      // QK of tile t+1 goes ahead of PV of tile t only when t+1 has already
+      // landed; otherwise PV(t) goes first, so tile t's ring stage is released
+      // without waiting for the next tile's copies.
+      int next_qk = 1;
       for (int t = 0; ok && t < ntiles; ++t) {
         const int tn = t + 1;
-        if (tn < ntiles) {
-          ok = ptx::mbar_wait(ptx::smem_u32(&kv_full[tn % nst]),
-                              static_cast<uint32_t>((tn / nst) & 1), abort_flag);
-          if (!ok) break;
+        if (tn < ntiles &&
+            ptx::mbar_test(ptx::smem_u32(&kv_full[tn % nst]), static_cast<uint32_t>((tn / nst) & 1))) {
           ptx::tc_fence_after();
           issue_qk(tn);
+          next_qk = tn + 1;
         }
         ok = ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag);
         if (!ok) break;
@@ -306,6 +338,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         ptx::mma_commit(ptx::smem_u32(o_done));
         ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
+        if (tn < ntiles && next_qk == tn) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&kv_full[tn % nst]),
+                              static_cast<uint32_t>((tn / nst) & 1), abort_flag);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_qk(tn);
+          next_qk = tn + 1;
+        }
       }
       if (!ok) {
         ptx::mma_commit(ptx::smem_u32(drain));
