@@ -427,10 +427,61 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         attn_ms = sum(s.elapsed_time(e) for s, e in evs) / len(evs)
 
+    attn_ss_ms, floor_ms = attention_steady_state(dl, step, stream)
     e2e = run_e2e(dl, step, stream, min(args.steps, 200))
     st = int(step.status.item())
-    return dict(ms_step=ms_step, attn_ms=attn_ms, clocks=clocks, e2e=e2e, prob=prob, status=st,
-                warmup_done=w)
+    return dict(ms_step=ms_step, attn_ms=attn_ms, attn_ss_ms=attn_ss_ms, floor_ms=floor_ms,
+                clocks=clocks, e2e=e2e, prob=prob, status=st, warmup_done=w)
+
+
+def attention_steady_state(dl, step, stream, rounds=5):
+    """Per-call duration of dflash_block_attention (main kernel + merge) in
+    steady state: one CUDA graph of `rounds` passes over the L layers' calls
+    back to back (each call reads its own layer plane of the pool, together
+    larger than L2), events only around the replay, divided by the number of
+    calls.  Also returns the floor of a per-call event pair: the same event
+    pair around one trivial kernel."""
+    import torch
+    g, o = step.g, step.outs
+    n = rounds * g["L"]
+
+    def calls():
+        for _ in range(rounds):
+            for layer in range(g["L"]):
+                dl.dflash_block_attention(
+                    step.geom, layer, step.q[layer], step.pool, o["block_table"], o["seq_lens"],
+                    step.attn_out[layer], step.attn_ws,
+                    q_rope=None if step.q_rope is None else step.q_rope[layer],
+                    window=step.prob["window"], sinks=step.sinks, scale=step.scale,
+                    dev_status=step.status)
+
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        calls()
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = None
+    for _ in range(5):
+        s.record(stream)
+        with torch.cuda.stream(stream):
+            gr.replay()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / n
+        best = ms if best is None else min(best, ms)
+    # floor of an event pair around one tiny kernel
+    x = torch.zeros(1, device="cuda")
+    floors = []
+    with torch.cuda.stream(stream):
+        for _ in range(25):
+            s.record(stream)
+            x.add_(1.0)
+            e.record(stream)
+            torch.cuda.synchronize()
+            floors.append(s.elapsed_time(e))
+    return best, statistics.median(floors[5:])
 
 
 def run_e2e(dl, step, stream, steps):
@@ -657,7 +708,10 @@ def main():
     headline = tag == WORKLOAD_TAG
     attn_bytes, attn_flops, kv_len = attention_work(prob)
     peaks = measured_peaks()
-    attn_s = res["attn_ms"] * 1e-3
+    # the roofline takes the steady-state per-call duration (calls back to
+    # back, as the layer loop issues them); the per-call figure inside the
+    # step, bracketed by an event pair each, is reported beside it
+    attn_s = res["attn_ss_ms"] * 1e-3
     us = res["ms_step"] * 1000.0
     # HBM-bound unless the call's arithmetic intensity is above the ridge point
     if attn_flops / attn_bytes > peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9):
@@ -678,7 +732,12 @@ def main():
                 "traffic": traffic, "bytes_per_launch": attn_bytes,
                 "peak_source": peaks["source"] + " hbm_gbs (of " + peaks["source"] + ")"}
     roof.update({"kernel": "dflash_block_attention (split + merge)",
-                 "launch_ms": round(res["attn_ms"], 5)})
+                 "launch_ms": round(res["attn_ss_ms"], 5),
+                 "launch_timing": "CUDA-graph replay of 5 x L back-to-back calls (one layer "
+                                  "plane each), CUDA events around the replay",
+                 "isolated_call_ms": round(res["attn_ms"], 5),
+                 "isolated_timing": "event pair around each call inside the step graph",
+                 "event_pair_floor_ms": round(res["floor_ms"], 5)})
     config = {"workload": tag, "B": prob["B"],
               "ctx_len": CTX if headline else [int(x) for x in prob["ctx_len"][:8]],
               "kv_len": kv_len, "layers": g["L"], "hq": g["hq"], "nkv": g["nkv"],
