@@ -5,7 +5,9 @@ and split-KV block attention, behind the C ABI of include/dflash.h.
 The Python names below are the C entry points of the same names (ctypes
 marshalling only).  ``inputs`` holds the seeded synthetic workloads.
 """
-from ._lib import (DflashError, Geom, StepOutputs, Weights, STEP_OUTPUT_FIELDS,  # noqa: F401
+from ._lib import (DflashError, Geom, LayerWeights, StepOutputs, Weights,  # noqa: F401
+                   STEP_OUTPUT_FIELDS, dflash_embedding_gather, dflash_pack_weights,
+                   dflash_packed_gamma_bytes, dflash_packed_kv_bytes, dflash_strict_accept,
                    dflash_attention_num_segments, dflash_attention_workspace_bytes,
                    dflash_block_attention, dflash_block_attention_noalloc,
                    dflash_block_attention_noalloc_max_scratch_bytes, dflash_block_kv_scatter,

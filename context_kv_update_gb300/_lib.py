@@ -27,6 +27,7 @@ DEV_CTX_OUTRUN = 4
 DEV_BAD_PAGE = 8
 DEV_KV_LEN_RANGE = 16
 DEV_WAIT_TIMEOUT = 32
+DEV_BAD_TOKEN = 64
 
 KIND_GQA = 0
 KIND_MLA = 1
@@ -40,7 +41,9 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_attention_workspace_bytes", "dflash_block_attention", "dflash_status_string",
            "dflash_abi_version", "dflash_block_attention_noalloc",
            "dflash_block_attention_noalloc_max_scratch_bytes", "dflash_ctx_staged_bytes",
-           "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope")
+           "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
+           "dflash_packed_kv_bytes", "dflash_packed_gamma_bytes", "dflash_pack_weights",
+           "dflash_strict_accept", "dflash_embedding_gather")
 
 
 class DflashError(RuntimeError):
@@ -64,6 +67,10 @@ class Geom(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("w_fc", ctypes.c_void_p), ("gamma_h", ctypes.c_void_p),
                 ("w_kv", ctypes.c_void_p), ("gamma_k", ctypes.c_void_p)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("w_k", ctypes.c_void_p), ("w_v", ctypes.c_void_p), ("k_norm", ctypes.c_void_p)]
 
 
 class StepOutputs(ctypes.Structure):
@@ -115,12 +122,21 @@ def load():
     lib.dflash_block_attention_noalloc.restype = ctypes.c_int
     lib.dflash_block_attention_noalloc_max_scratch_bytes.argtypes = []
     lib.dflash_block_attention_noalloc_max_scratch_bytes.restype = sz
+    lib.dflash_packed_kv_bytes.argtypes = [G]
+    lib.dflash_packed_kv_bytes.restype = sz
+    lib.dflash_packed_gamma_bytes.argtypes = [G]
+    lib.dflash_packed_gamma_bytes.restype = sz
+    lib.dflash_pack_weights.argtypes = [G, ctypes.POINTER(LayerWeights), vp, vp, vp]
+    lib.dflash_strict_accept.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp, vp, vp]
+    lib.dflash_embedding_gather.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, vp,
+                                            vp, vp]
     lib.dflash_status_string.argtypes = [ctypes.c_int]
     lib.dflash_status_string.restype = ctypes.c_char_p
     lib.dflash_abi_version.argtypes = []
     for name in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
                  "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version",
-                 "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope"):
+                 "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
+                 "dflash_pack_weights", "dflash_strict_accept", "dflash_embedding_gather"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -263,8 +279,7 @@ def dflash_block_attention(geom, layer, q, kv_pool, block_table, kv_len, out, wo
                            stream=None):
     lib = load()
     B, Tq = int(q.shape[0]), int(q.shape[1])
-    if scale is None:
-        scale = (1.0 / (geom.head_dim ** 0.5)) if geom.kind == KIND_GQA else 1.0 / (192 ** 0.5)
+    scale = 0.0 if scale is None else scale  # 0 = the library's default scale
     _check("dflash_block_attention", lib.dflash_block_attention(
         ctypes.byref(geom), B, layer, Tq, _ptr(q), _ptr(q_rope), _ptr(kv_pool), _ptr(block_table),
         _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
@@ -284,9 +299,50 @@ def dflash_block_attention_noalloc(geom, layer, q, kv_pool, block_table, kv_len,
     argument, nothing allocated)."""
     lib = load()
     B, Tq = int(q.shape[0]), int(q.shape[1])
-    if scale is None:
-        scale = (1.0 / (geom.head_dim ** 0.5)) if geom.kind == KIND_GQA else 1.0 / (192 ** 0.5)
+    scale = 0.0 if scale is None else scale  # 0 = the library's default scale
     _check("dflash_block_attention_noalloc", lib.dflash_block_attention_noalloc(
         ctypes.byref(geom), B, layer, Tq, _ptr(q), _ptr(q_rope), _ptr(kv_pool), _ptr(block_table),
         _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
         _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def dflash_packed_kv_bytes(geom) -> int:
+    return int(load().dflash_packed_kv_bytes(ctypes.byref(geom)))
+
+
+def dflash_packed_gamma_bytes(geom) -> int:
+    return int(load().dflash_packed_gamma_bytes(ctypes.byref(geom)))
+
+
+def dflash_pack_weights(geom, layers, w_kv, gamma_k, stream=None):
+    """layers: one (w_k, w_v or None, k_norm) tuple of bf16 CUDA tensors per
+    drafter layer; w_kv / gamma_k: preallocated CUDA outputs of
+    dflash_packed_kv_bytes / dflash_packed_gamma_bytes bytes."""
+    lib = load()
+    arr = (LayerWeights * len(layers))(*[
+        LayerWeights(w_k=wk.data_ptr(), w_v=None if wv is None else wv.data_ptr(),
+                     k_norm=kn.data_ptr()) for wk, wv, kn in layers])
+    _check("dflash_pack_weights", lib.dflash_pack_weights(
+        ctypes.byref(geom), arr, _ptr(w_kv), _ptr(gamma_k), _stream(stream)))
+
+
+def dflash_strict_accept(draft, target, n_accepted, accepted, stream=None):
+    """draft int32 [B, K] / target int32 [B, K + 1] CUDA tensors (row-strided
+    views allowed, unit column stride); n_accepted [B], accepted [B, K + 1]
+    preallocated."""
+    lib = load()
+    B, K = int(target.shape[0]), int(target.shape[1]) - 1
+    assert target.stride(1) == 1 and (K == 0 or draft.stride(1) == 1)
+    _check("dflash_strict_accept", lib.dflash_strict_accept(
+        B, K, _ptr(draft), draft.stride(0) if K > 0 else 0, _ptr(target), target.stride(0),
+        _ptr(n_accepted), _ptr(accepted), _stream(stream)))
+
+
+def dflash_embedding_gather(ids, table, out, dev_status=None, stream=None):
+    """ids int32 CUDA tensor (any shape, contiguous), table bf16 [vocab, dim],
+    out bf16 [ids.numel(), dim] (or ids.shape + (dim,))."""
+    lib = load()
+    vocab, dim = int(table.shape[0]), int(table.shape[1])
+    _check("dflash_embedding_gather", lib.dflash_embedding_gather(
+        int(ids.numel()), _ptr(ids), _ptr(table), vocab, dim, _ptr(out), _ptr(dev_status),
+        _stream(stream)))

@@ -4,11 +4,9 @@
 //
 // Who needs it: callers that cannot allocate device memory at the point where
 // they run the attention -- a plugin whose host framework owns all device
-// memory and offers it no allocator, code that runs while a stream is being
-// captured into a CUDA graph (cudaMalloc is not allowed there and a
-// caller-side pool may not exist), or a latency-critical loop that must never
-// block in the allocator.  Such a caller still owns q, the pool, the tables
-// and the output; only the scratch comes from here.
+// memory and offers it no allocator, or a latency-critical loop that must
+// never block in the allocator.  Such a caller still owns q, the pool, the
+// tables and the output; only the scratch comes from here.
 //
 // The scratch is one file-scope __device__ array of kNoAllocScratchBytes.  It
 // exists on every GPU that loads this library, for the life of the process.
@@ -34,6 +32,8 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 constexpr int kMaxDevices = 64;
 void *g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
 
 cudaError_t scratch_address(void **out) {
   int dev = 0;
@@ -67,14 +67,21 @@ extern "C" int dflash_block_attention_noalloc(const dflash_geom *g, int B, int l
                                               const float *sinks, float scale, int mask_mode,
                                               int num_segments, void *out, int32_t *dev_status,
                                               dflash_stream_t stream) {
-  if (!g || B < 0 || Tq < 1 || num_segments < 0) return DFLASH_ERR_INVALID_ARG;
+  // the argument checks of dflash_block_attention, then the size limit, then
+  // the buffer pointers
+  if (const int st =
+          attention_args_status(g, B, layer, Tq, q_rope, window, &scale, mask_mode, num_segments))
+    return st;
   if (B == 0) return DFLASH_OK;
-  const size_t need = dflash_attention_workspace_bytes(g, B, Tq, num_segments);
-  if (need == 0) return DFLASH_ERR_INVALID_ARG;
-  if (need > kNoAllocScratchBytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  const int S = num_segments > 0 ? num_segments : attention_num_segments(*g, B, Tq);
+  if (attention_workspace_bytes(*g, B, Tq, S) > kNoAllocScratchBytes)
+    return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  if (const int st = attention_ptrs_status(B, q, q_rope, kv_pool, block_table, kv_len, out))
+    return st;
   void *scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return DFLASH_ERR_CUDA;
-  return dflash_block_attention(g, B, layer, Tq, q, q_rope, kv_pool, block_table, kv_len, window,
-                                sinks, scale, mask_mode, num_segments, scratch,
-                                kNoAllocScratchBytes, out, dev_status, stream);
+  return cuda_status(launch_block_attention(*g, B, layer, Tq, q, q_rope, kv_pool, block_table,
+                                            kv_len, window, sinks, scale, mask_mode, S, scratch,
+                                            out, dev_status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -87,6 +87,56 @@ extern "C" int dflash_step_bookkeeping(const dflash_geom *g, int B, const int32_
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" size_t dflash_packed_kv_bytes(const dflash_geom *g) {
+  if (!geom_ok(g)) return 0;
+  return packed_kv_bytes(*g);
+}
+
+extern "C" size_t dflash_packed_gamma_bytes(const dflash_geom *g) {
+  if (!geom_ok(g)) return 0;
+  return packed_gamma_bytes(*g);
+}
+
+extern "C" int dflash_pack_weights(const dflash_geom *g, const dflash_layer_weights *layers,
+                                   void *w_kv, void *gamma_k, dflash_stream_t stream) {
+  if (!geom_ok(g) || !layers || !w_kv || !gamma_k) return DFLASH_ERR_INVALID_ARG;
+  if (g->num_layers > max_pack_layers() || g->d_model % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  const bool gqa = g->kind == DFLASH_KIND_GQA;
+  if (!aligned16(w_kv) || (reinterpret_cast<uintptr_t>(gamma_k) & 1u)) return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < g->num_layers; ++l) {
+    const dflash_layer_weights &w = layers[l];
+    if (!w.w_k || !w.k_norm || !aligned16(w.w_k) || (reinterpret_cast<uintptr_t>(w.k_norm) & 1u))
+      return DFLASH_ERR_INVALID_ARG;
+    if (gqa ? (!w.w_v || !aligned16(w.w_v)) : (w.w_v != nullptr)) return DFLASH_ERR_INVALID_ARG;
+  }
+  return cuda_status(
+      launch_pack_weights(*g, layers, w_kv, gamma_k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_strict_accept(int B, int K, const int32_t *draft, int64_t draft_row_stride,
+                                    const int32_t *target, int64_t target_row_stride,
+                                    int32_t *n_accepted, int32_t *accepted,
+                                    dflash_stream_t stream) {
+  if (B < 0 || K < 0) return DFLASH_ERR_INVALID_ARG;
+  if (B == 0) return DFLASH_OK;
+  if (!target || !n_accepted || !accepted || (K > 0 && !draft)) return DFLASH_ERR_INVALID_ARG;
+  if (draft_row_stride < K || target_row_stride < K + 1) return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(launch_strict_accept(B, K, draft, draft_row_stride, target,
+                                          target_row_stride, n_accepted, accepted,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_embedding_gather(int n, const int32_t *ids, const void *table, int vocab,
+                                       int dim, void *out, int32_t *dev_status,
+                                       dflash_stream_t stream) {
+  if (n < 0 || vocab < 1) return DFLASH_ERR_INVALID_ARG;
+  if (dim < 8 || dim % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  if (n == 0) return DFLASH_OK;
+  if (!ids || !table || !out || !aligned16(table) || !aligned16(out)) return DFLASH_ERR_INVALID_ARG;
+  return cuda_status(launch_embedding_gather(n, ids, table, vocab, dim, out, dev_status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" size_t dflash_ctx_workspace_bytes(const dflash_geom *g, int B) {
   if (!geom_ok(g) || B < 0) return 0;
   return ctx_workspace_bytes(*g, B);
@@ -232,26 +282,28 @@ extern "C" size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
   return attention_workspace_bytes(*g, B, Tq, num_segments);
 }
 
-extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq,
-                                      const void *q, const void *q_rope, const void *kv_pool,
-                                      const int32_t *block_table, const int32_t *kv_len,
-                                      int32_t window, const float *sinks, float scale,
-                                      int mask_mode, int num_segments, void *workspace,
-                                      size_t ws_bytes, void *out, int32_t *dev_status,
-                                      dflash_stream_t stream) {
+namespace dflash {
+
+// Host-side checks of a block-attention call, shared by the workspace and the
+// allocation-free entry points: first the arguments (geometry, indices,
+// modes, scale -- resolving scale <= 0 to the method's default), then the
+// buffer pointers.  B == 0 passes both (nothing to do).
+int attention_args_status(const dflash_geom *g, int B, int layer, int Tq, const void *q_rope,
+                          int32_t window, float *scale, int mask_mode, int num_segments) {
   if (!geom_ok(g) || B < 0 || Tq < 1 || layer < 0 || layer >= g->num_layers || window < 0 ||
       num_segments < 0)
     return DFLASH_ERR_INVALID_ARG;
   if (mask_mode != DFLASH_MASK_CAUSAL_TAIL && mask_mode != DFLASH_MASK_BLOCK_BIDIR)
     return DFLASH_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return DFLASH_ERR_INVALID_ARG;
+  if (!std::isfinite(*scale)) return DFLASH_ERR_INVALID_ARG;
   if (g->kind == DFLASH_KIND_GQA) {
     if (g->head_dim != 64 && g->head_dim != 128) return DFLASH_ERR_UNSUPPORTED_GEOM;
     if (q_rope) return DFLASH_ERR_INVALID_ARG;
   } else {
     if (g->latent_dim != 512 || g->rope_dim != 64) return DFLASH_ERR_UNSUPPORTED_GEOM;
-    if (!q_rope) return DFLASH_ERR_INVALID_ARG;
+    if (B > 0 && !q_rope) return DFLASH_ERR_INVALID_ARG;
   }
+  if (!(*scale > 0.f)) *scale = default_attention_scale(*g);
   const int P = g->page_size;
   if (P % 8 != 0 || !(kAttnTileKeys % P == 0 || P % kAttnTileKeys == 0))
     return DFLASH_ERR_UNSUPPORTED_GEOM;
@@ -259,11 +311,41 @@ extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, in
   const long long pool_rows = static_cast<long long>(g->num_layers) * g->num_pool_pages * P *
                               (g->kind == DFLASH_KIND_GQA ? 2LL * g->nkv : 1LL);
   if (pool_rows >= (1LL << 31)) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  return DFLASH_OK;
+}
+
+int attention_ptrs_status(int B, const void *q, const void *q_rope, const void *kv_pool,
+                          const int32_t *block_table, const int32_t *kv_len, const void *out) {
   if (B == 0) return DFLASH_OK;
-  if (!q || !kv_pool || !block_table || !kv_len || !workspace || !out) return DFLASH_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(workspace) || !aligned16(out) ||
-      (q_rope && !aligned16(q_rope)))
+  if (!q || !kv_pool || !block_table || !kv_len || !out) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || (q_rope && !aligned16(q_rope)))
     return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+float default_attention_scale(const dflash_geom &g) {
+  // GQA: 1/sqrt(head_dim).  MLA: the absorbed-latent form keeps the scale of
+  // the unabsorbed head, a 128-wide no-rope part plus the rope part.
+  const double d = (g.kind == DFLASH_KIND_GQA) ? g.head_dim : 128.0 + g.rope_dim;
+  return static_cast<float>(1.0 / std::sqrt(d));
+}
+
+}  // namespace dflash
+
+extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, int Tq,
+                                      const void *q, const void *q_rope, const void *kv_pool,
+                                      const int32_t *block_table, const int32_t *kv_len,
+                                      int32_t window, const float *sinks, float scale,
+                                      int mask_mode, int num_segments, void *workspace,
+                                      size_t ws_bytes, void *out, int32_t *dev_status,
+                                      dflash_stream_t stream) {
+  if (const int st =
+          attention_args_status(g, B, layer, Tq, q_rope, window, &scale, mask_mode, num_segments))
+    return st;
+  if (B == 0) return DFLASH_OK;
+  if (const int st = attention_ptrs_status(B, q, q_rope, kv_pool, block_table, kv_len, out))
+    return st;
+  if (!workspace || !aligned16(workspace)) return DFLASH_ERR_INVALID_ARG;
   const int S = num_segments > 0 ? num_segments : attention_num_segments(*g, B, Tq);
   if (ws_bytes < attention_workspace_bytes(*g, B, Tq, S)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
   return cuda_status(launch_block_attention(*g, B, layer, Tq, q, q_rope, kv_pool, block_table,

@@ -128,7 +128,26 @@ cudaError_t launch_block_scatter(const dflash_geom &g, int B, int layer, const v
                                  const void *blk_v, const int32_t *page, const int32_t *slot,
                                  const uint8_t *mask, void *pool, int32_t *st, cudaStream_t s);
 
+// weight packing (stacked per-layer K/V or latent projections and norm gains)
+size_t packed_kv_bytes(const dflash_geom &g);
+size_t packed_gamma_bytes(const dflash_geom &g);
+int max_pack_layers();
+cudaError_t launch_pack_weights(const dflash_geom &g, const dflash_layer_weights *layers,
+                                void *w_kv, void *gamma, cudaStream_t s);
+
+// either side of the path: strict acceptance, the noise-block embedding lookup
+cudaError_t launch_strict_accept(int B, int K, const int32_t *draft, int64_t draft_stride,
+                                 const int32_t *target, int64_t target_stride, int32_t *n_acc,
+                                 int32_t *accepted, cudaStream_t s);
+cudaError_t launch_embedding_gather(int n, const int32_t *ids, const void *table, int vocab,
+                                    int dim, void *out, int32_t *st, cudaStream_t s);
+
 int attention_num_segments(const dflash_geom &g, int B, int Tq);
+float default_attention_scale(const dflash_geom &g);
+int attention_args_status(const dflash_geom *g, int B, int layer, int Tq, const void *q_rope,
+                          int32_t window, float *scale, int mask_mode, int num_segments);
+int attention_ptrs_status(int B, const void *q, const void *q_rope, const void *kv_pool,
+                          const int32_t *block_table, const int32_t *kv_len, const void *out);
 size_t attention_workspace_bytes(const dflash_geom &g, int B, int Tq, int S);
 cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int Tq, const void *q,
                                    const void *q_rope, const void *pool, const int32_t *tbl,

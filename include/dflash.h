@@ -14,10 +14,14 @@
  *  - All pointers named as device buffers are device pointers the caller owns
  *    and keeps alive until the work on `stream` has finished.  No call
  *    allocates memory, synchronises the host, or reads a device value on the
- *    host, so every call may be captured in a CUDA graph.
+ *    host.  The calls of the decode step (bookkeeping, context update,
+ *    scatter, attention) may be captured in a CUDA graph; each makes its
+ *    one-time per-device set-up on its first eager call.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously; a return of DFLASH_OK means "validated and
- *    enqueued", not "finished".
+ *    enqueued", not "finished".  The device current on the calling thread
+ *    must be the device of `stream` (launch limits, SM counts and the
+ *    allocation-free scratch are looked up for the current device).
  *  - bf16 means IEEE bfloat16 (1-8-7).  Every tensor is dense row-major in the
  *    stated shape unless a row stride is given.  Device buffers read with
  *    vector loads or TMA (KV pool, weights, hidden, q, block K/V, workspace)
@@ -83,6 +87,7 @@ enum dflash_status_code {
 #define DFLASH_DEV_BAD_PAGE 8u        /* table entry outside [0, num_pool_pages): row/key masked */
 #define DFLASH_DEV_KV_LEN_RANGE 16u   /* kv_len < 0 or > max_pages * page_size: clamped */
 #define DFLASH_DEV_WAIT_TIMEOUT 32u   /* an on-chip pipeline wait hit its iteration limit */
+#define DFLASH_DEV_BAD_TOKEN 64u      /* embedding id outside [0, vocab): zero row written */
 
 enum dflash_kind { DFLASH_KIND_GQA = 0, DFLASH_KIND_MLA = 1 };
 enum dflash_mask_mode { DFLASH_MASK_CAUSAL_TAIL = 0, DFLASH_MASK_BLOCK_BIDIR = 1 };
@@ -127,6 +132,19 @@ typedef struct dflash_weights {
   const void *gamma_k;
 } dflash_weights;
 
+/* One drafter layer's projection weights as a model holds them (device,
+ * bf16, row-major), the input of dflash_pack_weights.
+ *  w_k     GQA: k_proj [nkv * head_dim, d_model]
+ *          MLA: the latent (down) projection [latent_dim + rope_dim, d_model]
+ *  w_v     GQA: v_proj [nkv * head_dim, d_model]; MLA: NULL
+ *  k_norm  GQA: the k RMSNorm gain [head_dim]; MLA: the latent RMSNorm gain
+ *          [latent_dim] */
+typedef struct dflash_layer_weights {
+  const void *w_k;
+  const void *w_v;
+  const void *k_norm;
+} dflash_layer_weights;
+
 /* Outputs of dflash_step_bookkeeping (all device, int32 unless noted;
  * [B] or [B, T] or [B, M] dense). */
 typedef struct dflash_step_outputs {
@@ -146,6 +164,75 @@ typedef struct dflash_step_outputs {
   int32_t *ctx_len_new;  /* [B]    c' = min(c + n, A) (advertised context length) */
   int32_t *seq_lens;     /* [B]    c' + T (kv_len of the block attention) */
 } dflash_step_outputs;
+
+/* ---------------------------------------------------------------------
+ * dflash_pack_weights -- stack every drafter layer's K/V (GQA) or latent (MLA)
+ * projection into the one matrix the context update's GEMM reads, and the
+ * layers' norm gains into one array [TRT-13995, "per-layer cached K/V pool":
+ * one GEMM stacked across the drafter layers; "fuse cross-layer k_norm": the
+ * k_norm weights stacked once so one RMSNorm covers every layer].
+ *
+ * layers   HOST array of num_layers entries; each names that layer's device
+ *          tensors (dflash_layer_weights).  w_k / w_v 16-byte aligned.
+ * w_kv     device output, dflash_packed_kv_bytes(g) bytes, 16-byte aligned:
+ *          GQA [L][2][nkv][head_dim][d_model] (row block 0 = w_k, 1 = w_v),
+ *          MLA [L][latent_dim + rope_dim][d_model].
+ * gamma_k  device output, dflash_packed_gamma_bytes(g) bytes: GQA
+ *          [L][head_dim], MLA [L][latent_dim].
+ * The copy is bit-exact (no conversion).  Done once at model load; the
+ * outputs are the dflash_weights.w_kv / gamma_k of the context update.
+ * Errors: DFLASH_ERR_INVALID_ARG (null or misaligned pointers),
+ * DFLASH_ERR_UNSUPPORTED_GEOM (more than 64 layers, d_model not a multiple of
+ * 8), DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API size_t dflash_packed_kv_bytes(const dflash_geom *g);
+DFLASH_API size_t dflash_packed_gamma_bytes(const dflash_geom *g);
+DFLASH_API int dflash_pack_weights(const dflash_geom *g, const dflash_layer_weights *layers,
+                                   void *w_kv, void *gamma_k, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * dflash_strict_accept -- acceptance of a uniform-width draft, one launch,
+ * ahead of the bookkeeping [TRT-20550, follow-up commit "spec_tail_kernels.py":
+ * strict acceptance of a uniform-width draft is one launch].
+ *
+ * Request r drafted K tokens draft[r, 0..K-1]; the target produced K + 1
+ * tokens target[r, 0..K] at the same positions.  Drafts are accepted while
+ * they equal the target's token; the target's token at the first
+ * disagreement (or after the last draft) is the bonus:
+ *   n_accepted[r] = 1 + (number of leading i with draft[r,i] == target[r,i]),
+ *   accepted[r, i] = target[r, i] for i < n_accepted[r], -1 after.
+ * So accepted[r, n - 1] is the bonus token dflash_step_bookkeeping reads, and
+ * (accepted, K + 1, n_accepted) can be passed to it as (accepted_tokens,
+ * acc_row_stride, n_accepted) with block_size = K + 1.
+ *
+ * draft       device int32, row r at draft + r * draft_row_stride (K entries).
+ * target      device int32, row r at target + r * target_row_stride (K + 1).
+ * n_accepted  device int32 [B] (out).  accepted  device int32 [B, K + 1] (out).
+ * Errors: DFLASH_ERR_INVALID_ARG (null pointers, B < 0, K < 0, strides below
+ * the row widths), DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_strict_accept(int B, int K, const int32_t *draft, int64_t draft_row_stride,
+                                    const int32_t *target, int64_t target_row_stride,
+                                    int32_t *n_accepted, int32_t *accepted,
+                                    dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * dflash_embedding_gather -- the noise block's input rows, one lookup over
+ * the block's ids [TRT-13995, "fuse query-input build in pure Torch + fused
+ * embedding lookup": one embed_tokens call over [bonus..., mask_token_id]].
+ *
+ * out[k, :] = table[ids[k], :] for k < n (e.g. ids = the bookkeeping's
+ * emb_ids, n = B * T).  An id outside [0, vocab) writes a zero row and ORs
+ * DFLASH_DEV_BAD_TOKEN into *dev_status.
+ * ids    device int32 [n].  table  device bf16 [vocab, dim], 16-byte aligned.
+ * out    device bf16 [n, dim], 16-byte aligned.
+ * Errors: DFLASH_ERR_INVALID_ARG (null or misaligned pointers, n < 0,
+ * vocab < 1), DFLASH_ERR_UNSUPPORTED_GEOM (dim not a positive multiple of 8),
+ * DFLASH_ERR_CUDA.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_embedding_gather(int n, const int32_t *ids, const void *table, int vocab,
+                                       int dim, void *out, int32_t *dev_status,
+                                       dflash_stream_t stream);
 
 /* ---------------------------------------------------------------------
  * dflash_step_bookkeeping -- one launch for the per-step bookkeeping groups
@@ -360,10 +447,13 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  *      values c_j; out bf16 [B, Tq, hq, latent].
  * kv_len      device int32 [B] (seq_lens of the bookkeeping).
  * sinks       device fp32 [hq] or NULL.
+ * scale       softmax scale; scale <= 0 selects the default, 1/sqrt(head_dim)
+ *             for GQA and 1/sqrt(128 + rope_dim) for MLA (the scale of the
+ *             unabsorbed head: a 128-wide no-rope part plus the rope part).
  * num_segments 0 = automatic, else >= 1.
  * workspace   device scratch >= dflash_attention_workspace_bytes(...), 16-byte
  *             aligned; clobbered.
- * Errors: DFLASH_ERR_INVALID_ARG (also: scale not finite and > 0, window < 0,
+ * Errors: DFLASH_ERR_INVALID_ARG (also: scale not finite, window < 0,
  * unknown mask_mode, a pointer not 16-byte aligned), DFLASH_ERR_UNSUPPORTED_GEOM
  * (hq not a multiple of nkv, GQA head_dim not 64 or 128, MLA dims not 512 + 64,
  * page_size not a multiple of 8 that divides 128 or is a multiple of 128, pool
@@ -380,9 +470,8 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
  * dflash_block_attention_noalloc -- the same computation as
  * dflash_block_attention, for callers that cannot allocate device memory
  * where they run it: a plugin whose host framework owns every device buffer
- * and gives it no allocator, code running while a stream is captured into a
- * CUDA graph (no cudaMalloc there), or a real-time loop that must not block in
- * an allocator.  The caller passes inputs and output as for
+ * and gives it no allocator, or a real-time loop that must not block in an
+ * allocator.  The caller passes inputs and output as for
  * dflash_block_attention; the split-KV scratch comes from one fixed array
  * inside the library.  The pages describe no such entry point: it is a
  * convenience of this library, with no counterpart in the method.
@@ -398,9 +487,11 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
  * Set-up: the first call on each device looks up the array's device address
  * (with that device current) and caches it; make that first call before any
  * stream capture.  The call allocates nothing and calls no allocating routine.
- * Errors: as dflash_block_attention, plus DFLASH_ERR_WORKSPACE_TOO_SMALL for
- * a problem larger than the fixed scratch and DFLASH_ERR_CUDA when the
- * address look-up fails.
+ * Errors: the argument checks of dflash_block_attention come first and give
+ * the same codes; then DFLASH_ERR_WORKSPACE_TOO_SMALL for a problem larger
+ * than the fixed scratch, and DFLASH_ERR_CUDA when the address look-up fails.
+ * The scratch address is that of the current device, which must be the
+ * device of `stream`.
  * ------------------------------------------------------------------- */
 DFLASH_API int dflash_block_attention_noalloc(const dflash_geom *g, int B, int layer, int Tq,
                                               const void *q, const void *q_rope,

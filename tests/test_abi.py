@@ -27,7 +27,8 @@ def test_header_declares_the_entry_points():
               "dflash_block_attention", "dflash_ctx_workspace_bytes",
               "dflash_attention_workspace_bytes", "dflash_attention_num_segments",
               "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes",
-              "dflash_q_norm_rope"):
+              "dflash_q_norm_rope", "dflash_pack_weights", "dflash_packed_kv_bytes",
+              "dflash_packed_gamma_bytes", "dflash_strict_accept", "dflash_embedding_gather"):
         assert n in names
 
 
@@ -47,6 +48,7 @@ def test_struct_sizes_match_header(lib):
     assert ctypes.sizeof(_lib.Geom) == 14 * 4 + 3 * 8
     assert ctypes.sizeof(_lib.Weights) == 4 * 8
     assert ctypes.sizeof(_lib.StepOutputs) == 15 * 8
+    assert ctypes.sizeof(_lib.LayerWeights) == 3 * 8
 
 
 def _geom():
@@ -152,3 +154,76 @@ def test_workspace_queries(lib):
     assert lib.dflash_attention_workspace_bytes(ctypes.byref(g), 1, 4, 3) >= 3 * 4 * 4 * (64 + 2) * 4
     assert lib.dflash_attention_workspace_bytes(None, 1, 4, 3) == 0
     assert lib.dflash_status_string(3) == b"workspace too small"
+
+
+def test_attention_scale_default_and_argument_order(lib):
+    """scale <= 0 selects the library's default (accepted: the call reaches the
+    workspace check); a non-finite scale is an argument error.  The
+    allocation-free call checks its arguments first, then its size limit, then
+    the buffer pointers (so NULL buffers on an oversized problem report the
+    size, and a bad mode reports the mode)."""
+    from context_kv_update_gb300 import _lib
+    g = _geom()
+    G = ctypes.byref(g)
+    p = ctypes.c_void_p(0x1000)
+    for scale in (0.0, -1.0):
+        assert lib.dflash_block_attention(G, 1, 0, 4, p, None, p, p, p, 0, None, scale, 0, 1, p, 16,
+                                          p, None, None) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    for scale in (float("nan"), float("inf")):
+        assert lib.dflash_block_attention(G, 1, 0, 4, p, None, p, p, p, 0, None, scale, 0, 1, p,
+                                          1 << 30, p, None, None) == _lib.DFLASH_ERR_INVALID_ARG
+    big_B, S = 4096, 64
+    assert lib.dflash_block_attention_noalloc(G, big_B, 0, 4, None, None, None, None, None, 0, None,
+                                              0.0, 0, S, None, None,
+                                              None) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    assert lib.dflash_block_attention_noalloc(G, big_B, 0, 4, None, None, None, None, None, 0, None,
+                                              0.0, 5, S, None, None,
+                                              None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_block_attention_noalloc(G, big_B, 9, 4, None, None, None, None, None, 0, None,
+                                              0.0, 0, S, None, None,
+                                              None) == _lib.DFLASH_ERR_INVALID_ARG
+    # a small problem with NULL buffers stops at the pointer check
+    assert lib.dflash_block_attention_noalloc(G, 1, 0, 4, None, None, None, None, None, 0, None,
+                                              0.0, 0, 1, None, None,
+                                              None) == _lib.DFLASH_ERR_INVALID_ARG
+    # B == 0 with a bad argument is still an error
+    assert lib.dflash_block_attention_noalloc(G, 0, 0, 4, None, None, None, None, None, -1, None,
+                                              0.0, 0, 0, None, None,
+                                              None) == _lib.DFLASH_ERR_INVALID_ARG
+
+
+def test_pack_accept_gather_validation(lib):
+    from context_kv_update_gb300 import _lib
+    g = _geom()
+    G = ctypes.byref(g)
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1008)
+    L, nkv, hd, D = g.num_layers, g.nkv, g.head_dim, g.d_model
+    assert lib.dflash_packed_kv_bytes(G) == L * 2 * nkv * hd * D * 2
+    assert lib.dflash_packed_gamma_bytes(G) == L * hd * 2
+    assert lib.dflash_packed_kv_bytes(None) == 0
+    ok = (_lib.LayerWeights * L)(*[_lib.LayerWeights(0x1000, 0x2000, 0x3000)] * L)
+    no_v = (_lib.LayerWeights * L)(*[_lib.LayerWeights(0x1000, None, 0x3000)] * L)
+    bad_al = (_lib.LayerWeights * L)(*[_lib.LayerWeights(0x1008, 0x2000, 0x3000)] * L)
+    assert lib.dflash_pack_weights(G, no_v, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_pack_weights(G, bad_al, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_pack_weights(G, ok, odd, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_pack_weights(G, None, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    g65 = _geom()
+    g65.num_layers = 65
+    assert lib.dflash_pack_weights(ctypes.byref(g65), ok, p, p,
+                                   None) == _lib.DFLASH_ERR_UNSUPPORTED_GEOM
+    # strict acceptance: negative sizes, short strides, missing outputs; B == 0
+    assert lib.dflash_strict_accept(-1, 3, p, 3, p, 4, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_strict_accept(2, 3, p, 2, p, 4, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_strict_accept(2, 3, p, 3, p, 3, p, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_strict_accept(2, 3, p, 3, p, 4, None, p, None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_strict_accept(0, 3, None, 3, None, 4, None, None, None) == _lib.DFLASH_OK
+    # embedding lookup: dim not a multiple of 8, misaligned table, n == 0
+    assert lib.dflash_embedding_gather(4, p, p, 100, 12, p, None,
+                                       None) == _lib.DFLASH_ERR_UNSUPPORTED_GEOM
+    assert lib.dflash_embedding_gather(4, p, odd, 100, 16, p, None,
+                                       None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_embedding_gather(4, p, p, 0, 16, p, None,
+                                       None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_embedding_gather(0, None, None, 100, 16, None, None, None) == _lib.DFLASH_OK

@@ -1,16 +1,18 @@
 """dflash_block_attention_noalloc: the block attention for callers that cannot
 allocate device memory where they run it (a plugin whose framework owns all
-device buffers, code inside a CUDA-graph capture, an allocation-free real-time
-loop).  Its scratch is a fixed array inside the library, so the test calls it
-through the C ABI with no workspace and checks its output against
-dflash_block_attention's (which takes a caller workspace) within the parity
-tolerance, on two calls in a row with different problems.
+device buffers and hands it no allocator, an allocation-free real-time loop).
+Its scratch is a fixed array inside the library, so the test calls it through
+the C ABI with no workspace and checks its output against
+dflash_block_attention's (which takes a caller workspace) and against the CPU
+oracle, within the parity tolerance, on two calls in a row with different
+problems (the second call finds the first one's partials in the shared array).
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process."""
 import numpy as np
 import pytest
 
+import oracle
 from context_kv_update_gb300 import inputs
 from tests.gpu_helpers import assert_close, bf16_f64, bits, to_dev
 
@@ -57,12 +59,16 @@ def _both(dl, prob, g, window, sinks):
     return bf16_f64(bits(ref)), bf16_f64(bits(out))
 
 
-def test_noalloc_matches_workspace_entry_point_twice(dl):
+def test_noalloc_matches_workspace_entry_point_and_oracle_twice(dl):
     # first call: 4K context, 16 queries, sinks; second: 9K context, 3 queries, window
     for seed, ctx, Tq, window, use_sinks in ((1, 4096, 16, 0, True), (2, 9000, 3, 700, False)):
         prob, g, window, sinks = _case(seed, ctx, Tq, window, use_sinks)
         ref, out = _both(dl, prob, g, window, sinks)
-        assert_close(out, ref, f"noalloc ctx={ctx} Tq={Tq}")
+        assert_close(out, ref, f"noalloc vs workspace entry point ctx={ctx} Tq={Tq}")
+        kv_len = np.array([int(prob["ctx_len"][0]) + g["T"]], np.int32)
+        want = oracle.attention_gqa(g, 1, prob["q"][1], prob["pool"], prob["pages"], kv_len,
+                                    window=window, sinks=sinks)
+        assert_close(out, want, f"noalloc vs oracle ctx={ctx} Tq={Tq}")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(dl):
@@ -76,7 +82,13 @@ def test_noalloc_rejects_problems_beyond_its_scratch(dl):
     # many requests and segments: the split-KV scratch would exceed the fixed array
     B, Tq, S = 64, 16, 64
     assert dl.dflash_attention_workspace_bytes(geom, B, Tq, S) > cap
-    p = ctypes.c_void_p(0x1000)
-    rc = _lib.load().dflash_block_attention_noalloc(ctypes.byref(geom), B, 0, Tq, p, None, p, p, p,
-                                                    0, None, 0.1, 0, S, p, None, None)
+    # every buffer is NULL: the size limit is checked before the pointers, so a
+    # library that lost the limit stops at the NULL check and launches nothing
+    lib = _lib.load()
+    rc = lib.dflash_block_attention_noalloc(ctypes.byref(geom), B, 0, Tq, None, None, None, None,
+                                            None, 0, None, 0.0, 0, S, None, None, None)
     assert rc == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    # argument errors come first, as for dflash_block_attention
+    rc = lib.dflash_block_attention_noalloc(ctypes.byref(geom), B, 0, Tq, None, None, None, None,
+                                            None, 0, None, 0.0, 9, S, None, None, None)
+    assert rc == _lib.DFLASH_ERR_INVALID_ARG
