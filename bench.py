@@ -471,11 +471,14 @@ def attention_steady_state(dl, step, stream, rounds=5):
         torch.cuda.synchronize()
         ms = s.elapsed_time(e) / n
         best = ms if best is None else min(best, ms)
-    # floor of an event pair around one tiny kernel
+    # floor of an event pair around one tiny kernel; a sleep kernel ahead of
+    # them keeps the GPU busy while the host enqueues the pair, so the figure
+    # holds no host launch latency
     x = torch.zeros(1, device="cuda")
     floors = []
     with torch.cuda.stream(stream):
         for _ in range(25):
+            torch.cuda._sleep(200000)
             s.record(stream)
             x.add_(1.0)
             e.record(stream)

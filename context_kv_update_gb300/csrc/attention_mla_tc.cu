@@ -14,8 +14,12 @@
 //                                                      B = Q from smem, K-major)
 //   O^T[512 dims x 64 rows] += V^T[512 x 128] . P^T   (A = the same latent rows
 //                                                      read MN-major; B = P^T)
-// in four 128-dim blocks.  TMEM: two 64-column S^T buffers + 4 x 64 O^T
-// columns.  Shared memory: Q (9 chunks of 64 rows x 64 dims, 72 KB) and one
+// in four 128-dim blocks.  The MMAs of a tile are issued by two threads (one
+// thread issues a tcgen05.mma only every ~70 cycles, about twice what an
+// N = 64 MMA takes to execute): each runs QK over part of the chunks into its
+// own S^T partial, which the softmax adds, and two of the four PV blocks.
+// TMEM: two S^T buffers of 2 x 64 columns + 4 x 64 O^T columns.  Shared
+// memory: Q (9 chunks of 64 rows x 64 dims, 72 KB) and one
 // 128-key tile as 9 chunks of 64 dims (8 latent + 1 rope, 144 KB); the rope
 // chunk's slot then holds P^T (it is free once QK has read it).
 //
@@ -30,10 +34,10 @@
 // A tile is loaded chunk by chunk: chunks 2b, 2b+1 of tile t+1 are issued as
 // soon as PV block b of tile t has released their slots (the rope chunk once
 // the whole PV is done), and QK of tile t+1 starts on chunk 0 while the
-// others are still landing.  The 18 TMA boxes of a tile (9 chunks x 2 pages
-// of 64 keys) are issued by 18 different lanes: copies issued by one thread
-// complete one after another, so a single issuing thread would cap the load
-// rate of the CTA far below what L2 delivers.  Every mbarrier wait is a
+// others are still landing.  The boxes of a slot group (2 chunks x 2 pages
+// of 64 keys) are issued by different lanes at once: a TMA issue does not
+// return before the copy engine takes it, so boxes issued one after another
+// (by one lane, or one lane per loop step) refill a tile ~2x slower.  Every mbarrier wait is a
 // bounded try_wait; a timeout raises DFLASH_DEV_WAIT_TIMEOUT.
 #include <cuda.h>
 
@@ -60,13 +64,13 @@ constexpr uint32_t kChunkBytes = kKT * 128;      // 128 keys x 64 dims
 constexpr uint32_t kQChunkBytes = kRowsN * 128;  // 64 rows x 64 dims
 constexpr uint32_t kSlotOff = kChunks * kQChunkBytes;
 constexpr uint32_t kBarOff = kSlotOff + kChunks * kChunkBytes;
-constexpr int kNumBars = 19;
+constexpr int kNumBars = 20;
 constexpr uint32_t kXOff = (kBarOff + kNumBars * 8 + 8 + 15) & ~15u;
 constexpr uint32_t kXBytes = (2 * 64 + 64 * 4 + 64 * 4) * 4 + 64 * 8;  // m_ref[2][64], xm, xl, roff
 constexpr uint32_t kSmemBytes = 1024 + kXOff + kXBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory plan");
-constexpr uint32_t kColS = 0;    // two 64-column S^T buffers
-constexpr uint32_t kColO = 128;  // O^T: 4 blocks x 64 columns
+constexpr uint32_t kColS = 0;    // two S^T buffers of 2 x 64 columns (one partial per issuer)
+constexpr uint32_t kColO = 256;  // O^T: 4 blocks x 64 columns
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -117,9 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *blk_empty = bars + 9;     // [4]  PV block b done with slots 2b, 2b+1
   uint64_t *s_full = bars + 13;       // [2]  S^T buffer written
   uint64_t *p_full = bars + 15;       //      P^T written (4 softmax warps)
-  uint64_t *o_done = bars + 16;       //      PV of the tile complete
+  uint64_t *o_done = bars + 16;       //      PV of the tile complete (2 issuers)
   uint64_t *q_full = bars + 17;       //      Q in shared memory (2 warps)
-  uint64_t *drain = bars + 18;
+  uint64_t *drain = bars + 18;        // [2]  per-issuer wind-down
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   float *m_ref = reinterpret_cast<float *>(sm + kXOff);  // [2][64], log2 units
@@ -135,12 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) ptx::mbar_init(ptx::smem_u32(&ch_full[c]), 1);
     for (int b = 0; b < 4; ++b) ptx::mbar_init(ptx::smem_u32(&blk_empty[b]), 1);
-    ptx::mbar_init(ptx::smem_u32(&s_full[0]), 1);
-    ptx::mbar_init(ptx::smem_u32(&s_full[1]), 1);
+    ptx::mbar_init(ptx::smem_u32(&s_full[0]), 2);
+    ptx::mbar_init(ptx::smem_u32(&s_full[1]), 2);
     ptx::mbar_init(ptx::smem_u32(p_full), 4);
-    ptx::mbar_init(ptx::smem_u32(o_done), 1);
+    ptx::mbar_init(ptx::smem_u32(o_done), 2);
     ptx::mbar_init(ptx::smem_u32(q_full), 2);
-    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&drain[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&drain[1]), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
@@ -232,11 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = c_lo; c < c_hi; ++c)
             ptx::mbar_arrive_expect_tx(ptx::smem_u32(&ch_full[c]), kChunkBytes);
         __syncwarp();
-        // box j = c * boxes + b of the tile is issued by lane j % 32
-        for (int j = c_lo * boxes; j < c_hi * boxes; ++j) {
+        // the group's boxes (chunk x page box) are issued by different lanes
+        // at once: a lane's TMA issue does not return before the copy engine
+        // takes it, so boxes issued one after another by one lane serialise
+        const int nb = (c_hi - c_lo) * boxes;
+        for (int j0 = 0; j0 < nb; j0 += 32) {
+          const int jj = j0 + lane;
+          const int j = c_lo * boxes + (jj < nb ? jj : 0);
           const int c = j / boxes, b = j % boxes;
           const int page = __shfl_sync(0xffffffffu, cur, tb * boxes + b);
-          if (lane == (j & 31)) {
+          if (jj < nb) {
             const int key0 = kbase + b * P.box_rows;
             const long long row0 =
                 (static_cast<long long>(p.layer) * p.NP + page) * p.P + key0 % p.P;
@@ -255,48 +265,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait(ptx::smem_u32(&ch_full[c]), static_cast<uint32_t>(last_fill[c] & 1), &dummy);
       }
     }
-  } else if (ntiles > 0 && warp == 3) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer (warp 3)
-      const uint32_t qb = ptx::smem_u32(sQ), sb = ptx::smem_u32(sSlot), pb = ptx::smem_u32(sPT);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag);
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const uint32_t ph = static_cast<uint32_t>(t & 1);
-        // S^T_t = K_t Q^T over the 9 dim chunks, each as soon as it lands
-        for (int c = 0; c < kChunks && ok; ++c) {
-          ok = ptx::mbar_wait(ptx::smem_u32(&ch_full[c]), ph, abort_flag);
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::mma_bf16(tm_s + (t & 1) * kRowsN,
-                          ptx::desc_kmajor_sw128(sb + c * kChunkBytes, j),
-                          ptx::desc_kmajor_sw128(qb + c * kQChunkBytes, j), P.idesc_qk,
-                          (c > 0 || j > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
-        // O^T += V^T P^T, one 128-dim block (slots 2b, 2b+1) at a time
-        ok = ptx::mbar_wait(ptx::smem_u32(p_full), ph, abort_flag);
+  }
+  if (ntiles > 0 && lane == 0 && (warp == 3 || warp == 0)) {
+    // ------------------------------------------------ MMA issuers
+    // One thread issues a tcgen05.mma only every ~70 cycles, and these N = 64
+    // MMAs execute in about half that, so the work of a tile is split over
+    // two issuing threads (warp 3 and warp 0, after its Q rows): issuer 0
+    // runs QK over latent chunks 0-4 into one S^T partial and PV blocks 0-1;
+    // issuer 1 QK over chunks 5-8 (rope) into a second partial and PV blocks
+    // 2-3.  The softmax adds the two partials.  Descriptors are formed once
+    // and advanced by adding the byte offset (>> 4) to the address field.
+    const int role = warp == 3 ? 0 : 1;
+    const int c_lo = role == 0 ? 0 : 5, c_hi = role == 0 ? 5 : kChunks;
+    const int b_lo = 2 * role;
+    const uint64_t dq0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sQ), 0);
+    const uint64_t dk0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sSlot), 0);
+    const uint64_t dv0 = ptx::smem_desc(ptx::smem_u32(sSlot), kChunkBytes, 1024, ptx::kSwizzle128B);
+    const uint64_t dp0 = ptx::smem_desc(ptx::smem_u32(sPT), kChunkBytes, 1024, ptx::kSwizzle128B);
+    bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag);
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const uint32_t ph = static_cast<uint32_t>(t & 1);
+      const uint32_t d_s = tm_s + (t & 1) * (2 * kRowsN) + role * kRowsN;
+      // S^T partial = K_t Q^T over this issuer's chunks, each as it lands
+      for (int c = c_lo; c < c_hi && ok; ++c) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&ch_full[c]), ph, abort_flag);
         if (!ok) break;
         ptx::tc_fence_after();
-        for (int b = 0; b < 4; ++b) {
 #pragma unroll
-          for (int ks = 0; ks < kKT / 16; ++ks)
-            ptx::mma_bf16(tm_o + b * kRowsN,
-                          ptx::smem_desc(sb + 2 * b * kChunkBytes + ks * 2048, kChunkBytes, 1024,
-                                         ptx::kSwizzle128B),
-                          ptx::smem_desc(pb + ks * 2048, kChunkBytes, 1024, ptx::kSwizzle128B),
-                          P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&blk_empty[b]));
-        }
-        ptx::mma_commit(ptx::smem_u32(o_done));
+        for (int j = 0; j < 4; ++j)
+          ptx::mma_bf16(d_s, dk0 + ((c * kChunkBytes + j * 32) >> 4),
+                        dq0 + ((c * kQChunkBytes + j * 32) >> 4), P.idesc_qk,
+                        (c > c_lo || j > 0) ? 1u : 0u);
       }
-      if (!ok) {
-        ptx::mma_commit(ptx::smem_u32(drain));
-        volatile int dummy = 0;
-        ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      if (!ok) break;
+      ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
+      // O^T += V^T P^T for this issuer's two 128-dim blocks
+      ok = ptx::mbar_wait(ptx::smem_u32(p_full), ph, abort_flag);
+      if (!ok) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb) {
+        const int b = b_lo + bb;
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks)
+          ptx::mma_bf16(tm_o + b * kRowsN, dv0 + ((2 * b * kChunkBytes + ks * 2048) >> 4),
+                        dp0 + ((ks * 2048) >> 4), P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&blk_empty[b]));
       }
+      ptx::mma_commit(ptx::smem_u32(o_done));
+    }
+    if (!ok) {
+      ptx::mma_commit(ptx::smem_u32(&drain[role]));
+      volatile int dummy = 0;
+      ptx::mbar_wait(ptx::smem_u32(&drain[role]), 0u, &dummy);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax (warps 4-7)
@@ -327,7 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[kRowsN];
       if (got) {
         ptx::tc_fence_after();
-        ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kRowsN, sv);
+        const uint32_t sa = tm_s + lane_off + (t & 1) * (2 * kRowsN);
+        ptx::tmem_ld64f_sync(sa, sv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float s2[32];
+          ptx::tmem_ld32f_sync(sa + kRowsN + 32 * h, s2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 * h + c] += s2[c];
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < kRowsN; ++c) sv[c] = -INFINITY;
