@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
   uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
   uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1, *q_full = drain + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(q_full + 1);
+  uint64_t *s_free = q_full + 1, *drain_pv = s_free + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain_pv + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *consumed = reinterpret_cast<volatile int *>(tslot + 2);
 
@@ -107,10 +108,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // one arrival per softmax warp at work: all four in the split layout,
     // else those owning at least one real row
     const int real_rows = min(kRows, P.GT - static_cast<int>(blockIdx.x % P.RT) * kRows);
-    ptx::mbar_init(ptx::smem_u32(p_full),
-                   P.split ? 4u : static_cast<uint32_t>((real_rows + 31) / 32));
+    const uint32_t sm_warps = P.split ? 4u : static_cast<uint32_t>((real_rows + 31) / 32);
+    ptx::mbar_init(ptx::smem_u32(p_full), sm_warps);
+    ptx::mbar_init(ptx::smem_u32(&s_free[0]), sm_warps);
+    ptx::mbar_init(ptx::smem_u32(&s_free[1]), sm_warps);
     ptx::mbar_init(ptx::smem_u32(o_done), 1);
     ptx::mbar_init(ptx::smem_u32(drain), 1);
+    ptx::mbar_init(ptx::smem_u32(drain_pv), 1);
     ptx::mbar_init(ptx::smem_u32(q_full), 4u);  // one arrival per softmax warp
     *abort_flag = 0;
     *consumed = 0;
@@ -294,63 +298,62 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
   } else if (ntiles > 0 && warp == 3) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer (warp 3)
-      // Per tile t: S_{t+1} = Q K_{t+1}^T (its S buffer was released when
-      // PV_{t-1} was issued), then O += P_t V_t once the softmax has written
-      // P_t.
-      auto issue_qk = [&](int t) {
-        *consumed = t + 1;
-        const uint32_t kb = ptx::smem_u32(sKV + (t % nst) * P.stage_bytes);
-        for (int ks = 0; ks < P.chunks * 4; ++ks) {
-          const int c = ks >> 2, j = ks & 3;
-          ptx::mma_bf16_ts(tm_s + (t & 1) * kKT, tm_q + ks * 8,
-                           ptx::desc_kmajor_sw128(kb + c * kVChunk, j), P.idesc_qk,
-                           ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
-      };
-      bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag) &&
-                ptx::mbar_wait(ptx::smem_u32(&kv_full[0]), 0u, abort_flag);
-      ptx::tc_fence_after();
-      if (ok) issue_qk(0);
-      // QK of tile t+1 goes ahead of PV of tile t only when t+1 has already
-      // landed; otherwise PV(t) goes first, so tile t's ring stage is released
-      // without waiting for the next tile's copies.
-      int next_qk = 1;
+      // ------------------------------------------------ QK issuer (warp 3)
+      // S_t = Q K_t^T into S buffer t & 1 once tile t has landed and the
+      // softmax has read S_{t-2} from that buffer.  A thread issues a
+      // tcgen05.mma only every ~70 cycles, so QK and PV have an issuing
+      // thread each: PV of tile t never waits behind QK of tile t+1.
+      const uint64_t dk0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sKV), 0);
+      bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag);
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int tn = t + 1;
-        if (tn < ntiles &&
-            ptx::mbar_test(ptx::smem_u32(&kv_full[tn % nst]), static_cast<uint32_t>((tn / nst) & 1))) {
-          ptx::tc_fence_after();
-          issue_qk(tn);
-          next_qk = tn + 1;
-        }
-        ok = ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag);
+        const int st = t % nst;
+        ok = ptx::mbar_wait(ptx::smem_u32(&kv_full[st]), static_cast<uint32_t>((t / nst) & 1),
+                            abort_flag);
+        if (ok && t >= 2)
+          ok = ptx::mbar_wait(ptx::smem_u32(&s_free[t & 1]),
+                              static_cast<uint32_t>(((t >> 1) & 1) ^ 1), abort_flag);
         if (!ok) break;
         ptx::tc_fence_after();
-        const int st = t % nst;
-        const uint32_t vb = ptx::smem_u32(sKV + st * P.stage_bytes + P.k_bytes);
-#pragma unroll
-        for (int ks = 0; ks < kKT / 16; ++ks) {
-          ptx::mma_bf16_ts(tm_o, tm_p + ks * 8,
-                           ptx::smem_desc(vb + ks * 2048, P.v_lbo, P.v_sbo, ptx::kSwizzle128B),
-                           P.idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+        *consumed = t + 1;
+        const uint64_t kb = dk0 + ((st * P.stage_bytes) >> 4);
+        for (int ks = 0; ks < P.chunks * 4; ++ks) {
+          const int c = ks >> 2, j = ks & 3;
+          ptx::mma_bf16_ts(tm_s + (t & 1) * kKT, tm_q + ks * 8, kb + ((c * kVChunk + j * 32) >> 4),
+                           P.idesc_qk, ks > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(o_done));
-        ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
-        if (tn < ntiles && next_qk == tn) {
-          ok = ptx::mbar_wait(ptx::smem_u32(&kv_full[tn % nst]),
-                              static_cast<uint32_t>((tn / nst) & 1), abort_flag);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_qk(tn);
-          next_qk = tn + 1;
-        }
+        ptx::mma_commit(ptx::smem_u32(&s_full[t & 1]));
       }
       if (!ok) {
         ptx::mma_commit(ptx::smem_u32(drain));
         volatile int dummy = 0;
         ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      }
+    }
+  } else if (ntiles > 0 && warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ PV issuer (warp 0)
+      // O += P_t V_t once the softmax has written P_t; its completion frees
+      // the ring stage (QK of the tile completed before its softmax began).
+      const uint64_t dv0 = ptx::smem_desc(ptx::smem_u32(sKV) + P.k_bytes, P.v_lbo, P.v_sbo,
+                                          ptx::kSwizzle128B);
+      bool ok = true;
+      for (int t = 0; ok && t < ntiles; ++t) {
+        ok = ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(t & 1), abort_flag);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int st = t % nst;
+        const uint64_t vb = dv0 + ((st * P.stage_bytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks)
+          ptx::mma_bf16_ts(tm_o, tm_p + ks * 8, vb + ((ks * 2048) >> 4), P.idesc_pv,
+                           (t > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(o_done));
+        ptx::mma_commit(ptx::smem_u32(&kv_empty[st]));
+      }
+      if (!ok) {
+        ptx::mma_commit(ptx::smem_u32(drain_pv));
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(drain_pv), 0u, &dummy);
       }
     }
   } else if (warp >= 4 && P.split) {
@@ -384,6 +387,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (got) {
         ptx::tc_fence_after();
         ptx::tmem_ld64f_sync(tm_s + lane_off + (t & 1) * kKT + 64 * half, sv);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s_free[t & 1]));
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[c] = -INFINITY;
@@ -633,7 +639,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&s_free[t & 1]));
+        ptx::mbar_arrive(ptx::smem_u32(p_full));
+      }
     }
     // epilogue: (m, l, O) of this segment
     if (ntiles > 0 && ok && warp_active) {
@@ -688,11 +697,11 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.k_bytes = P.chunks * kVChunk;
   P.stage_bytes = 2 * P.k_bytes;
   const uint32_t x_bytes = 320 * 4;  // split-layout row maxima and row sums
-  const uint32_t bar_bytes = 8 * 8 * 2 + 7 * 8 + 16;
+  const uint32_t bar_bytes = 8 * 8 * 2 + 10 * 8 + 16;
   P.nst = std::max(2, std::min<int>(8, static_cast<int>((kSmemMax - 1024 - bar_bytes - x_bytes) /
                                                           P.stage_bytes)));
   P.bar_off = P.nst * P.stage_bytes;
-  P.x_off = (P.bar_off + (2 * P.nst + 7) * 8 + 16 + 15) & ~15u;
+  P.x_off = (P.bar_off + (2 * P.nst + 10) * 8 + 16 + 15) & ~15u;
   const uint32_t smem = 1024 + P.x_off + x_bytes;
   P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);
