@@ -15,7 +15,9 @@ numpy float64 matmul for the projection, a hand-worked bookkeeping case
 (tests/golden/bookkeeping_tiny.json) and bookkeeping invariants; the split
 update against the fused one; the query RMSNorm + RoPE against numpy RMSNorm
 and RoPE's position-difference and length invariants; strict acceptance by
-hand cases and brute force; the embedding lookup as a one-hot product.
+hand cases and brute force; the embedding lookup as a one-hot product; the
+prefill context store against the pinned decode update (one request as one
+all-accepted block), request independence and the RoPE position shift.
 """
 from __future__ import annotations
 
@@ -235,6 +237,38 @@ def ctx_kv_update_mla(g, hidden, n_acc, ctx_in, alloc_limit, tbl, valid, w_fc, g
         _p(ctx_out), _p(_c(alloc_limit, np.int32)), _p(tbl),
         _p(None if valid is None else _c(valid, np.uint8)), _p(_c(w_fc, np.uint16)),
         _p(_c(g_h, np.uint16)), _p(_c(w_dkv, np.uint16)), _p(_c(g_kv, np.uint16)), _p(pool))
+    assert rc == 0
+    return ctx_out
+
+
+# ------------------------------------------------ prefill context store
+
+
+def ctx_kv_prefill(g, hidden, cu_rows, ctx_in, alloc_limit, tbl, valid, w_fc, g_h, w_kv, g_k,
+                   pool):
+    """Prefill context store: hidden [N, D_in] (rows of all requests, request r
+    at cu_rows[r]..cu_rows[r+1]-1), written in place into ``pool`` at
+    positions ctx_in[r] + i; returns ctx_out."""
+    lib = _load()
+    is_f32 = hidden.dtype == np.float32
+    hid = _c(hidden, np.float32 if is_f32 else np.uint16)
+    cu = _c(cu_rows, np.int32)
+    B = cu.shape[0] - 1
+    assert pool.dtype == np.uint16 and pool.flags.c_contiguous
+    gqa = g["kind"] == "gqa"
+    tbl = _c(tbl, np.int32)
+    ctx_out = np.empty(B, np.int32)
+    rc = lib.oracle_ctx_kv_prefill(
+        ctypes.c_int(0 if gqa else 1), ctypes.c_int(B), ctypes.c_int(g["L"]),
+        ctypes.c_int(g["D_in"]), ctypes.c_int(g["D"]), ctypes.c_int(g["nkv"] if gqa else 1),
+        ctypes.c_int(g["hd"] if gqa else 0), ctypes.c_int(g.get("latent", 512)),
+        ctypes.c_int(g.get("rope_dim", 64)), ctypes.c_int(g["P"]), ctypes.c_int(tbl.shape[1]),
+        ctypes.c_int(g["num_pool_pages"]), ctypes.c_double(g["rope_theta"]),
+        ctypes.c_double(g["eps_h"]), ctypes.c_double(g["eps_k"]), _p(hid),
+        ctypes.c_int(int(is_f32)), _p(cu), _p(_c(ctx_in, np.int32)), _p(ctx_out),
+        _p(_c(alloc_limit, np.int32)), _p(tbl), _p(None if valid is None else _c(valid, np.uint8)),
+        _p(_c(w_fc, np.uint16)), _p(_c(g_h, np.uint16)), _p(_c(w_kv, np.uint16)),
+        _p(_c(g_k, np.uint16)), _p(pool))
     assert rc == 0
     return ctx_out
 

@@ -389,6 +389,95 @@ int oracle_ctx_kv_update_mla(int B, int T, int L, int D_in, int D, int lat, int 
   return 0;
 }
 
+/* ------------------------------------------- prefill context store */
+/* TensorRT-LLM PR #20550, Description (TLLM_DFLASH_FUSED_PROLOGUE): the
+ * single-latent _store_context_kv_paged scatter used by prefill.  Every
+ * prompt row of a request goes through the decode update's context
+ * projection (fc, hidden RMSNorm, per-layer K/V or latent projection, k or
+ * latent RMSNorm, RoPE at its position) and is stored into the paged pool; no
+ * acceptance mask applies.  Rows of request r are hidden rows
+ * cu_rows[r] .. cu_rows[r+1]-1 and sit at positions c_r + i (c_r = ctx_in[r]);
+ * a row is stored when the request is live (valid, c_r >= 0), c_r + i is
+ * below alloc_limit[r] and its page is mapped inside the pool.  ctx_out[r] =
+ * live ? min(c_r + n_r, alloc_limit[r]) : 0.  kind 0 = GQA (w_kv [L, 2, nkv,
+ * hd, D], g_k [L, hd], pool [L][NP][2][nkv][P][hd]); kind 1 = MLA (w_kv
+ * [L, lat + rope, D], g_k [L, lat], pool [L][NP][P][lat + rope]). */
+int oracle_ctx_kv_prefill(int kind, int B, int L, int D_in, int D, int nkv, int hd, int lat,
+                          int rope, int P, int M, int num_pool_pages, double theta, double eps_h,
+                          double eps_k, const void *hidden, int hidden_is_f32,
+                          const int32_t *cu_rows, const int32_t *ctx_in, int32_t *ctx_out,
+                          const int32_t *alloc_limit, const int32_t *tbl, const uint8_t *valid,
+                          const uint16_t *w_fc, const uint16_t *g_h, const uint16_t *w_kv,
+                          const uint16_t *g_k, uint16_t *pool) {
+  size_t esz = hidden_is_f32 ? 4 : 2;
+  int N = cu_rows[B];
+  int W = kind == 0 ? hd : lat + rope;
+  int GW = kind == 0 ? hd : lat;
+  for (int r = 0; r < B; ++r)
+    if (cu_rows[r + 1] < cu_rows[r]) return -1;
+#pragma omp parallel
+  {
+    double *x = malloc(sizeof(double) * D_in);
+    double *h = malloc(sizeof(double) * D);
+    double *g = malloc(sizeof(double) * D);
+    double *hn = malloc(sizeof(double) * D);
+    double *t = malloc(sizeof(double) * W);
+    double *nrm = malloc(sizeof(double) * GW);
+    double *rot = malloc(sizeof(double) * W);
+    double *gk = malloc(sizeof(double) * GW);
+#pragma omp for schedule(dynamic, 1)
+    for (int n = 0; n < N; ++n) {
+      int r = 0;
+      while (cu_rows[r + 1] <= n) ++r; /* the request holding hidden row n */
+      int i = n - cu_rows[r];
+      int c = ctx_in[r];
+      int live = (valid ? valid[r] != 0 : 1) && c >= 0;
+      int page, slot;
+      if (!ctx_row_dest(live, i, i + 1, c, alloc_limit[r], tbl + (int64_t)r * M, M, P,
+                        num_pool_pages, &page, &slot))
+        continue;
+      const char *row = (const char *)hidden + (size_t)n * D_in * esz;
+      fc_hidden_norm(row, hidden_is_f32, D_in, D, w_fc, g_h, eps_h, x, h, g, hn);
+      double pos = (double)(c + i);
+      for (int l = 0; l < L; ++l) {
+        for (int d = 0; d < GW; ++d) gk[d] = oracle_bf16_to_double(g_k[(size_t)l * GW + d]);
+        if (kind == 0) {
+          for (int kv = 0; kv < 2; ++kv)
+            for (int hh = 0; hh < nkv; ++hh) {
+              const uint16_t *Wm = w_kv + ((((size_t)l * 2 + kv) * nkv + hh) * hd) * (size_t)D;
+              oracle_matvec_bf16(Wm, hd, D, hn, t);
+              uint16_t *dst =
+                  pool + (((((size_t)l * num_pool_pages + page) * 2 + kv) * nkv + hh) * P + slot) *
+                             (size_t)hd;
+              if (kv == 0) {
+                oracle_rmsnorm(t, gk, hd, eps_k, nrm);
+                oracle_rope_neox(nrm, hd, pos, theta, rot);
+                for (int d = 0; d < hd; ++d) dst[d] = oracle_double_to_bf16(rot[d]);
+              } else {
+                for (int d = 0; d < hd; ++d) dst[d] = oracle_double_to_bf16(t[d]);
+              }
+            }
+        } else {
+          oracle_matvec_bf16(w_kv + (size_t)l * W * D, W, D, hn, t);
+          oracle_rmsnorm(t, gk, lat, eps_k, nrm);
+          oracle_rope_neox(t + lat, rope, pos, theta, rot);
+          uint16_t *dst = pool + (((size_t)l * num_pool_pages + page) * P + slot) * (size_t)W;
+          for (int d = 0; d < lat; ++d) dst[d] = oracle_double_to_bf16(nrm[d]);
+          for (int d = 0; d < rope; ++d) dst[lat + d] = oracle_double_to_bf16(rot[d]);
+        }
+      }
+    }
+    free(x); free(h); free(g); free(hn); free(t); free(nrm); free(rot); free(gk);
+  }
+  for (int r = 0; r < B; ++r) {
+    int c = ctx_in[r];
+    int live = (valid ? valid[r] != 0 : 1) && c >= 0;
+    long long s = (long long)c + (cu_rows[r + 1] - cu_rows[r]);
+    ctx_out[r] = live ? (int)(s < alloc_limit[r] ? s : alloc_limit[r]) : 0;
+  }
+  return 0;
+}
+
 /* ------------------------------------------- split context-KV update */
 /* TensorRT-LLM PR #20550, Description (TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION):
  * the context projection (fc, hidden norm, latent / K-V projection, norm and

@@ -9,6 +9,7 @@ import pytest
 import oracle
 import tests.test_oracle_accept_gather as accept_pins
 import tests.test_oracle_pins as pins
+import tests.test_oracle_prefill as prefill_pins
 import tests.test_oracle_q_rope as q_pins
 import tests.test_oracle_split_update as split_pins
 
@@ -52,6 +53,14 @@ MUTATIONS = [
      "blk_lat + (size_t)k * W, sizeof(uint16_t) * W);",
      "blk_lat + (size_t)i * W, sizeof(uint16_t) * W);",
      [pins.test_block_latent_scatter_places_rows]),
+    # prefill context store
+    ("prefill_position_off_by_one", "int i = n - cu_rows[r];", "int i = n - cu_rows[r] + 1;",
+     [lambda: prefill_pins.test_prefill_of_one_request_is_one_all_accepted_update_block("gqa")]),
+    ("prefill_request_lookup", "while (cu_rows[r + 1] <= n) ++r;", "while (cu_rows[r + 1] < n) ++r;",
+     [lambda: prefill_pins.test_prefill_requests_are_independent("mla")]),
+    ("prefill_advance", "long long s = (long long)c + (cu_rows[r + 1] - cu_rows[r]);",
+     "long long s = (long long)c + (cu_rows[r + 1] - cu_rows[r]) - 1;",
+     [lambda: prefill_pins.test_prefill_of_one_request_is_one_all_accepted_update_block("mla")]),
 ]
 
 
