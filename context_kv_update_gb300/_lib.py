@@ -43,7 +43,8 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_block_attention_noalloc_max_scratch_bytes", "dflash_ctx_staged_bytes",
            "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
            "dflash_packed_kv_bytes", "dflash_packed_gamma_bytes", "dflash_pack_weights",
-           "dflash_strict_accept", "dflash_embedding_gather")
+           "dflash_strict_accept", "dflash_embedding_gather", "dflash_ctx_prefill_workspace_bytes",
+           "dflash_ctx_kv_prefill")
 
 
 class DflashError(RuntimeError):
@@ -122,6 +123,10 @@ def load():
     lib.dflash_block_attention_noalloc.restype = ctypes.c_int
     lib.dflash_block_attention_noalloc_max_scratch_bytes.argtypes = []
     lib.dflash_block_attention_noalloc_max_scratch_bytes.restype = sz
+    lib.dflash_ctx_prefill_workspace_bytes.argtypes = [G, ctypes.c_int, ctypes.c_int]
+    lib.dflash_ctx_prefill_workspace_bytes.restype = sz
+    lib.dflash_ctx_kv_prefill.argtypes = [G, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp,
+                                          vp, vp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp, vp]
     lib.dflash_packed_kv_bytes.argtypes = [G]
     lib.dflash_packed_kv_bytes.restype = sz
     lib.dflash_packed_gamma_bytes.argtypes = [G]
@@ -136,7 +141,8 @@ def load():
     for name in ("dflash_step_bookkeeping", "dflash_ctx_kv_update", "dflash_block_kv_scatter",
                  "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version",
                  "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
-                 "dflash_pack_weights", "dflash_strict_accept", "dflash_embedding_gather"):
+                 "dflash_pack_weights", "dflash_strict_accept", "dflash_embedding_gather",
+                 "dflash_ctx_kv_prefill"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -346,3 +352,24 @@ def dflash_embedding_gather(ids, table, out, dev_status=None, stream=None):
     _check("dflash_embedding_gather", lib.dflash_embedding_gather(
         int(ids.numel()), _ptr(ids), _ptr(table), vocab, dim, _ptr(out), _ptr(dev_status),
         _stream(stream)))
+
+
+def dflash_ctx_prefill_workspace_bytes(geom, B, n_rows) -> int:
+    return int(load().dflash_ctx_prefill_workspace_bytes(ctypes.byref(geom), B, n_rows))
+
+
+def dflash_ctx_kv_prefill(geom, hidden, cu_rows, ctx_len, alloc_limit, block_table, valid,
+                          weights: dict, kv_pool, workspace, dev_status=None, stream=None):
+    """hidden [n_rows, d_in] CUDA tensor (bf16 or fp32), cu_rows int32 [B + 1]
+    (request r = rows cu_rows[r]..cu_rows[r+1]-1), ctx_len int32 [B] (in:
+    start positions, out: advanced)."""
+    import torch
+    lib = load()
+    w = _weights(weights)
+    dt = DTYPE_F32 if hidden.dtype == torch.float32 else DTYPE_BF16
+    B = int(ctx_len.shape[0])
+    _check("dflash_ctx_kv_prefill", lib.dflash_ctx_kv_prefill(
+        ctypes.byref(geom), B, int(hidden.shape[0]), _ptr(hidden), dt, _ptr(cu_rows),
+        _ptr(ctx_len), _ptr(alloc_limit), _ptr(block_table), _ptr(valid), ctypes.byref(w),
+        _ptr(kv_pool), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))

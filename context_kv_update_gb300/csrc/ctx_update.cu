@@ -38,9 +38,9 @@ struct CtxDims {
   int N, Npad, D_in, D, Wrows;
 };
 
-CtxDims ctx_dims(const dflash_geom &g, int B) {
+CtxDims ctx_dims_rows(const dflash_geom &g, int N) {
   CtxDims d;
-  d.N = B * g.block_size;
+  d.N = N;
   d.Npad = static_cast<int>(align_up(static_cast<size_t>(d.N > 0 ? d.N : 1), 16));
   d.D_in = g.d_in;
   d.D = g.d_model;
@@ -49,8 +49,11 @@ CtxDims ctx_dims(const dflash_geom &g, int B) {
   return d;
 }
 
-CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
-  const CtxDims d = ctx_dims(g, B);
+CtxDims ctx_dims(const dflash_geom &g, int B) { return ctx_dims_rows(g, B * g.block_size); }
+
+// B requests, N rows (the decode update's N = B * T)
+CtxWs ctx_ws_map_rows(const dflash_geom &g, int B, int N, void *base) {
+  const CtxDims d = ctx_dims_rows(g, N);
   char *p = static_cast<char *>(base);
   size_t off = 0;
   CtxWs w;
@@ -66,6 +69,10 @@ CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
   off = align_up(off + gemm_partial_bytes(d.Wrows, d.D, d.Npad), 256);
   w.bytes = off;
   return w;
+}
+
+CtxWs ctx_ws_map(const dflash_geom &g, int B, void *base) {
+  return ctx_ws_map_rows(g, B, B * g.block_size, base);
 }
 
 // ------------------------------------------------------------------ prep
@@ -158,19 +165,41 @@ struct MaskArgs {
   const int32_t *alloc_limit;
   const int32_t *tbl;
   const uint8_t *valid;
-  int T, M, P, NP;
+  const int32_t *cu_rows;  // prefill: request r owns rows cu_rows[r] .. cu_rows[r+1]-1
+  int T, M, P, NP, B;
   int32_t *st;
 };
+
+// Request and in-request index of GEMM row n: (n / T, n % T) for the decode
+// update, a binary search of cu_rows for the prefill store.  False when the
+// prefill row lies in no request's range (cu_rows inconsistent with the row
+// count; the row is skipped).
+__device__ __forceinline__ bool row_of(const MaskArgs &m, int n, int *r, int *i) {
+  if (!m.cu_rows) {
+    *r = n / m.T;
+    *i = n % m.T;
+    return true;
+  }
+  int lo = 0, hi = m.B - 1;  // the last request whose first row is <= n
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (m.cu_rows[mid] <= n) lo = mid; else hi = mid - 1;
+  }
+  const int a = m.cu_rows[lo], b = m.cu_rows[lo + 1];
+  *r = lo;
+  *i = n - a;
+  return n >= a && n < b;
+}
 
 // Destination of context row (r, i), or false when the row is not written.
 __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, int *page, int *slot,
                                              int *pos, bool report) {
   // the row's scalars are independent loads, issued together
-  const int n = m.n_acc[r];
+  const int n = m.cu_rows ? i + 1 : m.n_acc[r];  // prefill: every row of the request
   const int c = m.ctx_snap[r];
   const int A = m.alloc_limit[r];
   const bool live = m.valid ? (m.valid[r] != 0) : true;
-  if (!live || n < 1 || n > m.T || c < 0 || i >= n) return false;
+  if (!live || n < 1 || (!m.cu_rows && n > m.T) || c < 0 || i >= n) return false;
   const int p = c + i;
   if (p >= A) return false;
   const int lp = p / m.P;
@@ -190,7 +219,16 @@ __device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, in
 // Advance of ctx_len[r] from the pre-step length c (the snapshot).
 __device__ __forceinline__ void advance_ctx_len(const MaskArgs &m, int32_t *ctx_len, int B) {
   for (int r = threadIdx.x; r < B; r += blockDim.x) {
-    const int nn = m.n_acc[r], c = m.ctx_snap[r];
+    const int c = m.ctx_snap[r];
+    if (m.cu_rows) {  // prefill: all of the request's rows
+      const int nn = max(0, m.cu_rows[r + 1] - m.cu_rows[r]);
+      const bool live = (m.valid ? (m.valid[r] != 0) : true) && c >= 0;
+      const long long s = static_cast<long long>(c) + nn;
+      const int A = m.alloc_limit[r];
+      ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
+      continue;
+    }
+    const int nn = m.n_acc[r];
     const bool live = (m.valid ? (m.valid[r] != 0) : true) && nn >= 1 && nn <= m.T && c >= 0;
     const long long s = static_cast<long long>(c) + nn;
     const int A = m.alloc_limit[r];
@@ -224,7 +262,8 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   }
   // ctx_len advance; every reader of the pre-step value uses the snapshot
   if (!kStaged && n == 0 && head == 0) advance_ctx_len(m, ctx_len, B);
-  const int r = n / m.T, i = n % m.T;
+  int r, i;
+  if (!row_of(m, n, &r, &i)) return;
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
@@ -278,7 +317,8 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
     gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
   }
   if (!kStaged && n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
-  const int r = n / m.T, i = n % m.T;
+  int r, i;
+  if (!row_of(m, n, &r, &i)) return;
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
@@ -319,7 +359,8 @@ __global__ void commit_kernel(const uint4 *staged, const MaskArgs m, uint16_t *p
   griddep_wait();
   const int n = blockIdx.x, l = blockIdx.y;
   if (n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
-  const int r = n / m.T, i = n % m.T;
+  int r, i;
+  row_of(m, n, &r, &i);
   int page, slot, pos;
   if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && threadIdx.x == 0)) return;
   const bool gqa = kind == DFLASH_KIND_GQA;
@@ -355,9 +396,11 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
                              const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
                              const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
                              void *pool, void *ws, int32_t *st, int32_t *staged_c,
-                             uint16_t *staged, cudaStream_t s) {
-  const CtxDims d = ctx_dims(g, B);
-  const CtxWs W = ctx_ws_map(g, B, ws);
+                             uint16_t *staged, cudaStream_t s, int rows = -1,
+                             const int32_t *cu_rows = nullptr) {
+  const int N = rows >= 0 ? rows : B * g.block_size;
+  const CtxDims d = ctx_dims_rows(g, N);
+  const CtxWs W = ctx_ws_map_rows(g, B, N, ws);
   const bool split = staged != nullptr;
   int32_t *snap = split ? staged_c : W.ctx_snap;
   cudaError_t e;
@@ -427,10 +470,12 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   m.alloc_limit = alloc_limit;
   m.tbl = tbl;
   m.valid = valid;
+  m.cu_rows = cu_rows;
   m.T = g.block_size;
   m.M = g.max_pages;
   m.P = g.page_size;
   m.NP = g.num_pool_pages;
+  m.B = B;
   m.st = st;
   RopeFreqs rf;
   cudaLaunchConfig_t cfg = {};
@@ -474,6 +519,20 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
                           pool, ws, st, nullptr, nullptr, s);
 }
 
+size_t ctx_prefill_workspace_bytes(const dflash_geom &g, int B, int rows) {
+  return ctx_ws_map_rows(g, B, rows, nullptr).bytes;
+}
+
+cudaError_t launch_ctx_kv_prefill(const dflash_geom &g, int B, int rows, const void *hidden,
+                                  int hidden_dtype, const int32_t *cu_rows, int32_t *ctx_len,
+                                  const int32_t *alloc_limit, const int32_t *tbl,
+                                  const uint8_t *valid, const dflash_weights &w, void *pool,
+                                  void *ws, int32_t *st, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  return launch_ctx_chain(g, B, hidden, hidden_dtype, nullptr, ctx_len, alloc_limit, tbl, valid, w,
+                          pool, ws, st, nullptr, nullptr, s, rows, cu_rows);
+}
+
 size_t ctx_staged_bytes(const dflash_geom &g, int B) {
   const CtxDims d = ctx_dims(g, B);
   return staged_rows_offset(B) + sizeof(uint16_t) * static_cast<size_t>(d.N) * d.Wrows;
@@ -503,10 +562,12 @@ cudaError_t launch_ctx_kv_commit(const dflash_geom &g, int B, const void *staged
   m.alloc_limit = alloc_limit;
   m.tbl = tbl;
   m.valid = valid;
+  m.cu_rows = nullptr;
   m.T = g.block_size;
   m.M = g.max_pages;
   m.P = g.page_size;
   m.NP = g.num_pool_pages;
+  m.B = B;
   m.st = st;
   const bool gqa = g.kind == DFLASH_KIND_GQA;
   const int W = g.latent_dim + g.rope_dim;

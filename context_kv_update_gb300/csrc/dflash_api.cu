@@ -189,6 +189,35 @@ extern "C" int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
                                           dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" size_t dflash_ctx_prefill_workspace_bytes(const dflash_geom *g, int B, int n_rows) {
+  if (!geom_ok(g) || B < 0 || n_rows < 0 || n_rows > kMaxPrefillRows) return 0;
+  return ctx_prefill_workspace_bytes(*g, B, n_rows);
+}
+
+extern "C" int dflash_ctx_kv_prefill(const dflash_geom *g, int B, int n_rows, const void *hidden,
+                                     int hidden_dtype, const int32_t *cu_rows, int32_t *ctx_len,
+                                     const int32_t *alloc_limit, const int32_t *block_table,
+                                     const uint8_t *valid, const dflash_weights *w,
+                                     void *kv_pool, void *workspace, size_t ws_bytes,
+                                     int32_t *dev_status, dflash_stream_t stream) {
+  if (!geom_ok(g) || B < 0 || n_rows < 0 || !w) return DFLASH_ERR_INVALID_ARG;
+  if (n_rows > kMaxPrefillRows) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  if (hidden_dtype != DFLASH_DTYPE_BF16 && hidden_dtype != DFLASH_DTYPE_F32)
+    return DFLASH_ERR_INVALID_ARG;
+  if (const int gs = update_geom_status(g)) return gs;
+  if (B == 0) return DFLASH_OK;
+  if (!cu_rows || !ctx_len || !alloc_limit || !block_table || !kv_pool || !workspace ||
+      (n_rows > 0 && !hidden))
+    return DFLASH_ERR_INVALID_ARG;
+  if (!weights_ok(w) || (hidden && !aligned16(hidden)) || !aligned16(kv_pool) ||
+      !aligned256(workspace))
+    return DFLASH_ERR_INVALID_ARG;
+  if (ws_bytes < ctx_prefill_workspace_bytes(*g, B, n_rows)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_ctx_kv_prefill(*g, B, n_rows, hidden, hidden_dtype, cu_rows, ctx_len,
+                                           alloc_limit, block_table, valid, *w, kv_pool, workspace,
+                                           dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 extern "C" size_t dflash_ctx_staged_bytes(const dflash_geom *g, int B) {
   if (!geom_ok(g) || B < 0) return 0;
   return ctx_staged_bytes(*g, B);

@@ -15,6 +15,7 @@ constexpr int kMaxHeadDim = 256;
 constexpr int kAttnTileKeys = 128;  // keys per attention tile
 constexpr int kGemmTileM = 128;     // weight rows per GEMM tile
 constexpr int kGemmTileK = 64;      // reduction depth per pipeline stage (128 B of bf16)
+constexpr int kMaxPrefillRows = 65535;  // rows of one prefill store (the norm's grid height)
 
 // ------------------------------------------------------------ status
 __device__ __forceinline__ void raise_status(int32_t *st, unsigned bits) {
@@ -109,6 +110,13 @@ cudaError_t launch_ctx_kv_update(const dflash_geom &g, int B, const void *hidden
                                  const int32_t *n_acc, int32_t *ctx_len, const int32_t *alloc_limit,
                                  const int32_t *tbl, const uint8_t *valid, const dflash_weights &w,
                                  void *pool, void *ws, int32_t *st, cudaStream_t s);
+// prefill store: every row of each request (rows cu_rows[r]..cu_rows[r+1]-1)
+size_t ctx_prefill_workspace_bytes(const dflash_geom &g, int B, int rows);
+cudaError_t launch_ctx_kv_prefill(const dflash_geom &g, int B, int rows, const void *hidden,
+                                  int hidden_dtype, const int32_t *cu_rows, int32_t *ctx_len,
+                                  const int32_t *alloc_limit, const int32_t *tbl,
+                                  const uint8_t *valid, const dflash_weights &w, void *pool,
+                                  void *ws, int32_t *st, cudaStream_t s);
 // split update: projection into a staged buffer, then the masked store
 size_t ctx_staged_bytes(const dflash_geom &g, int B);
 cudaError_t launch_ctx_kv_project(const dflash_geom &g, int B, const void *hidden, int hidden_dtype,

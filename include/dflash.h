@@ -321,6 +321,41 @@ DFLASH_API int dflash_ctx_kv_update(const dflash_geom *g, int B, const void *hid
                          dflash_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * dflash_ctx_kv_prefill -- the prefill-side context store: every prompt row
+ * of every request through the context projection and into the paged pool
+ * [TRT-20550 Description, TLLM_DFLASH_FUSED_PROLOGUE: the single-latent
+ * _store_context_kv_paged scatter used by prefill].
+ *
+ * The rows of request r are hidden rows cu_rows[r] .. cu_rows[r+1]-1 (a
+ * variable number per request; cu_rows[0] = 0, nondecreasing, cu_rows[B] =
+ * n_rows).  Row i of request r sits at position p = c_r + i, c_r = ctx_len[r]
+ * (0 for a fresh prompt, the chunk start for a chunked prefill), and gets the
+ * values dflash_ctx_kv_update computes for an accepted row: x = bf16(hidden),
+ * h = bf16(W_fc x), hn = bf16(RMSNorm(h)), per layer GQA k' = RoPE(RMSNorm(W_k
+ * hn), p) and v = W_v hn, MLA bf16(RMSNorm(c[:lat])) || bf16(RoPE(c[lat:], p)).
+ * It is stored when the request is live (valid != 0 and c_r >= 0), p is below
+ * alloc_limit[r] and block_table[r, p / P] is a page inside the pool; nothing
+ * else in the pool changes.  Then, in place, ctx_len[r] = live ?
+ * min(c_r + n_r, alloc_limit[r]) : 0.  A row outside every request's range
+ * (cu_rows inconsistent with n_rows) is skipped.
+ *
+ * n_rows      host int, 0 .. 65535 rows per call (chunk longer prompts).
+ * hidden      device [n_rows, d_in], bf16 or fp32 per hidden_dtype.
+ * cu_rows     device int32 [B + 1].
+ * workspace   device scratch of dflash_ctx_prefill_workspace_bytes(g, B,
+ *             n_rows) bytes (grows with n_rows), 256-byte aligned.
+ * Other arguments as dflash_ctx_kv_update.  Errors: as dflash_ctx_kv_update,
+ * plus DFLASH_ERR_UNSUPPORTED_GEOM for n_rows > 65535.
+ * ------------------------------------------------------------------- */
+DFLASH_API size_t dflash_ctx_prefill_workspace_bytes(const dflash_geom *g, int B, int n_rows);
+DFLASH_API int dflash_ctx_kv_prefill(const dflash_geom *g, int B, int n_rows, const void *hidden,
+                                     int hidden_dtype, const int32_t *cu_rows, int32_t *ctx_len,
+                                     const int32_t *alloc_limit, const int32_t *block_table,
+                                     const uint8_t *valid, const dflash_weights *w, void *kv_pool,
+                                     void *workspace, size_t ws_bytes, int32_t *dev_status,
+                                     dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * Split context update: dflash_ctx_kv_project + dflash_ctx_kv_commit
  * [TRT-20550 Description, TLLM_DFLASH_OVERLAP_CONTEXT_PROJECTION: the
  * context projection of the generation tokens is forked onto an auxiliary

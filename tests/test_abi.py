@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
               "dflash_attention_workspace_bytes", "dflash_attention_num_segments",
               "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes",
               "dflash_q_norm_rope", "dflash_pack_weights", "dflash_packed_kv_bytes",
-              "dflash_packed_gamma_bytes", "dflash_strict_accept", "dflash_embedding_gather"):
+              "dflash_packed_gamma_bytes", "dflash_strict_accept", "dflash_embedding_gather",
+              "dflash_ctx_kv_prefill", "dflash_ctx_prefill_workspace_bytes"):
         assert n in names
 
 
@@ -227,3 +228,25 @@ def test_pack_accept_gather_validation(lib):
     assert lib.dflash_embedding_gather(4, p, p, 0, 16, p, None,
                                        None) == _lib.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_embedding_gather(0, None, None, 100, 16, None, None, None) == _lib.DFLASH_OK
+
+
+def test_prefill_validation(lib):
+    from context_kv_update_gb300 import _lib
+    g = _geom()
+    G = ctypes.byref(g)
+    p = ctypes.c_void_p(0x1000)
+    w = _lib.Weights(0x1000, 0x1000, 0x1000, 0x1000)
+    W = ctypes.byref(w)
+    assert lib.dflash_ctx_prefill_workspace_bytes(G, 2, 100) > lib.dflash_ctx_prefill_workspace_bytes(G, 2, 10)
+    assert lib.dflash_ctx_prefill_workspace_bytes(G, 2, 70000) == 0
+    # more rows than one call takes, bad dtype, missing cu_rows, short workspace
+    assert lib.dflash_ctx_kv_prefill(G, 1, 70000, p, 0, p, p, p, p, None, W, p, p, 1 << 40, None,
+                                     None) == _lib.DFLASH_ERR_UNSUPPORTED_GEOM
+    assert lib.dflash_ctx_kv_prefill(G, 1, 10, p, 7, p, p, p, p, None, W, p, p, 1 << 40, None,
+                                     None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_prefill(G, 1, 10, p, 0, None, p, p, p, None, W, p, p, 1 << 40, None,
+                                     None) == _lib.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_ctx_kv_prefill(G, 1, 10, p, 0, p, p, p, p, None, W, p, p, 64, None,
+                                     None) == _lib.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    assert lib.dflash_ctx_kv_prefill(G, 0, 0, None, 0, None, None, None, None, None, W, None, None,
+                                     0, None, None) == _lib.DFLASH_OK
