@@ -247,6 +247,7 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
                                     int L, int nkv, int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float kbuf[kMaxHeadDim];
+  __shared__ __align__(16) uint16_t obuf[kMaxHeadDim];  // the bf16 row, stored as 16-byte vectors
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
@@ -286,12 +287,14 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
     rope_cos_sin(pos, rf.f[j], &c, &s);
     v = d < half ? kn * c - kbuf[d + half] * s : kn * c + kbuf[d - half] * s;
   }
-  if (kStaged) {
-    staged[static_cast<size_t>(n) * L * 2 * nkv * hd + col] = f32_to_bf16_rn(v);
-  } else {
-    const size_t dst =
-        ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P + slot) * hd + d;
-    pool[dst] = f32_to_bf16_rn(v);
+  obuf[d] = f32_to_bf16_rn(v);
+  __syncthreads();
+  if (d < hd / 8) {  // head_dim % 8 == 0: the row leaves as 16-byte vectors
+    uint16_t *row =
+        kStaged ? staged + static_cast<size_t>(n) * L * 2 * nkv * hd + head * hd
+                : pool + ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P +
+                          slot) * hd;
+    reinterpret_cast<uint4 *>(row)[d] = reinterpret_cast<const uint4 *>(obuf)[d];
   }
 }
 
@@ -303,6 +306,7 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
                                     int L, int lat, int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
   __shared__ float rbuf[kMaxHeadDim];
+  __shared__ __align__(16) uint16_t obuf[1024];  // lat + rope <= 1024
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
@@ -342,10 +346,13 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
     rope_cos_sin(pos, rf.f[j], &c, &s);
     outv = e < half ? v * c - rbuf[e + half] * s : v * c + rbuf[e - half] * s;
   }
-  if (kStaged)
-    staged[static_cast<size_t>(n) * L * W + col] = f32_to_bf16_rn(outv);
-  else
-    pool[((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * W + d] = f32_to_bf16_rn(outv);
+  obuf[d] = f32_to_bf16_rn(outv);
+  __syncthreads();
+  if (d < W / 8) {  // (lat + rope) % 8 == 0: the row leaves as 16-byte vectors
+    uint16_t *row = kStaged ? staged + static_cast<size_t>(n) * L * W + static_cast<size_t>(l) * W
+                            : pool + ((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * W;
+    reinterpret_cast<uint4 *>(row)[d] = reinterpret_cast<const uint4 *>(obuf)[d];
+  }
 }
 
 // ------------------------------------------------------------ commit
