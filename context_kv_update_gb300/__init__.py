@@ -14,5 +14,5 @@ from ._lib import (DflashError, Geom, LayerWeights, StepOutputs, Weights,  # noq
                    dflash_ctx_kv_commit, dflash_ctx_kv_prefill, dflash_ctx_kv_project,
                    dflash_ctx_kv_update, dflash_ctx_prefill_workspace_bytes,
                    dflash_ctx_staged_bytes, dflash_ctx_workspace_bytes, dflash_q_norm_rope,
-                   dflash_step_bookkeeping, load, make_geom,
+                   dflash_step_bookkeeping, dflash_test_attention_skip_tile, load, make_geom,
                    KIND_GQA, KIND_MLA, MASK_CAUSAL_TAIL, MASK_BLOCK_BIDIR)

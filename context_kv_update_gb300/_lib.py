@@ -44,7 +44,7 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
            "dflash_packed_kv_bytes", "dflash_packed_gamma_bytes", "dflash_pack_weights",
            "dflash_strict_accept", "dflash_embedding_gather", "dflash_ctx_prefill_workspace_bytes",
-           "dflash_ctx_kv_prefill")
+           "dflash_ctx_kv_prefill", "dflash_test_attention_skip_tile")
 
 
 class DflashError(RuntimeError):
@@ -127,6 +127,8 @@ def load():
     lib.dflash_ctx_prefill_workspace_bytes.restype = sz
     lib.dflash_ctx_kv_prefill.argtypes = [G, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                           vp, vp, vp, ctypes.POINTER(Weights), vp, vp, sz, vp, vp]
+    lib.dflash_test_attention_skip_tile.argtypes = [ctypes.c_int]
+    lib.dflash_test_attention_skip_tile.restype = None
     lib.dflash_packed_kv_bytes.argtypes = [G]
     lib.dflash_packed_kv_bytes.restype = sz
     lib.dflash_packed_gamma_bytes.argtypes = [G]
@@ -373,3 +375,8 @@ def dflash_ctx_kv_prefill(geom, hidden, cu_rows, ctx_len, alloc_limit, block_tab
         _ptr(ctx_len), _ptr(alloc_limit), _ptr(block_table), _ptr(valid), ctypes.byref(w),
         _ptr(kv_pool), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))
+
+
+def dflash_test_attention_skip_tile(tile: int) -> None:
+    """Tests of the bounded-wait path only (see include/dflash.h)."""
+    load().dflash_test_attention_skip_tile(int(tile))

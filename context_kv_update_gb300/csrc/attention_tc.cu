@@ -73,6 +73,7 @@ constexpr int kMaxAttnHeadDim = 128;
 struct TcParams {
   AttnParams a;
   int GT, RT, box_rows, nst, chunks, split;
+  int skip_tile;  // tests only: the producer never issues this tile (-1: off)
   uint32_t stage_bytes, k_bytes, bar_off, x_off;
   uint32_t idesc_qk, idesc_pv, v_lbo, v_sbo;
   float scale_log2;
@@ -263,7 +264,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ok = false;
         break;
       }
-      if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
+      const bool skip = t == P.skip_tile;
+      if (lane == 0 && !skip)
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&kv_full[st]), P.stage_bytes);
       __syncwarp();
       // The tile's boxes (page x K/V x 64-dim chunk) are issued by different
       // lanes: copies issued by one thread complete one after another, so
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int j = j0 + lane;
         const int b = (j < nbox) ? j / (2 * P.chunks) : 0;
         const int page = __shfl_sync(0xffffffffu, cur, tb * boxes + b);
-        if (j < nbox) {
+        if (j < nbox && !skip) {
           const int kv = (j / P.chunks) & 1, c = j % P.chunks;
           const int key0 = kbase + b * P.box_rows;
           const long long row0 =
@@ -682,11 +685,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
 }
 
+thread_local int t_skip_tile = -1;
+
 }  // namespace
+
+void attention_test_skip_tile(int tile) { t_skip_tile = tile; }
 
 cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s) {
   TcParams P;
   P.a = a;
+  P.skip_tile = t_skip_tile;
   const int hd = g.head_dim;  // 64 or 128 (validated by the caller)
   P.chunks = hd / 64;
   P.GT = a.Tq * a.G;

@@ -87,6 +87,10 @@ extern "C" int dflash_step_bookkeeping(const dflash_geom *g, int B, const int32_
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" void dflash_test_attention_skip_tile(int tile) {
+  attention_test_skip_tile(tile < 0 ? -1 : tile);
+}
+
 extern "C" size_t dflash_packed_kv_bytes(const dflash_geom *g) {
   if (!geom_ok(g)) return 0;
   return packed_kv_bytes(*g);

@@ -151,6 +151,7 @@ cudaError_t launch_embedding_gather(int n, const int32_t *ids, const void *table
                                     int dim, void *out, int32_t *st, cudaStream_t s);
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq);
+void attention_test_skip_tile(int tile);
 float default_attention_scale(const dflash_geom &g);
 int attention_args_status(const dflash_geom *g, int B, int layer, int Tq, const void *q_rope,
                           int32_t window, float *scale, int mask_mode, int num_segments);
