@@ -18,6 +18,8 @@
 //             paged bf16 store, ctx_len advance
 // Y1 and Y2 stay as the GEMMs' per-CTA partial tiles; the norm and the
 // epilogue add them up as they read (gemm_out_issue / gemm_out_finish).
+#include <algorithm>
+
 #include "dflash_internal.cuh"
 #include "gemm_tc.cuh"
 
@@ -97,6 +99,7 @@ __global__ void prep_kernel(const float *hidden_f32, uint16_t *x, int n_elems, i
 // for the epilogue, which advances it.
 constexpr int kNormThreads = 128;
 constexpr int kNormMaxCols = 8 * kNormThreads;  // columns per CTA
+constexpr int kClusterNormMaxRows = 256;        // beyond: the row-per-CTA kernel
 
 __global__ void __launch_bounds__(kNormThreads) hidden_norm_kernel(
     const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, int cols, float eps,
@@ -156,6 +159,55 @@ __global__ void __launch_bounds__(kNormThreads) hidden_norm_kernel(
     if (col < c1) hn[static_cast<size_t>(n) * D + col] = f32_to_bf16_rn(h[i] * inv * gv[i]);
   }
   ptx::cluster_wait();  // no CTA leaves while another may still read its s_part
+}
+
+// The same norm for many rows (prefill): one 256-thread CTA per row and no
+// cluster -- with thousands of rows there is parallelism enough, and a
+// cluster per row would serialise on cluster scheduling.  Each thread holds
+// up to 32 columns; the partials are read in batches of 8 columns.
+constexpr int kRowNormThreads = 256;
+constexpr int kRowNormMaxCols = 32;  // per thread: d_model <= 8192
+
+__global__ void __launch_bounds__(kRowNormThreads) hidden_norm_rows_kernel(
+    const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, float eps,
+    const int32_t *ctx_len, int32_t *ctx_snap, int B) {
+  __shared__ float red[32];
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x, tid = threadIdx.x;
+  if (n == 0)
+    for (int r = tid; r < B; r += kRowNormThreads) ctx_snap[r] = ctx_len[r];
+  const int nt = n / y.ntile, nr = n - nt * y.ntile;
+  const int per = (D + kRowNormThreads - 1) / kRowNormThreads;
+  float h[kRowNormMaxCols];
+  float ss = 0.f;
+#pragma unroll
+  for (int b0 = 0; b0 < kRowNormMaxCols; b0 += 8) {
+    if (b0 < per) {
+      GemmOutLoad ld[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int col = (b0 + k) * kRowNormThreads + tid;
+        const unsigned t = static_cast<unsigned>(nt) * y.mtiles + static_cast<unsigned>(col >> 7);
+        gemm_out_issue(y, t, (b0 + k < per && col < D) ? gemm_tile_parts(y, t) : 0, nr, col & 127,
+                       ld[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float v = bf16_to_f32(f32_to_bf16_rn(gemm_out_finish(y, ld[k])));
+        h[b0 + k] = v;
+        ss += v * v;
+      }
+    }
+  }
+  const float tot = block_sum(ss, red);
+  const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
+#pragma unroll
+  for (int k = 0; k < kRowNormMaxCols; ++k) {
+    const int col = k * kRowNormThreads + tid;
+    if (k < per && col < D)
+      hn[static_cast<size_t>(n) * D + col] = f32_to_bf16_rn(h[k] * inv * bf16_to_f32(gamma[col]));
+  }
 }
 
 // ----------------------------------------------------------- write mask
@@ -237,29 +289,33 @@ __device__ __forceinline__ void advance_ctx_len(const MaskArgs &m, int32_t *ctx_
 }
 
 // ------------------------------------------------------ GQA epilogue
-// grid (N rows, L*2*nkv heads), block = head_dim threads.  kStaged = false:
-// the fused update (write-masked paged store, ctx_len advance).  kStaged =
-// true: the projection half of a split update -- every row, RoPE at
-// c + i, the bf16 value to staged[n][col] (no mask, no store to the pool).
+// grid (N rows, L*2*nkv heads), block = head_dim / 2 threads rounded up to a
+// warp: thread t holds columns t and t + hd/2 of the head -- a rotate-half
+// pair, so one cos/sin serves both and RoPE needs no exchange.  kStaged =
+// false: the fused update (write-masked paged store, ctx_len advance).
+// kStaged = true: the projection half of a split update -- every row, RoPE at
+// c + i, the bf16 values to staged[n][col] (no mask, no store to the pool).
 template <bool kStaged>
 __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_k, uint16_t *pool, uint16_t *staged,
                                     int L, int nkv, int hd, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
-  __shared__ float kbuf[kMaxHeadDim];
   __shared__ __align__(16) uint16_t obuf[kMaxHeadDim];  // the bf16 row, stored as 16-byte vectors
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
   const int head = blockIdx.y;  // ((l * 2 + kv) * nkv + h)
-  const int d = threadIdx.x;
-  const int col = head * hd + d;
+  const int t = threadIdx.x, half = hd >> 1;
+  const bool act = t < half;
   // the Y2 loads go out first, overlapping the destination lookup
-  GemmOutLoad ld;
+  GemmOutLoad ld0, ld1;
   {
-    const int nt = n / y.ntile;
-    const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
-    gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
+    const int c0 = head * hd + (act ? t : 0), c1 = c0 + half;
+    const int nt = n / y.ntile, nr = n - nt * y.ntile;
+    const unsigned t0 = static_cast<unsigned>(nt) * y.mtiles + (c0 >> 7);
+    const unsigned t1 = static_cast<unsigned>(nt) * y.mtiles + (c1 >> 7);
+    gemm_out_issue(y, t0, act ? gemm_tile_parts(y, t0) : 0, nr, c0 & 127, ld0);
+    gemm_out_issue(y, t1, act ? gemm_tile_parts(y, t1) : 0, nr, c1 & 127, ld1);
   }
   // ctx_len advance; every reader of the pre-step value uses the snapshot
   if (!kStaged && n == 0 && head == 0) advance_ctx_len(m, ctx_len, B);
@@ -268,57 +324,67 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
-  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && d == 0)) {
+  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && t == 0)) {
     return;
   }
   const int l = head / (2 * nkv);
   const int kv = (head / nkv) & 1;
   const int h = head % nkv;
-  float v = gemm_out_finish(y, ld);
+  float v0 = gemm_out_finish(y, ld0), v1 = gemm_out_finish(y, ld1);
   if (kv == 0) {
-    const float ss = block_sum(v * v, red);
+    const float ss = block_sum(act ? v0 * v0 + v1 * v1 : 0.f, red);
     const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
-    const float kn = v * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + d]);
-    kbuf[d] = kn;
-    __syncthreads();
-    const int half = hd >> 1;
-    const int j = d < half ? d : d - half;
-    float c, s;
-    rope_cos_sin(pos, rf.f[j], &c, &s);
-    v = d < half ? kn * c - kbuf[d + half] * s : kn * c + kbuf[d - half] * s;
+    if (act) {
+      const float k0 = v0 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t]);
+      const float k1 = v1 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t + half]);
+      float c, s;
+      rope_cos_sin(pos, rf.f[t], &c, &s);
+      v0 = k0 * c - k1 * s;
+      v1 = k1 * c + k0 * s;
+    }
   }
-  obuf[d] = f32_to_bf16_rn(v);
+  if (act) {
+    obuf[t] = f32_to_bf16_rn(v0);
+    obuf[t + half] = f32_to_bf16_rn(v1);
+  }
   __syncthreads();
-  if (d < hd / 8) {  // head_dim % 8 == 0: the row leaves as 16-byte vectors
+  if (t < hd / 8) {  // head_dim % 8 == 0: the row leaves as 16-byte vectors
     uint16_t *row =
         kStaged ? staged + static_cast<size_t>(n) * L * 2 * nkv * hd + head * hd
                 : pool + ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P +
                           slot) * hd;
-    reinterpret_cast<uint4 *>(row)[d] = reinterpret_cast<const uint4 *>(obuf)[d];
+    reinterpret_cast<uint4 *>(row)[t] = reinterpret_cast<const uint4 *>(obuf)[t];
   }
 }
 
 // ------------------------------------------------------ MLA epilogue
-// grid (N rows, L), block = lat + rope threads; kStaged as for GQA.
+// grid (N rows, L), block = lat / 2 + rope / 2 threads rounded up to a warp:
+// thread t < lat/2 holds latent columns t and t + lat/2; thread lat/2 + j
+// holds the rope pair j, j + rope/2.  kStaged as for GQA.
 template <bool kStaged>
 __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_kv, uint16_t *pool, uint16_t *staged,
                                     int L, int lat, int rope, float eps, int32_t *ctx_len, int B) {
   __shared__ float red[32];
-  __shared__ float rbuf[kMaxHeadDim];
   __shared__ __align__(16) uint16_t obuf[1024];  // lat + rope <= 1024
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x;
   const int l = blockIdx.y;
-  const int d = threadIdx.x;
-  const int W = lat + rope;
-  const int col = l * W + d;
-  GemmOutLoad ld;
+  const int t = threadIdx.x;
+  const int W = lat + rope, hl = lat >> 1, hr = rope >> 1;
+  const bool is_lat = t < hl, is_rope = !is_lat && t < hl + hr;
+  const int ca = is_lat ? t : (is_rope ? lat + (t - hl) : 0);
+  const int cb = is_lat ? t + hl : ca + hr;
+  GemmOutLoad ld0, ld1;
   {
-    const int nt = n / y.ntile;
-    const unsigned t = static_cast<unsigned>(nt) * y.mtiles + (col >> 7);
-    gemm_out_issue(y, t, gemm_tile_parts(y, t), n - nt * y.ntile, col & 127, ld);
+    const int nt = n / y.ntile, nr = n - nt * y.ntile;
+    const int g0 = l * W + ca, g1 = l * W + cb;
+    const unsigned t0 = static_cast<unsigned>(nt) * y.mtiles + (g0 >> 7);
+    const unsigned t1 = static_cast<unsigned>(nt) * y.mtiles + (g1 >> 7);
+    const bool act = is_lat || is_rope;
+    gemm_out_issue(y, t0, act ? gemm_tile_parts(y, t0) : 0, nr, g0 & 127, ld0);
+    gemm_out_issue(y, t1, act ? gemm_tile_parts(y, t1) : 0, nr, g1 & 127, ld1);
   }
   if (!kStaged && n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
   int r, i;
@@ -326,32 +392,31 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
-  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && d == 0)) {
+  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && t == 0)) {
     return;
   }
-  const float v = gemm_out_finish(y, ld);
-  const float ss = block_sum(d < lat ? v * v : 0.f, red);
-  float outv;
-  if (d < lat) {
+  const float v0 = gemm_out_finish(y, ld0), v1 = gemm_out_finish(y, ld1);
+  const float ss = block_sum(is_lat ? v0 * v0 + v1 * v1 : 0.f, red);
+  float o0 = 0.f, o1 = 0.f;
+  if (is_lat) {
     const float inv = rsqrtf(ss / static_cast<float>(lat) + eps);
-    outv = v * inv * bf16_to_f32(gamma_kv[static_cast<size_t>(l) * lat + d]);
-  } else {
-    rbuf[d - lat] = v;
-  }
-  __syncthreads();
-  if (d >= lat) {
-    const int e = d - lat, half = rope >> 1;
-    const int j = e < half ? e : e - half;
+    o0 = v0 * inv * bf16_to_f32(gamma_kv[static_cast<size_t>(l) * lat + ca]);
+    o1 = v1 * inv * bf16_to_f32(gamma_kv[static_cast<size_t>(l) * lat + cb]);
+  } else if (is_rope) {
     float c, s;
-    rope_cos_sin(pos, rf.f[j], &c, &s);
-    outv = e < half ? v * c - rbuf[e + half] * s : v * c + rbuf[e - half] * s;
+    rope_cos_sin(pos, rf.f[t - hl], &c, &s);
+    o0 = v0 * c - v1 * s;
+    o1 = v1 * c + v0 * s;
   }
-  obuf[d] = f32_to_bf16_rn(outv);
+  if (is_lat || is_rope) {
+    obuf[ca] = f32_to_bf16_rn(o0);
+    obuf[cb] = f32_to_bf16_rn(o1);
+  }
   __syncthreads();
-  if (d < W / 8) {  // (lat + rope) % 8 == 0: the row leaves as 16-byte vectors
+  if (t < W / 8) {  // (lat + rope) % 8 == 0: the row leaves as 16-byte vectors
     uint16_t *row = kStaged ? staged + static_cast<size_t>(n) * L * W + static_cast<size_t>(l) * W
                             : pool + ((static_cast<size_t>(l) * m.NP + page) * m.P + slot) * W;
-    reinterpret_cast<uint4 *>(row)[d] = reinterpret_cast<const uint4 *>(obuf)[d];
+    reinterpret_cast<uint4 *>(row)[t] = reinterpret_cast<const uint4 *>(obuf)[t];
   }
 }
 
@@ -439,8 +504,25 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
                        /*pdl=*/true, s, &y1)) != cudaSuccess)
     return e;
 
-  // hidden RMSNorm: a cluster of G CTAs per row
-  {
+  // hidden RMSNorm: a cluster of G CTAs per row for decode-sized row counts,
+  // one CTA per row beyond (prefill)
+  if (d.N > kClusterNormMaxRows) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(d.N);
+    cfg.blockDim = dim3(kRowNormThreads);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (d.D > kRowNormThreads * kRowNormMaxCols) return cudaErrorInvalidValue;
+    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_rows_kernel, y1,
+                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
+                                static_cast<float>(g.eps_hidden),
+                                static_cast<const int32_t *>(ctx_len), snap, B)) != cudaSuccess)
+      return e;
+  } else {
     int G = (d.D + 511) / 512;
     if (G > 8) G = 8;
     const int cols = (d.D + G - 1) / G;  // <= kNormMaxCols, as d_model <= 8192
@@ -496,14 +578,14 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   if (g.kind == DFLASH_KIND_GQA) {
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
-    cfg.blockDim = dim3(g.head_dim);
+    cfg.blockDim = dim3(std::max(32, (g.head_dim / 2 + 31) / 32 * 32));
     e = cudaLaunchKernelEx(&cfg, split ? epilogue_gqa_kernel<true> : epilogue_gqa_kernel<false>, y2,
                            m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
                            g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else {
     fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers);
-    cfg.blockDim = dim3(g.latent_dim + g.rope_dim);
+    cfg.blockDim = dim3((g.latent_dim / 2 + g.rope_dim / 2 + 31) / 32 * 32);
     e = cudaLaunchKernelEx(&cfg, split ? epilogue_mla_kernel<true> : epilogue_mla_kernel<false>, y2,
                            m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
                            g.num_layers, g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k),
