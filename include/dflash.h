@@ -520,8 +520,8 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
  * at zero.  Calls whose GPU work overlaps (other streams, graph branches) race
  * on it: serialise them.
  * Set-up: the first call on each device looks up the array's device address
- * (with that device current) and caches it; make that first call before any
- * stream capture.  The call allocates nothing and calls no allocating routine.
+ * (with that device current) and caches it.  The call allocates nothing and
+ * calls no allocating routine.
  * Errors: the argument checks of dflash_block_attention come first and give
  * the same codes; then DFLASH_ERR_WORKSPACE_TOO_SMALL for a problem larger
  * than the fixed scratch, and DFLASH_ERR_CUDA when the address look-up fails.
