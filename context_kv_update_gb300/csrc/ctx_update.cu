@@ -18,6 +18,10 @@
 //             paged bf16 store, ctx_len advance
 // Y1 and Y2 stay as the GEMMs' per-CTA partial tiles; the norm and the
 // epilogue add them up as they read (gemm_out_issue / gemm_out_finish).
+// Up to 256 rows (decode) the norm is a cluster per row and the epilogue a
+// CTA per (row, head); beyond (prefill, large batches) one CTA per row of
+// 16-byte loads, with the row destinations resolved once by the norm, and
+// an epilogue of 16-byte loads and 8-byte stores.
 #include <algorithm>
 
 #include "dflash_internal.cuh"
@@ -33,6 +37,7 @@ struct CtxWs {
   uint16_t *hn;       // [Npad, D]    bf16
   float *part1;       // fc partial tiles (Y1)
   float *part2;       // K/V (or latent) partial tiles (Y2)
+  int4 *dst;          // [Npad] row destinations (many-row epilogue)
   size_t bytes;
 };
 
@@ -69,6 +74,8 @@ CtxWs ctx_ws_map_rows(const dflash_geom &g, int B, int N, void *base) {
   off = align_up(off + gemm_partial_bytes(d.D, d.D_in, d.Npad), 256);
   w.part2 = reinterpret_cast<float *>(p + off);
   off = align_up(off + gemm_partial_bytes(d.Wrows, d.D, d.Npad), 256);
+  w.dst = reinterpret_cast<int4 *>(p + off);
+  off = align_up(off + sizeof(int4) * d.Npad, 256);
   w.bytes = off;
   return w;
 }
@@ -161,55 +168,6 @@ __global__ void __launch_bounds__(kNormThreads) hidden_norm_kernel(
   ptx::cluster_wait();  // no CTA leaves while another may still read its s_part
 }
 
-// The same norm for many rows (prefill): one 256-thread CTA per row and no
-// cluster -- with thousands of rows there is parallelism enough, and a
-// cluster per row would serialise on cluster scheduling.  Each thread holds
-// up to 32 columns; the partials are read in batches of 8 columns.
-constexpr int kRowNormThreads = 256;
-constexpr int kRowNormMaxCols = 32;  // per thread: d_model <= 8192
-
-__global__ void __launch_bounds__(kRowNormThreads) hidden_norm_rows_kernel(
-    const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, float eps,
-    const int32_t *ctx_len, int32_t *ctx_snap, int B) {
-  __shared__ float red[32];
-  griddep_launch();
-  griddep_wait();
-  const int n = blockIdx.x, tid = threadIdx.x;
-  if (n == 0)
-    for (int r = tid; r < B; r += kRowNormThreads) ctx_snap[r] = ctx_len[r];
-  const int nt = n / y.ntile, nr = n - nt * y.ntile;
-  const int per = (D + kRowNormThreads - 1) / kRowNormThreads;
-  float h[kRowNormMaxCols];
-  float ss = 0.f;
-#pragma unroll
-  for (int b0 = 0; b0 < kRowNormMaxCols; b0 += 8) {
-    if (b0 < per) {
-      GemmOutLoad ld[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int col = (b0 + k) * kRowNormThreads + tid;
-        const unsigned t = static_cast<unsigned>(nt) * y.mtiles + static_cast<unsigned>(col >> 7);
-        gemm_out_issue(y, t, (b0 + k < per && col < D) ? gemm_tile_parts(y, t) : 0, nr, col & 127,
-                       ld[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float v = bf16_to_f32(f32_to_bf16_rn(gemm_out_finish(y, ld[k])));
-        h[b0 + k] = v;
-        ss += v * v;
-      }
-    }
-  }
-  const float tot = block_sum(ss, red);
-  const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
-#pragma unroll
-  for (int k = 0; k < kRowNormMaxCols; ++k) {
-    const int col = k * kRowNormThreads + tid;
-    if (k < per && col < D)
-      hn[static_cast<size_t>(n) * D + col] = f32_to_bf16_rn(h[k] * inv * bf16_to_f32(gamma[col]));
-  }
-}
-
 // ----------------------------------------------------------- write mask
 struct MaskArgs {
   const int32_t *n_acc;
@@ -286,6 +244,247 @@ __device__ __forceinline__ void advance_ctx_len(const MaskArgs &m, int32_t *ctx_
     const int A = m.alloc_limit[r];
     ctx_len[r] = live ? static_cast<int>(s < A ? s : A) : 0;
   }
+}
+
+// ------------------------------------------- many rows (prefill, large batches)
+// Beyond kClusterNormMaxRows rows the norm and the epilogue trade per-row
+// parallelism for bytes in flight: thousands of small CTAs, each waiting on a
+// few 4-byte loads, leave HBM idle.  Here every thread moves 16-byte vectors
+// and issues all its loads before it adds any.
+
+// Y[n, col..col+3] as a float4, the tile's partials added in CTA order (the
+// order gemm_out_finish uses).  The second partial's load goes out with the
+// first; any further ones follow.
+struct Vec4Load {
+  float4 a, b;
+  int cnt;
+};
+
+__device__ __forceinline__ float4 add4(float4 x, float4 y) {
+  return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+}
+
+__device__ __forceinline__ const float *vec4_src(const GemmOut &g, int n, int col, unsigned *t) {
+  const int nt = n / g.ntile, nr = n - nt * g.ntile;
+  *t = static_cast<unsigned>(nt) * g.mtiles + static_cast<unsigned>(col >> 7);
+  const size_t stride = static_cast<size_t>(g.ntile) * 128;
+  return g.part + static_cast<size_t>(*t) * g.maxc * stride + static_cast<size_t>(nr) * 128 +
+         (col & 127);
+}
+
+__device__ __forceinline__ void vec4_issue(const GemmOut &g, int n, int col, bool on, Vec4Load &v) {
+  unsigned t;
+  const float *src = vec4_src(g, n, col, &t);
+  const size_t stride = static_cast<size_t>(g.ntile) * 128;
+  v.cnt = on ? gemm_tile_parts(g, t) : 0;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  v.a = v.cnt > 0 ? __ldcg(reinterpret_cast<const float4 *>(src)) : z;
+  v.b = v.cnt > 1 ? __ldcg(reinterpret_cast<const float4 *>(src + stride)) : z;
+}
+
+__device__ __forceinline__ float4 vec4_finish(const GemmOut &g, int n, int col, const Vec4Load &v) {
+  float4 acc = v.a;
+  if (v.cnt > 1) acc = add4(acc, v.b);
+  if (v.cnt > 2) {
+    unsigned t;
+    const float *src = vec4_src(g, n, col, &t);
+    const size_t stride = static_cast<size_t>(g.ntile) * 128;
+    for (int j = 2; j < v.cnt; ++j)
+      acc = add4(acc, __ldcg(reinterpret_cast<const float4 *>(src + j * stride)));
+  }
+  return acc;
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+// Destination of each GEMM row, resolved once per row by the norm for the
+// epilogue: {page, slot, position, 0}, page -1 when the row is not stored.
+struct RowDest {
+  int4 *dst;  // [N] or nullptr (the epilogue resolves rows itself)
+  MaskArgs m; // ctx_snap = the live ctx_len (nothing advances it before the epilogue)
+};
+
+// hn = bf16(bf16(Y1 row) * gamma_h / rms), one CTA of D/32 threads per row:
+// thread t holds the 8-column groups t + k*D/32, k < 4, two float4 loads per
+// partial.  CTA 0 snapshots ctx_len; thread 0 of each CTA resolves the row's
+// destination when the wide epilogue follows.
+constexpr int kWideNormGroups = 4;
+
+__global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
+    const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, float eps,
+    const int32_t *ctx_len, int32_t *ctx_snap, int B, const RowDest rd) {
+  __shared__ float red[32];
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x, tid = threadIdx.x;
+  const int T = D >> 5;
+  const bool act = tid < T;
+  if (n == 0)
+    for (int r = tid; r < B; r += blockDim.x) ctx_snap[r] = ctx_len[r];
+  Vec4Load ld[kWideNormGroups][2];
+#pragma unroll
+  for (int k = 0; k < kWideNormGroups; ++k) {
+    const int col = 8 * (tid + k * T);
+    vec4_issue(y, n, col, act, ld[k][0]);
+    vec4_issue(y, n, col + 4, act, ld[k][1]);
+  }
+  if (rd.dst && tid == 0) {
+    int r, i, page = 0, slot = 0, pos = 0;
+    const bool w = row_of(rd.m, n, &r, &i) && ctx_row_dest(rd.m, r, i, &page, &slot, &pos, true);
+    rd.dst[n] = make_int4(w ? page : -1, slot, pos, 0);
+  }
+  float h[kWideNormGroups][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kWideNormGroups; ++k) {
+    const int col = 8 * (tid + k * T);
+    const float4 u0 = vec4_finish(y, n, col, ld[k][0]), u1 = vec4_finish(y, n, col + 4, ld[k][1]);
+    const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      h[k][e] = bf16_to_f32(f32_to_bf16_rn(v[e]));
+      ss += h[k][e] * h[k][e];
+    }
+  }
+  const float tot = block_sum(ss, red);
+  const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
+  if (!act) return;
+  const bool g16 = (reinterpret_cast<uintptr_t>(gamma) & 15u) == 0;
+#pragma unroll
+  for (int k = 0; k < kWideNormGroups; ++k) {
+    const int col = 8 * (tid + k * T);
+    uint16_t gb[8];
+    if (g16) {
+      const uint4 q = *reinterpret_cast<const uint4 *>(gamma + col);
+      const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        gb[2 * e] = static_cast<uint16_t>(wv[e] & 0xffffu);
+        gb[2 * e + 1] = static_cast<uint16_t>(wv[e] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gb[e] = gamma[col + e];
+    }
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = h[k][e] * inv * bf16_to_f32(gb[e]);
+    uint4 q;
+    q.x = pack2_bf16(o[0], o[1]);
+    q.y = pack2_bf16(o[2], o[3]);
+    q.z = pack2_bf16(o[4], o[5]);
+    q.w = pack2_bf16(o[6], o[7]);
+    *reinterpret_cast<uint4 *>(hn + static_cast<size_t>(n) * D + col) = q;
+  }
+}
+
+// GQA epilogue for many rows: a unit is one head row (row n, head = (l*2+kv)*nkv
+// + h) handled by hd/8 lanes; lane j holds columns 4j..4j+3 and hd/2 + 4j..+3,
+// i.e. four rotate-half pairs.  256 threads = 256 / (hd/8) units per CTA.
+// The k RMSNorm is a shuffle sum over the unit's lanes; the row leaves as two
+// 8-byte stores per lane.  Needs hd / 8 a power of two <= 32.
+__global__ void __launch_bounds__(256) epilogue_gqa_wide_kernel(
+    const GemmOut y, const MaskArgs m, const int4 *dst, const RopeFreqs rf,
+    const uint16_t *gamma_k, uint16_t *pool, int N, int L, int nkv, int hd, float eps,
+    int32_t *ctx_len, int B) {
+  griddep_launch();
+  griddep_wait();
+  if (blockIdx.x == 0) advance_ctx_len(m, ctx_len, B);
+  const int lpu = hd >> 3, half = hd >> 1;
+  const int H = L * 2 * nkv;
+  const long long u = static_cast<long long>(blockIdx.x) * (blockDim.x / lpu) + threadIdx.x / lpu;
+  const int j = threadIdx.x % lpu;
+  if (u >= static_cast<long long>(N) * H) return;  // whole units leave together
+  const int n = static_cast<int>(u / H), head = static_cast<int>(u % H);
+  Vec4Load lo, hi;
+  const int ca = head * hd + 4 * j, cb = ca + half;
+  vec4_issue(y, n, ca, true, lo);
+  vec4_issue(y, n, cb, true, hi);
+  const int4 d = dst[n];
+  float4 a = vec4_finish(y, n, ca, lo), b = vec4_finish(y, n, cb, hi);
+  if (d.x < 0) return;
+  const int l = head / (2 * nkv), kv = (head / nkv) & 1, h = head % nkv;
+  if (kv == 0) {
+    const unsigned mask = (lpu == 32 ? 0xffffffffu : ((1u << lpu) - 1u))
+                          << ((threadIdx.x & 31) & ~(lpu - 1));
+    float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
+               b.w * b.w;
+    for (int o = lpu >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+    const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
+    const uint16_t *gk = gamma_k + static_cast<size_t>(l) * hd;
+    float va[4] = {a.x, a.y, a.z, a.w}, vb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * j + e;
+      const float k0 = va[e] * inv * bf16_to_f32(gk[c]);
+      const float k1 = vb[e] * inv * bf16_to_f32(gk[c + half]);
+      float cs, sn;
+      rope_cos_sin(d.z, rf.f[c], &cs, &sn);
+      va[e] = k0 * cs - k1 * sn;
+      vb[e] = k1 * cs + k0 * sn;
+    }
+    a = make_float4(va[0], va[1], va[2], va[3]);
+    b = make_float4(vb[0], vb[1], vb[2], vb[3]);
+  }
+  uint16_t *row =
+      pool + ((((static_cast<size_t>(l) * m.NP + d.x) * 2 + kv) * nkv + h) * m.P + d.y) * hd;
+  *reinterpret_cast<uint2 *>(row + 4 * j) = make_uint2(pack2_bf16(a.x, a.y), pack2_bf16(a.z, a.w));
+  *reinterpret_cast<uint2 *>(row + half + 4 * j) =
+      make_uint2(pack2_bf16(b.x, b.y), pack2_bf16(b.z, b.w));
+}
+
+// MLA epilogue for many rows: grid (N rows, L), lat/8 latent lanes (columns
+// 4j..+3 and lat/2 + 4j..+3) and rope/8 rope lanes (the same split of the
+// rope part); two 8-byte stores per lane.  Needs lat % 8 == rope % 8 == 0.
+__global__ void __launch_bounds__(256) epilogue_mla_wide_kernel(
+    const GemmOut y, const MaskArgs m, const int4 *dst, const RopeFreqs rf,
+    const uint16_t *gamma_kv, uint16_t *pool, int L, int lat, int rope, float eps,
+    int32_t *ctx_len, int B) {
+  __shared__ float red[32];
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x, l = blockIdx.y, t = threadIdx.x;
+  if (n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
+  const int W = lat + rope, nl = lat >> 3, nr = rope >> 3;
+  const bool is_lat = t < nl, is_rope = !is_lat && t < nl + nr;
+  const int j = is_lat ? t : t - nl;
+  const int ca = is_lat ? 4 * j : lat + 4 * j;
+  const int cb = ca + (is_lat ? lat >> 1 : rope >> 1);
+  Vec4Load lo, hi;
+  const int ga = l * W + (is_lat || is_rope ? ca : 0), gb = l * W + (is_lat || is_rope ? cb : 0);
+  vec4_issue(y, n, ga, is_lat || is_rope, lo);
+  vec4_issue(y, n, gb, is_lat || is_rope, hi);
+  const int4 d = dst[n];
+  float4 a = vec4_finish(y, n, ga, lo), b = vec4_finish(y, n, gb, hi);
+  const float ss = block_sum(is_lat ? a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x +
+                                          b.y * b.y + b.z * b.z + b.w * b.w
+                                    : 0.f,
+                             red);
+  if (d.x < 0 || !(is_lat || is_rope)) return;
+  float va[4] = {a.x, a.y, a.z, a.w}, vb[4] = {b.x, b.y, b.z, b.w};
+  if (is_lat) {
+    const float inv = rsqrtf(ss / static_cast<float>(lat) + eps);
+    const uint16_t *gk = gamma_kv + static_cast<size_t>(l) * lat;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      va[e] = va[e] * inv * bf16_to_f32(gk[ca + e]);
+      vb[e] = vb[e] * inv * bf16_to_f32(gk[cb + e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float cs, sn;
+      rope_cos_sin(d.z, rf.f[4 * j + e], &cs, &sn);
+      const float x0 = va[e], x1 = vb[e];
+      va[e] = x0 * cs - x1 * sn;
+      vb[e] = x1 * cs + x0 * sn;
+    }
+  }
+  uint16_t *row = pool + ((static_cast<size_t>(l) * m.NP + d.x) * m.P + d.y) * W;
+  *reinterpret_cast<uint2 *>(row + ca) = make_uint2(pack2_bf16(va[0], va[1]), pack2_bf16(va[2], va[3]));
+  *reinterpret_cast<uint2 *>(row + cb) = make_uint2(pack2_bf16(vb[0], vb[1]), pack2_bf16(vb[2], vb[3]));
 }
 
 // ------------------------------------------------------ GQA epilogue
@@ -504,23 +703,48 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
                        /*pdl=*/true, s, &y1)) != cudaSuccess)
     return e;
 
+  // epilogue arguments (the norm resolves row destinations with them)
+  MaskArgs m;
+  m.n_acc = n_acc;
+  m.ctx_snap = snap;
+  m.alloc_limit = alloc_limit;
+  m.tbl = tbl;
+  m.valid = valid;
+  m.cu_rows = cu_rows;
+  m.T = g.block_size;
+  m.M = g.max_pages;
+  m.P = g.page_size;
+  m.NP = g.num_pool_pages;
+  m.B = B;
+  m.st = st;
+  const bool gqa = g.kind == DFLASH_KIND_GQA;
+  const int lpu = g.head_dim / 8;
+  const bool wide = d.N > kClusterNormMaxRows;
+  const bool wide_epi = wide && !split &&
+                        (gqa ? (lpu >= 1 && lpu <= 32 && (lpu & (lpu - 1)) == 0 && g.head_dim % 8 == 0)
+                             : (g.latent_dim % 8 == 0 && g.rope_dim % 8 == 0));
+  RowDest rd;
+  rd.dst = wide_epi ? W.dst : nullptr;
+  rd.m = m;
+  rd.m.ctx_snap = ctx_len;
+
   // hidden RMSNorm: a cluster of G CTAs per row for decode-sized row counts,
-  // one CTA per row beyond (prefill)
-  if (d.N > kClusterNormMaxRows) {
+  // one CTA per row beyond
+  if (wide) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(d.N);
-    cfg.blockDim = dim3(kRowNormThreads);
+    cfg.blockDim = dim3((d.D / 32 + 31) / 32 * 32);
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (d.D > kRowNormThreads * kRowNormMaxCols) return cudaErrorInvalidValue;
-    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_rows_kernel, y1,
+    if (d.D % 64 != 0 || d.D > 8192) return cudaErrorInvalidValue;
+    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_wide_kernel, y1,
                                 static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
                                 static_cast<float>(g.eps_hidden),
-                                static_cast<const int32_t *>(ctx_len), snap, B)) != cudaSuccess)
+                                static_cast<const int32_t *>(ctx_len), snap, B, rd)) != cudaSuccess)
       return e;
   } else {
     int G = (d.D + 511) / 512;
@@ -553,19 +777,6 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     return e;
 
   // epilogue
-  MaskArgs m;
-  m.n_acc = n_acc;
-  m.ctx_snap = snap;
-  m.alloc_limit = alloc_limit;
-  m.tbl = tbl;
-  m.valid = valid;
-  m.cu_rows = cu_rows;
-  m.T = g.block_size;
-  m.M = g.max_pages;
-  m.P = g.page_size;
-  m.NP = g.num_pool_pages;
-  m.B = B;
-  m.st = st;
   RopeFreqs rf;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -575,7 +786,25 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   cfg.numAttrs = 1;
   cfg.stream = s;
   uint16_t *pool16 = static_cast<uint16_t *>(pool);
-  if (g.kind == DFLASH_KIND_GQA) {
+  if (wide_epi && gqa) {
+    fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
+    const long long units = static_cast<long long>(d.N) * g.num_layers * 2 * g.nkv;
+    const int upc = 256 / lpu;
+    cfg.gridDim = dim3(static_cast<unsigned>((units + upc - 1) / upc));
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, epilogue_gqa_wide_kernel, y2, m,
+                           static_cast<const int4 *>(W.dst), rf,
+                           static_cast<const uint16_t *>(w.gamma_k), pool16, d.N, g.num_layers,
+                           g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
+  } else if (wide_epi) {
+    fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
+    cfg.gridDim = dim3(d.N, g.num_layers);
+    cfg.blockDim = dim3(((g.latent_dim + g.rope_dim) / 8 + 31) / 32 * 32);
+    e = cudaLaunchKernelEx(&cfg, epilogue_mla_wide_kernel, y2, m,
+                           static_cast<const int4 *>(W.dst), rf,
+                           static_cast<const uint16_t *>(w.gamma_k), pool16, g.num_layers,
+                           g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k), ctx_len, B);
+  } else if (gqa) {
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
     cfg.blockDim = dim3(std::max(32, (g.head_dim / 2 + 31) / 32 * 32));
