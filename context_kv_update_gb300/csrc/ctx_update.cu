@@ -38,11 +38,12 @@ struct CtxWs {
   float *part1;       // fc partial tiles (Y1)
   float *part2;       // K/V (or latent) partial tiles (Y2)
   int4 *dst;          // [Npad] row destinations (many-row epilogue)
+  float2 *cs;         // [Npad][nf] RoPE cos/sin per row (many-row epilogue)
   size_t bytes;
 };
 
 struct CtxDims {
-  int N, Npad, D_in, D, Wrows;
+  int N, Npad, D_in, D, Wrows, nf;
 };
 
 CtxDims ctx_dims_rows(const dflash_geom &g, int N) {
@@ -53,6 +54,7 @@ CtxDims ctx_dims_rows(const dflash_geom &g, int N) {
   d.D = g.d_model;
   d.Wrows = (g.kind == DFLASH_KIND_GQA) ? g.num_layers * 2 * g.nkv * g.head_dim
                                         : g.num_layers * (g.latent_dim + g.rope_dim);
+  d.nf = (g.kind == DFLASH_KIND_GQA) ? g.head_dim / 2 : g.rope_dim / 2;
   return d;
 }
 
@@ -76,6 +78,8 @@ CtxWs ctx_ws_map_rows(const dflash_geom &g, int B, int N, void *base) {
   off = align_up(off + gemm_partial_bytes(d.Wrows, d.D, d.Npad), 256);
   w.dst = reinterpret_cast<int4 *>(p + off);
   off = align_up(off + sizeof(int4) * d.Npad, 256);
+  w.cs = reinterpret_cast<float2 *>(p + off);
+  off = align_up(off + sizeof(float2) * d.Npad * d.nf, 256);
   w.bytes = off;
   return w;
 }
@@ -295,6 +299,32 @@ __device__ __forceinline__ float4 vec4_finish(const GemmOut &g, int n, int col, 
   return acc;
 }
 
+// The same with only the first partial's load in flight (fewer registers:
+// for the K/V GEMM at prefill sizes a second partial is the exception).
+struct Vec4Load1 {
+  float4 a;
+  int cnt;
+};
+
+__device__ __forceinline__ void vec4_issue1(const GemmOut &g, int n, int col, bool on, Vec4Load1 &v) {
+  unsigned t;
+  const float *src = vec4_src(g, n, col, &t);
+  v.cnt = on ? gemm_tile_parts(g, t) : 0;
+  v.a = v.cnt > 0 ? __ldcg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ float4 vec4_finish1(const GemmOut &g, int n, int col, const Vec4Load1 &v) {
+  float4 acc = v.a;
+  if (v.cnt > 1) {
+    unsigned t;
+    const float *src = vec4_src(g, n, col, &t);
+    const size_t stride = static_cast<size_t>(g.ntile) * 128;
+    for (int j = 1; j < v.cnt; ++j)
+      acc = add4(acc, __ldcg(reinterpret_cast<const float4 *>(src + j * stride)));
+  }
+  return acc;
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
 }
@@ -302,8 +332,10 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // Destination of each GEMM row, resolved once per row by the norm for the
 // epilogue: {page, slot, position, 0}, page -1 when the row is not stored.
 struct RowDest {
-  int4 *dst;  // [N] or nullptr (the epilogue resolves rows itself)
-  MaskArgs m; // ctx_snap = the live ctx_len (nothing advances it before the epilogue)
+  int4 *dst;     // [N] or nullptr (the epilogue resolves rows itself)
+  float2 *cs;    // [N][nf] cos/sin of the row's RoPE angles
+  int nf;        // rotate-half pairs per row (GQA hd/2, MLA rope/2)
+  MaskArgs m;    // ctx_snap = the live ctx_len (nothing advances it before the epilogue)
 };
 
 // hn = bf16(bf16(Y1 row) * gamma_h / rms), one CTA of D/32 threads per row:
@@ -314,8 +346,9 @@ constexpr int kWideNormGroups = 4;
 
 __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
     const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, float eps,
-    const int32_t *ctx_len, int32_t *ctx_snap, int B, const RowDest rd) {
+    const int32_t *ctx_len, int32_t *ctx_snap, int B, const RowDest rd, const RopeFreqs rf) {
   __shared__ float red[32];
+  __shared__ int s_pos;
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x, tid = threadIdx.x;
@@ -334,6 +367,7 @@ __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
     int r, i, page = 0, slot = 0, pos = 0;
     const bool w = row_of(rd.m, n, &r, &i) && ctx_row_dest(rd.m, r, i, &page, &slot, &pos, true);
     rd.dst[n] = make_int4(w ? page : -1, slot, pos, 0);
+    s_pos = w ? pos : -1;
   }
   float h[kWideNormGroups][8];
   float ss = 0.f;
@@ -348,8 +382,16 @@ __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
       ss += h[k][e] * h[k][e];
     }
   }
-  const float tot = block_sum(ss, red);
+  const float tot = block_sum(ss, red);  // its barriers also publish s_pos
   const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
+  // the row's RoPE cos/sin, once per (row, pair) for every head and layer
+  // of the epilogue (the angle is formed in double precision)
+  if (rd.dst && s_pos >= 0)
+    for (int f = tid; f < rd.nf; f += blockDim.x) {
+      float c, sn;
+      rope_cos_sin(s_pos, rf.f[f], &c, &sn);
+      rd.cs[static_cast<size_t>(n) * rd.nf + f] = make_float2(c, sn);
+    }
   if (!act) return;
   const bool g16 = (reinterpret_cast<uintptr_t>(gamma) & 15u) == 0;
 #pragma unroll
@@ -380,111 +422,154 @@ __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
   }
 }
 
-// GQA epilogue for many rows: a unit is one head row (row n, head = (l*2+kv)*nkv
-// + h) handled by hd/8 lanes; lane j holds columns 4j..4j+3 and hd/2 + 4j..+3,
-// i.e. four rotate-half pairs.  256 threads = 256 / (hd/8) units per CTA.
-// The k RMSNorm is a shuffle sum over the unit's lanes; the row leaves as two
-// 8-byte stores per lane.  Needs hd / 8 a power of two <= 32.
-__global__ void __launch_bounds__(256) epilogue_gqa_wide_kernel(
-    const GemmOut y, const MaskArgs m, const int4 *dst, const RopeFreqs rf,
+// GQA epilogue for many rows: a unit is one KV head of one layer of one row,
+// K and V, handled by hd/8 lanes; lane j holds columns 4j..4j+3 and
+// hd/2 + 4j..+3 of K and of V (four rotate-half pairs of K, whose cos/sin the
+// norm stored per row) and issues all four 16-byte loads before it adds any.
+// 256 threads = 256 / (hd/8) units per CTA.  The k RMSNorm is a shuffle sum
+// over the unit's lanes; each row leaves as two 8-byte stores per lane.
+// Needs hd / 8 a power of two <= 32.
+__global__ void __launch_bounds__(256, 4) epilogue_gqa_wide_kernel(
+    const GemmOut y, const MaskArgs m, const int4 *dst, const float2 *cs,
     const uint16_t *gamma_k, uint16_t *pool, int N, int L, int nkv, int hd, float eps,
     int32_t *ctx_len, int B) {
   griddep_launch();
   griddep_wait();
   if (blockIdx.x == 0) advance_ctx_len(m, ctx_len, B);
   const int lpu = hd >> 3, half = hd >> 1;
-  const int H = L * 2 * nkv;
+  const int H = L * nkv;
   const long long u = static_cast<long long>(blockIdx.x) * (blockDim.x / lpu) + threadIdx.x / lpu;
   const int j = threadIdx.x % lpu;
   if (u >= static_cast<long long>(N) * H) return;  // whole units leave together
-  const int n = static_cast<int>(u / H), head = static_cast<int>(u % H);
-  Vec4Load lo, hi;
-  const int ca = head * hd + 4 * j, cb = ca + half;
-  vec4_issue(y, n, ca, true, lo);
-  vec4_issue(y, n, cb, true, hi);
+  const int n = static_cast<int>(u / H), lh = static_cast<int>(u % H);
+  const int l = lh / nkv, h = lh % nkv;
+  const int ck = ((l * 2) * nkv + h) * hd + 4 * j, cv = ck + nkv * hd;
+  Vec4Load1 kl, kh, vl, vh;
+  vec4_issue1(y, n, ck, true, kl);
+  vec4_issue1(y, n, ck + half, true, kh);
+  vec4_issue1(y, n, cv, true, vl);
+  vec4_issue1(y, n, cv + half, true, vh);
   const int4 d = dst[n];
-  float4 a = vec4_finish(y, n, ca, lo), b = vec4_finish(y, n, cb, hi);
+  // cos/sin of pairs 4j..4j+3 (16-byte aligned: hd/2 is a multiple of 4)
+  const float4 *t = reinterpret_cast<const float4 *>(cs + static_cast<size_t>(n) * half + 4 * j);
+  const float4 c01 = t[0], c23 = t[1];
+  const float4 a = vec4_finish1(y, n, ck, kl), b = vec4_finish1(y, n, ck + half, kh);
+  const float4 va4 = vec4_finish1(y, n, cv, vl), vb4 = vec4_finish1(y, n, cv + half, vh);
   if (d.x < 0) return;
-  const int l = head / (2 * nkv), kv = (head / nkv) & 1, h = head % nkv;
-  if (kv == 0) {
-    const unsigned mask = (lpu == 32 ? 0xffffffffu : ((1u << lpu) - 1u))
-                          << ((threadIdx.x & 31) & ~(lpu - 1));
-    float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
-               b.w * b.w;
-    for (int o = lpu >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
-    const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
-    const uint16_t *gk = gamma_k + static_cast<size_t>(l) * hd;
-    float va[4] = {a.x, a.y, a.z, a.w}, vb[4] = {b.x, b.y, b.z, b.w};
+  const unsigned mask = (lpu == 32 ? 0xffffffffu : ((1u << lpu) - 1u))
+                        << ((threadIdx.x & 31) & ~(lpu - 1));
+  float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
+             b.w * b.w;
+  for (int o = lpu >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+  const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
+  const uint16_t *gk = gamma_k + static_cast<size_t>(l) * hd;
+  float ka[4] = {a.x, a.y, a.z, a.w}, kb[4] = {b.x, b.y, b.z, b.w};
+  const float cv4[4] = {c01.x, c01.z, c23.x, c23.z}, sv4[4] = {c01.y, c01.w, c23.y, c23.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = 4 * j + e;
-      const float k0 = va[e] * inv * bf16_to_f32(gk[c]);
-      const float k1 = vb[e] * inv * bf16_to_f32(gk[c + half]);
-      float cs, sn;
-      rope_cos_sin(d.z, rf.f[c], &cs, &sn);
-      va[e] = k0 * cs - k1 * sn;
-      vb[e] = k1 * cs + k0 * sn;
-    }
-    a = make_float4(va[0], va[1], va[2], va[3]);
-    b = make_float4(vb[0], vb[1], vb[2], vb[3]);
+  for (int e = 0; e < 4; ++e) {
+    const int c = 4 * j + e;
+    const float k0 = ka[e] * inv * bf16_to_f32(gk[c]);
+    const float k1 = kb[e] * inv * bf16_to_f32(gk[c + half]);
+    ka[e] = k0 * cv4[e] - k1 * sv4[e];
+    kb[e] = k1 * cv4[e] + k0 * sv4[e];
   }
-  uint16_t *row =
-      pool + ((((static_cast<size_t>(l) * m.NP + d.x) * 2 + kv) * nkv + h) * m.P + d.y) * hd;
-  *reinterpret_cast<uint2 *>(row + 4 * j) = make_uint2(pack2_bf16(a.x, a.y), pack2_bf16(a.z, a.w));
-  *reinterpret_cast<uint2 *>(row + half + 4 * j) =
-      make_uint2(pack2_bf16(b.x, b.y), pack2_bf16(b.z, b.w));
+  const size_t plane = static_cast<size_t>(nkv) * m.P * hd;  // K -> V of the same page
+  uint16_t *krow =
+      pool + ((((static_cast<size_t>(l) * m.NP + d.x) * 2) * nkv + h) * m.P + d.y) * hd;
+  uint16_t *vrow = krow + plane;
+  *reinterpret_cast<uint2 *>(krow + 4 * j) = make_uint2(pack2_bf16(ka[0], ka[1]), pack2_bf16(ka[2], ka[3]));
+  *reinterpret_cast<uint2 *>(krow + half + 4 * j) =
+      make_uint2(pack2_bf16(kb[0], kb[1]), pack2_bf16(kb[2], kb[3]));
+  *reinterpret_cast<uint2 *>(vrow + 4 * j) =
+      make_uint2(pack2_bf16(va4.x, va4.y), pack2_bf16(va4.z, va4.w));
+  *reinterpret_cast<uint2 *>(vrow + half + 4 * j) =
+      make_uint2(pack2_bf16(vb4.x, vb4.y), pack2_bf16(vb4.z, vb4.w));
 }
 
-// MLA epilogue for many rows: grid (N rows, L), lat/8 latent lanes (columns
-// 4j..+3 and lat/2 + 4j..+3) and rope/8 rope lanes (the same split of the
-// rope part); two 8-byte stores per lane.  Needs lat % 8 == rope % 8 == 0.
+// MLA epilogue for many rows: one warp per (row, layer).  Lane l holds the
+// latent groups g = l + 32k (columns 4g..4g+3 and lat/2 + 4g..+3, k < G) and,
+// for l < rope/8, the rope group l (rope columns 4l..+3 and rope/2 + 4l..+3):
+// rotate-half pairs again.  All loads go out first; the latent RMSNorm is a
+// warp sum; every group leaves as two 8-byte stores.  Needs lat % 8 == rope %
+// 8 == 0 and lat <= 256 G.
+template <int G>
 __global__ void __launch_bounds__(256) epilogue_mla_wide_kernel(
-    const GemmOut y, const MaskArgs m, const int4 *dst, const RopeFreqs rf,
-    const uint16_t *gamma_kv, uint16_t *pool, int L, int lat, int rope, float eps,
+    const GemmOut y, const MaskArgs m, const int4 *dst, const float2 *cs,
+    const uint16_t *gamma_kv, uint16_t *pool, int N, int L, int lat, int rope, float eps,
     int32_t *ctx_len, int B) {
-  __shared__ float red[32];
   griddep_launch();
   griddep_wait();
-  const int n = blockIdx.x, l = blockIdx.y, t = threadIdx.x;
-  if (n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
-  const int W = lat + rope, nl = lat >> 3, nr = rope >> 3;
-  const bool is_lat = t < nl, is_rope = !is_lat && t < nl + nr;
-  const int j = is_lat ? t : t - nl;
-  const int ca = is_lat ? 4 * j : lat + 4 * j;
-  const int cb = ca + (is_lat ? lat >> 1 : rope >> 1);
-  Vec4Load lo, hi;
-  const int ga = l * W + (is_lat || is_rope ? ca : 0), gb = l * W + (is_lat || is_rope ? cb : 0);
-  vec4_issue(y, n, ga, is_lat || is_rope, lo);
-  vec4_issue(y, n, gb, is_lat || is_rope, hi);
+  if (blockIdx.x == 0) advance_ctx_len(m, ctx_len, B);
+  const long long u = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (u >= static_cast<long long>(N) * L) return;  // warp-uniform
+  const int n = static_cast<int>(u / L), l = static_cast<int>(u % L);
+  const int W = lat + rope, hl = lat >> 1, hr = rope >> 1;
+  const int base = l * W;
+  Vec4Load1 la[G], lb[G], ra, rb;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int g = lane + 32 * k;
+    const bool on = g < (lat >> 3);
+    vec4_issue1(y, n, base + (on ? 4 * g : 0), on, la[k]);
+    vec4_issue1(y, n, base + (on ? hl + 4 * g : 0), on, lb[k]);
+  }
+  const bool ron = lane < (rope >> 3);
+  vec4_issue1(y, n, base + (ron ? lat + 4 * lane : 0), ron, ra);
+  vec4_issue1(y, n, base + (ron ? lat + hr + 4 * lane : 0), ron, rb);
   const int4 d = dst[n];
-  float4 a = vec4_finish(y, n, ga, lo), b = vec4_finish(y, n, gb, hi);
-  const float ss = block_sum(is_lat ? a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x +
-                                          b.y * b.y + b.z * b.z + b.w * b.w
-                                    : 0.f,
-                             red);
-  if (d.x < 0 || !(is_lat || is_rope)) return;
-  float va[4] = {a.x, a.y, a.z, a.w}, vb[4] = {b.x, b.y, b.z, b.w};
-  if (is_lat) {
-    const float inv = rsqrtf(ss / static_cast<float>(lat) + eps);
-    const uint16_t *gk = gamma_kv + static_cast<size_t>(l) * lat;
+  float4 c01 = make_float4(0.f, 0.f, 0.f, 0.f), c23 = c01;
+  if (ron) {  // cos/sin of rope pairs 4*lane..+3 (16-byte aligned: rope/2 is a multiple of 4)
+    const float4 *t = reinterpret_cast<const float4 *>(cs + static_cast<size_t>(n) * hr + 4 * lane);
+    c01 = t[0];
+    c23 = t[1];
+  }
+  float4 a[G], b[G];
+  float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      va[e] = va[e] * inv * bf16_to_f32(gk[ca + e]);
-      vb[e] = vb[e] * inv * bf16_to_f32(gk[cb + e]);
-    }
-  } else {
+  for (int k = 0; k < G; ++k) {
+    const int g = lane + 32 * k;
+    const bool on = g < (lat >> 3);
+    a[k] = vec4_finish1(y, n, base + (on ? 4 * g : 0), la[k]);
+    b[k] = vec4_finish1(y, n, base + (on ? hl + 4 * g : 0), lb[k]);
+    ss += a[k].x * a[k].x + a[k].y * a[k].y + a[k].z * a[k].z + a[k].w * a[k].w + b[k].x * b[k].x +
+          b[k].y * b[k].y + b[k].z * b[k].z + b[k].w * b[k].w;
+  }
+  float4 ro = vec4_finish1(y, n, base + (ron ? lat + 4 * lane : 0), ra);
+  float4 rh = vec4_finish1(y, n, base + (ron ? lat + hr + 4 * lane : 0), rb);
+  ss = warp_sum(ss);
+  if (d.x < 0) return;  // warp-uniform
+  uint16_t *row = pool + ((static_cast<size_t>(l) * m.NP + d.x) * m.P + d.y) * W;
+  const float inv = rsqrtf(ss / static_cast<float>(lat) + eps);
+  const uint16_t *gk = gamma_kv + static_cast<size_t>(l) * lat;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float cs, sn;
-      rope_cos_sin(d.z, rf.f[4 * j + e], &cs, &sn);
-      const float x0 = va[e], x1 = vb[e];
-      va[e] = x0 * cs - x1 * sn;
-      vb[e] = x1 * cs + x0 * sn;
+  for (int k = 0; k < G; ++k) {
+    const int g = lane + 32 * k;
+    if (g < (lat >> 3)) {
+      const int c0 = 4 * g, c1 = hl + 4 * g;
+      const float4 x = a[k], z = b[k];
+      *reinterpret_cast<uint2 *>(row + c0) =
+          make_uint2(pack2_bf16(x.x * inv * bf16_to_f32(gk[c0]), x.y * inv * bf16_to_f32(gk[c0 + 1])),
+                     pack2_bf16(x.z * inv * bf16_to_f32(gk[c0 + 2]), x.w * inv * bf16_to_f32(gk[c0 + 3])));
+      *reinterpret_cast<uint2 *>(row + c1) =
+          make_uint2(pack2_bf16(z.x * inv * bf16_to_f32(gk[c1]), z.y * inv * bf16_to_f32(gk[c1 + 1])),
+                     pack2_bf16(z.z * inv * bf16_to_f32(gk[c1 + 2]), z.w * inv * bf16_to_f32(gk[c1 + 3])));
     }
   }
-  uint16_t *row = pool + ((static_cast<size_t>(l) * m.NP + d.x) * m.P + d.y) * W;
-  *reinterpret_cast<uint2 *>(row + ca) = make_uint2(pack2_bf16(va[0], va[1]), pack2_bf16(va[2], va[3]));
-  *reinterpret_cast<uint2 *>(row + cb) = make_uint2(pack2_bf16(vb[0], vb[1]), pack2_bf16(vb[2], vb[3]));
+  if (ron) {
+    float va[4] = {ro.x, ro.y, ro.z, ro.w}, vb[4] = {rh.x, rh.y, rh.z, rh.w};
+    const float cv[4] = {c01.x, c01.z, c23.x, c23.z}, sv[4] = {c01.y, c01.w, c23.y, c23.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = va[e], x1 = vb[e];
+      va[e] = x0 * cv[e] - x1 * sv[e];
+      vb[e] = x1 * cv[e] + x0 * sv[e];
+    }
+    *reinterpret_cast<uint2 *>(row + lat + 4 * lane) =
+        make_uint2(pack2_bf16(va[0], va[1]), pack2_bf16(va[2], va[3]));
+    *reinterpret_cast<uint2 *>(row + lat + hr + 4 * lane) =
+        make_uint2(pack2_bf16(vb[0], vb[1]), pack2_bf16(vb[2], vb[3]));
+  }
 }
 
 // ------------------------------------------------------ GQA epilogue
@@ -725,8 +810,12 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
                              : (g.latent_dim % 8 == 0 && g.rope_dim % 8 == 0));
   RowDest rd;
   rd.dst = wide_epi ? W.dst : nullptr;
+  rd.cs = W.cs;
+  rd.nf = d.nf;
   rd.m = m;
   rd.m.ctx_snap = ctx_len;
+  RopeFreqs rf;
+  fill_rope_freqs(&rf, gqa ? g.head_dim : g.rope_dim, g.rope_theta);
 
   // hidden RMSNorm: a cluster of G CTAs per row for decode-sized row counts,
   // one CTA per row beyond
@@ -744,7 +833,7 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_wide_kernel, y1,
                                 static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
                                 static_cast<float>(g.eps_hidden),
-                                static_cast<const int32_t *>(ctx_len), snap, B, rd)) != cudaSuccess)
+                                static_cast<const int32_t *>(ctx_len), snap, B, rd, rf)) != cudaSuccess)
       return e;
   } else {
     int G = (d.D + 511) / 512;
@@ -777,7 +866,6 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     return e;
 
   // epilogue
-  RopeFreqs rf;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -787,22 +875,25 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   cfg.stream = s;
   uint16_t *pool16 = static_cast<uint16_t *>(pool);
   if (wide_epi && gqa) {
-    fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
-    const long long units = static_cast<long long>(d.N) * g.num_layers * 2 * g.nkv;
+    const long long units = static_cast<long long>(d.N) * g.num_layers * g.nkv;
     const int upc = 256 / lpu;
     cfg.gridDim = dim3(static_cast<unsigned>((units + upc - 1) / upc));
     cfg.blockDim = dim3(256);
     e = cudaLaunchKernelEx(&cfg, epilogue_gqa_wide_kernel, y2, m,
-                           static_cast<const int4 *>(W.dst), rf,
+                           static_cast<const int4 *>(W.dst), static_cast<const float2 *>(W.cs),
                            static_cast<const uint16_t *>(w.gamma_k), pool16, d.N, g.num_layers,
                            g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else if (wide_epi) {
-    fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
-    cfg.gridDim = dim3(d.N, g.num_layers);
-    cfg.blockDim = dim3(((g.latent_dim + g.rope_dim) / 8 + 31) / 32 * 32);
-    e = cudaLaunchKernelEx(&cfg, epilogue_mla_wide_kernel, y2, m,
-                           static_cast<const int4 *>(W.dst), rf,
-                           static_cast<const uint16_t *>(w.gamma_k), pool16, g.num_layers,
+    const long long units = static_cast<long long>(d.N) * g.num_layers;
+    cfg.gridDim = dim3(static_cast<unsigned>((units + 7) / 8));
+    cfg.blockDim = dim3(256);
+    auto kern = g.latent_dim <= 256   ? epilogue_mla_wide_kernel<1>
+                : g.latent_dim <= 512 ? epilogue_mla_wide_kernel<2>
+                : g.latent_dim <= 768 ? epilogue_mla_wide_kernel<3>
+                                      : epilogue_mla_wide_kernel<4>;
+    e = cudaLaunchKernelEx(&cfg, kern, y2, m, static_cast<const int4 *>(W.dst),
+                           static_cast<const float2 *>(W.cs),
+                           static_cast<const uint16_t *>(w.gamma_k), pool16, d.N, g.num_layers,
                            g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k), ctx_len, B);
   } else if (gqa) {
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);

@@ -196,25 +196,31 @@ def test_update_qwen_shapes(dl, name, over):
     (512, 8192, 1, 128, 1, 3, "bf16"),   # 8 CTAs of 1024 columns; fc has 8 K blocks
     (4096, 576, 2, 64, 1, 2, "f32"),     # 2 CTAs of 288 columns: tiles straddle CTAs
     (64, 64, 1, 64, 1, 1, "bf16"),       # one 64-column CTA, one K block
+    (1024, 2560, 4, 64, 2, 20, "bf16"),  # 320 rows: the many-row norm (80 of 96 threads)
+    (512, 1536, 2, 32, 1, 17, "f32"),    # 272 rows, head rows of 4 lanes
 ])
 def test_update_odd_widths(dl, D_in, D, nkv, hd, L, B, hidden):
     """d_model / d_in / stacked K/V widths off the benchmark shapes: every
     cluster layout of the hidden RMSNorm and GEMMs whose tiles are shared by
     few or many CTAs, checked against the oracle."""
+    n_acc = [16 - (3 * b) % 16 for b in range(B)]
     over = dict(D_in=D_in, D=D, nkv=nkv, hq=2 * nkv, hd=hd, L=L, B=B, T=16, hidden_dtype=hidden,
-                ctx=[100 + 7 * b for b in range(B)], n_acc=[16 - 3 * b for b in range(B)],
+                ctx=[100 + 7 * (b % 8) for b in range(B)], n_acc=n_acc,
                 alloc_pages=[12] * B, pool_pages=16 * B, max_pages=16)
     prob = inputs.make_problem(inputs.workload("tiny", **over), seed=11)
     pool_ref, ctx_ref, pool_gpu, ctx_gpu, st = _update_both(dl, prob)
     n = _check_pool(prob, pool_ref, pool_gpu)
-    assert n == sum(16 - 3 * b for b in range(B)) * 2 * nkv * L
+    assert n == sum(n_acc) * 2 * nkv * L
     np.testing.assert_array_equal(ctx_gpu, ctx_ref)
     assert st == 0
 
 
-def test_update_dummies_bad_pages_and_ceiling(dl):
-    prob = inputs.make_problem(inputs.workload("batch_sweep_8"), seed=5)
-    valid = np.array([1, 0, 1, 1, 0, 1, 1, 1], np.uint8)
+@pytest.mark.parametrize("name", ["batch_sweep_8", "batch_sweep_32"])
+def test_update_dummies_bad_pages_and_ceiling(dl, name):
+    # batch 32 = 512 rows: the many-row norm resolves the destinations
+    prob = inputs.make_problem(inputs.workload(name), seed=5)
+    valid = np.ones(prob["B"], np.uint8)
+    valid[[1, 4]] = 0
     tbl = prob["pages"].copy()
     # request 2: its next page points outside the pool -> rows there masked + flag
     c2 = int(prob["ctx_len"][2])

@@ -103,11 +103,12 @@ def test_prefill_tiny_varlen_fp32(dl):
 
 
 def test_prefill_qwen_shape_multi_row_tiles(dl):
-    # 700 rows: the projection GEMMs run three 256-row tiles, the last ragged
-    g, *rest = _case("qwen3_8b", [300, 400], [0, 4096], 2, over={"ctx": [2048]})
+    # 701 rows: the projection GEMMs run three 256-row tiles, the last ragged;
+    # the many-row epilogue pairs rows, and the odd last row has no partner
+    g, *rest = _case("qwen3_8b", [301, 400], [0, 4096], 2, over={"ctx": [2048]})
     n, ctx, _ = _run(dl, g, *rest)
-    assert ctx.tolist() == [300, 4496]
-    assert n == 700 * 2 * g["nkv"] * g["L"]
+    assert ctx.tolist() == [301, 4496]
+    assert n == 701 * 2 * g["nkv"] * g["L"]
 
 
 def test_prefill_mla_single_latent_pool(dl):
