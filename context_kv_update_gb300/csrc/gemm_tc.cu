@@ -20,6 +20,10 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kMaxSmem = 227 * 1024;
+// Ring depth cap.  The weight tiles of the first ring slots are copied before
+// the dependency wait, so a deep ring lets a decode-sized GEMM stream much of
+// its weights while the previous kernel finishes.
+constexpr int kMaxStages = 12;
 
 struct GemmParams {
   int K, ntile, mtiles, kblocks, maxc, stages;
@@ -273,7 +277,7 @@ Schedule make_schedule(int M, int K, int Npad) {
   const long long q = s.units / s.ctas;
   s.maxc = static_cast<int>(std::min<long long>({s.ctas, s.kblocks, s.kblocks / q + 2}));
   const int stage_bytes = static_cast<int>(a_tile_bytes() + b_tile_bytes(s.ntile));
-  s.stages = std::min(8, (kMaxSmem - 2048) / stage_bytes);
+  s.stages = std::min(kMaxStages, (kMaxSmem - 2048) / stage_bytes);
   return s;
 }
 
