@@ -181,35 +181,13 @@ class Step:
         # The per-step inputs a caller uploads live in one device buffer, each
         # at a 256-byte aligned offset, so the end-to-end leg moves them with
         # one host-to-device copy (prob key -> device view).
-        in_keys = ["raw_offsets", "acc", "n_acc", "ctx_len", "hidden"] + (
-            ["q_lat", "q_rope", "blk_lat"] if self.mla else ["q", "blk_k", "blk_v"])
-        self.in_buf, self.in_layout, self.step_inputs = self._pack(
-            {k: np.ascontiguousarray(prob[k]) for k in in_keys})
-        v = self.step_inputs
-        self.raw_offsets, self.acc, self.n_acc = v["raw_offsets"], v["acc"], v["n_acc"]
-        self.ctx_pre = v["ctx_len"]
-        self.ctx_len = self.ctx_pre.clone()
-        self.hidden = v["hidden"]
+        self._make_io()
         self.weights = {k: td(prob[k]) for k in ("w_fc", "g_h", "w_kv", "g_k")}
         self.pool = td(prob["pool"])
-        if self.mla:
-            self.q, self.q_rope, self.blk_k, self.blk_v = v["q_lat"], v["q_rope"], v["blk_lat"], None
-            dv = g["latent"]
-        else:
-            self.q, self.q_rope, self.blk_k, self.blk_v = v["q"], None, v["blk_k"], v["blk_v"]
-            dv = g["hd"]
         self.sinks = td(prob["sinks"]) if prob["use_sinks"] else None
         M = g["max_pages"]
-        self.outs = {}
-        # the outputs read back every step (attention output, advanced
-        # ctx_len) share one device buffer: one device-to-host copy
-        attn_shape = (L, B, T, g["hq"], dv)
-        self.out_buf, _, outv = self._pack(
-            {"attn_out": np.zeros(attn_shape, np.uint16), "ctx_len_new": np.zeros(B, np.int32)})
-        self.attn_out = outv["attn_out"]
         for k in dl.STEP_OUTPUT_FIELDS:
             if k == "ctx_len_new":
-                self.outs[k] = outv[k]
                 continue
             shape = (B, M) if k == "block_table" else (B, T) if k in (
                 "emb_ids", "ctx_pos", "q_pos", "ctx_dst_page", "ctx_dst_slot", "ctx_wmask",
@@ -232,6 +210,43 @@ class Step:
             self.aux = torch.cuda.Stream()
             self.fork_ev = torch.cuda.Event()
             self.join_ev = torch.cuda.Event()
+
+    def _make_io(self):
+        """The step's uploaded inputs and read-back outputs, each packed in
+        one device buffer (so the end-to-end leg moves them with one copy
+        each way), and the typed views the launches use."""
+        prob, g = self.prob, self.g
+        B, T, L = prob["B"], g["T"], g["L"]
+        in_keys = ["raw_offsets", "acc", "n_acc", "ctx_len", "hidden"] + (
+            ["q_lat", "q_rope", "blk_lat"] if self.mla else ["q", "blk_k", "blk_v"])
+        self.in_buf, self.in_layout, self.step_inputs = self._pack(
+            {k: np.ascontiguousarray(prob[k]) for k in in_keys})
+        v = self.step_inputs
+        self.raw_offsets, self.acc, self.n_acc = v["raw_offsets"], v["acc"], v["n_acc"]
+        self.ctx_pre = v["ctx_len"]
+        self.ctx_len = self.ctx_pre.clone()
+        self.hidden = v["hidden"]
+        if self.mla:
+            self.q, self.q_rope, self.blk_k, self.blk_v = v["q_lat"], v["q_rope"], v["blk_lat"], None
+            dv = g["latent"]
+        else:
+            self.q, self.q_rope, self.blk_k, self.blk_v = v["q"], None, v["blk_k"], v["blk_v"]
+            dv = g["hd"]
+        attn_shape = (L, B, T, g["hq"], dv)
+        self.out_buf, _, outv = self._pack(
+            {"attn_out": np.zeros(attn_shape, np.uint16), "ctx_len_new": np.zeros(B, np.int32)})
+        self.attn_out = outv["attn_out"]
+        self.outs = dict(getattr(self, "outs", {}))
+        self.outs["ctx_len_new"] = outv["ctx_len_new"]
+
+    def twin(self):
+        """A step over the same pool, weights, workspaces and bookkeeping
+        buffers with its own input and output buffers: two of them let the
+        end-to-end leg copy one step's data while the other step computes."""
+        import copy
+        t = copy.copy(self)
+        t._make_io()
+        return t
 
     @staticmethod
     def _pack(arrays):
@@ -489,52 +504,106 @@ def attention_steady_state(dl, step, stream, rounds=5):
 
 def run_e2e(dl, step, stream, steps):
     """Same step through the public API with inputs from pinned host memory
-    and the outputs read back every step (copies inside the timed region)."""
+    and the outputs read back every step (copies inside the timed region).
+
+    value: steps in flight two at a time.  Two input / output buffer pairs
+    alternate: a copy stream uploads step i + 1's inputs and reads back step
+    i - 1's outputs while step i computes (step i + 2's upload waits until
+    step i is done with the buffer).  serial_value: one buffer pair, upload,
+    compute and read-back of each step back to back.  eager_value: the serial
+    form with every C-ABI call launched from the host (no graph)."""
     import torch
     prob = step.prob
-    # the step's inputs, packed on the host as the device buffer holds them
-    host_in = torch.zeros(step.in_buf.numel(), dtype=torch.uint8).pin_memory()
-    hv = host_in.numpy()
-    for k, (o, n) in step.in_layout.items():
-        hv[o:o + n] = np.frombuffer(np.ascontiguousarray(prob[k]).tobytes(), np.uint8)
-    out_host = torch.empty(step.out_buf.numel(), dtype=torch.uint8).pin_memory()
-    h2d = host_in.numel()
-    d2h = out_host.numel()
+    pair = [step, step.twin()]
+    host_in, host_out = [], []
+    for st_ in pair:
+        hin = torch.zeros(st_.in_buf.numel(), dtype=torch.uint8).pin_memory()
+        hv = hin.numpy()
+        for k, (o, n) in st_.in_layout.items():
+            hv[o:o + n] = np.frombuffer(np.ascontiguousarray(prob[k]).tobytes(), np.uint8)
+        host_in.append(hin)
+        host_out.append(torch.empty(st_.out_buf.numel(), dtype=torch.uint8).pin_memory())
+    h2d = host_in[0].numel()
+    d2h = host_out[0].numel()
 
     def one():
-        step.in_buf.copy_(host_in, non_blocking=True)
+        step.in_buf.copy_(host_in[0], non_blocking=True)
         step.run()
-        out_host.copy_(step.out_buf, non_blocking=True)
+        host_out[0].copy_(step.out_buf, non_blocking=True)
+
+    copy_stream = torch.cuda.Stream()
+    n_pipe = 10
+
+    def pipelined(n):
+        comp = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(comp)
+        copy_stream.wait_event(fork)
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_done = [torch.cuda.Event() for _ in range(n)]
+
+        def upload(i):
+            with torch.cuda.stream(copy_stream):
+                pair[i % 2].in_buf.copy_(host_in[i % 2], non_blocking=True)
+                ev_in[i].record(copy_stream)
+
+        upload(0)
+        if n > 1:
+            upload(1)
+        for i in range(n):
+            comp.wait_event(ev_in[i])
+            pair[i % 2].run()
+            ev_done[i].record(comp)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(ev_done[i])
+                host_out[i % 2].copy_(pair[i % 2].out_buf, non_blocking=True)
+            if i + 2 < n:
+                upload(i + 2)
+        join = torch.cuda.Event()
+        join.record(copy_stream)
+        comp.wait_event(join)
+
+    def timed(fn, reps, per):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) * 1000.0 / (reps * per)
 
     with torch.cuda.stream(stream):
         one()
+        pipelined(2)
     torch.cuda.synchronize()
-    gr = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gr, stream=stream):
+    g_one, g_pipe = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_one, stream=stream):
         one()
-    for _ in range(5):
-        gr.replay()
+    with torch.cuda.graph(g_pipe, stream=stream):
+        pipelined(n_pipe)
+    for _ in range(3):
+        g_one.replay()
+        g_pipe.replay()
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
+    reps = max(1, steps // n_pipe)
+    us = timed(g_pipe.replay, reps, n_pipe)
+    serial = timed(g_one.replay, steps, 1)
+    eager = timed(one, steps, 1)
+    # the pipelined leg read back the right thing
     with torch.cuda.stream(stream):
-        for _ in range(steps):
-            gr.replay()
-    e.record(stream)
+        g_pipe.replay()
     torch.cuda.synchronize()
-    us = s.elapsed_time(e) * 1000.0 / steps
-    # the same step enqueued eagerly (every C-ABI call from the host, no graph)
-    s.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            one()
-    e.record(stream)
-    torch.cuda.synchronize()
-    eager = s.elapsed_time(e) * 1000.0 / steps
+    same = bool(torch.equal(host_out[0], host_out[1]))
     return {"value": round(us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps, "timing": "CUDA-graph replay",
+            "d2h_bytes_per_step": int(d2h), "steps": reps * n_pipe,
+            "timing": f"CUDA-graph replay of {n_pipe} steps, two in flight (uploads and "
+                      "read-backs on a copy stream beside the compute)",
+            "serial_value": round(serial, 2),
+            "serial_timing": "CUDA-graph replay of one step: upload, compute, read-back",
             "eager_value": round(eager, 2),
-            "eager_timing": "the same calls launched from the host each step (no graph)"}
+            "eager_timing": "the serial step launched from the host each step (no graph)",
+            "pair_outputs_equal": same}
 
 
 def run_kernel_only(args):
