@@ -293,6 +293,53 @@ def _peak_mla(ql, qr, pool, tbl, kv_len, g, layer, window, seed, frac=0.5, gain=
     return ql, qr
 
 
+def _mla_case(seed, kv_lens, *, hq, P, Tq, L=1, lat=512, rope=64):
+    rng = np.random.default_rng(seed)
+    B = len(kv_lens)
+    M = max(-(-k // P) for k in kv_lens) + 2
+    NP = sum(-(-k // P) for k in kv_lens) + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    tbl = np.zeros((B, M), np.int32)
+    pos = 0
+    for r, k in enumerate(kv_lens):
+        n = -(-k // P)
+        tbl[r, :n] = perm[pos:pos + n]
+        pos += n
+    pool = inputs.f32_to_bf16_bits(rng.standard_normal((L, NP, P, lat + rope), dtype=np.float32))
+    ql = inputs.f32_to_bf16_bits(rng.standard_normal((B, Tq, hq, lat), dtype=np.float32))
+    qr = inputs.f32_to_bf16_bits(rng.standard_normal((B, Tq, hq, rope), dtype=np.float32))
+    sinks = rng.standard_normal(hq).astype(np.float32)
+    g = dict(kind="mla", L=L, D_in=64, D=64, hq=hq, nkv=1, hd=lat + rope, latent=lat,
+             rope_dim=rope, P=P, T=Tq, max_pages=M, num_pool_pages=NP, rope_theta=1e6,
+             eps_h=1e-6, eps_k=1e-6)
+    return g, pool, tbl, ql, qr, sinks
+
+
+@pytest.mark.parametrize("P,Tq,hq,S,mode,window", [
+    (64, 8, 64, 0, 0, 0),
+    (16, 3, 16, 0, 1, 0),      # 4 boxes per chunk of a 64-key half-tile; 48 of 64 rows real
+    (128, 1, 64, 0, 1, 300),   # half-tiles at either half of a 128-key page
+    (32, 5, 32, 1, 0, 0),      # one segment: every half-tile through one CTA
+    (64, 2, 64, 3, 1, 90),
+    (8, 8, 24, 50, 0, 0),      # more segments than tiles; 8 boxes per chunk
+    (64, 16, 64, 0, 1, 0),     # 1024 query rows: 16 row tiles
+])
+def test_attention_mla_pages_batches_segments(dl, P, Tq, hq, S, mode, window):
+    """MLA latent attention on small cases across page sizes, query counts,
+    segment counts and requests whose context ends in the first half of a
+    128-key tile (1, 64, 190), in its second half (65, 130, 1000) or on a tile
+    boundary (256)."""
+    kv_lens = [1, 64, 65, 130, 190, 256, 1000]
+    g, pool, tbl, ql, qr, sinks = _mla_case(P * 31 + Tq + S, kv_lens, hq=hq, P=P, Tq=Tq)
+    scale = inputs.attention_scale(g)
+    ref = oracle.attention_mla(g, 0, ql, qr, pool, tbl, np.array(kv_lens), window=window,
+                               sinks=sinks, scale=scale, mask_mode=mode)
+    got, st = _run_gpu(dl, g, 0, ql, pool, tbl, kv_lens, window=window, sinks=sinks,
+                       mask_mode=mode, S=S, q_rope=qr, scale=scale)
+    assert_close(got, ref, f"mla P={P} Tq={Tq} hq={hq} S={S} mode={mode} window={window}")
+    assert st == 0
+
+
 @pytest.mark.parametrize("ctx,mode,window,sinks,heads,peaked", [
     (300, 0, 0, False, None, False),
     (4096, 0, 0, False, None, False),
