@@ -319,11 +319,14 @@ class Step:
                 events[layer][1].record()
 
 
-def kernel_launches_per_step(g, hidden_is_f32=False, split_update=False) -> int:
+def kernel_launches_per_step(g, hidden_is_f32=False, split_update=False, B=1) -> int:
     # bookkeeping 1; update: fc gemm, hidden norm, kv gemm, epilogue = 4 (+ the
-    # fp32 -> bf16 prep for fp32 hidden; + the commit when split); per layer:
-    # scatter 1 + attention (split + merge) 2
-    return 1 + 4 + (1 if hidden_is_f32 else 0) + (1 if split_update else 0) + g["L"] * 3
+    # fp32 -> bf16 prep for fp32 hidden; + the commit when split; + the row
+    # set-up of the many-row epilogue beyond 256 rows); per layer: scatter 1 +
+    # attention (split + merge) 2
+    many = B * g["T"] > 256 and not split_update
+    return (1 + 4 + (1 if hidden_is_f32 else 0) + (1 if split_update else 0) + (1 if many else 0)
+            + g["L"] * 3)
 
 
 def make_events(n_layers, count):
@@ -1013,7 +1016,7 @@ def main():
         "clocks": res["clocks"],
         "e2e": res["e2e"],
         "gpu_launches": kernel_launches_per_step(
-            g, prob["hidden"].dtype == np.float32, args.split_update) * args.steps,
+            g, prob["hidden"].dtype == np.float32, args.split_update, prob["B"]) * args.steps,
         "device_status": res["status"],
     }
     if not args.no_cpu_baseline and headline:

@@ -338,17 +338,44 @@ struct RowDest {
   MaskArgs m;    // ctx_snap = the live ctx_len (nothing advances it before the epilogue)
 };
 
+// Row set-up of the many-row epilogue, the first launch of the chain: one
+// warp per GEMM row resolves the row's destination (request by binary search
+// of cu_rows, write rule, page lookup) and stores the row's RoPE cos/sin for
+// every rotate-half pair (the angle formed in double precision, once per row
+// instead of once per head and layer).  It reads only the call's index
+// inputs, so the fc GEMM streams its weights meanwhile.
+__global__ void __launch_bounds__(256) row_setup_kernel(const RowDest rd, const RopeFreqs rf,
+                                                        int N) {
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;  // warp-uniform
+  int pos = -1;
+  if (lane == 0) {
+    int r, i, page = 0, slot = 0, p = 0;
+    const bool w = row_of(rd.m, n, &r, &i) && ctx_row_dest(rd.m, r, i, &page, &slot, &p, true);
+    rd.dst[n] = make_int4(w ? page : -1, slot, p, 0);
+    pos = w ? p : -1;
+  }
+  pos = __shfl_sync(0xffffffffu, pos, 0);
+  if (pos < 0) return;
+  for (int f = lane; f < rd.nf; f += 32) {
+    float c, sn;
+    rope_cos_sin(pos, rf.f[f], &c, &sn);
+    rd.cs[static_cast<size_t>(n) * rd.nf + f] = make_float2(c, sn);
+  }
+}
+
 // hn = bf16(bf16(Y1 row) * gamma_h / rms), one CTA of D/32 threads per row:
 // thread t holds the 8-column groups t + k*D/32, k < 4, two float4 loads per
-// partial.  CTA 0 snapshots ctx_len; thread 0 of each CTA resolves the row's
-// destination when the wide epilogue follows.
+// partial.  CTA 0 snapshots ctx_len.
 constexpr int kWideNormGroups = 4;
 
 __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
     const GemmOut y, const uint16_t *gamma, uint16_t *hn, int D, float eps,
-    const int32_t *ctx_len, int32_t *ctx_snap, int B, const RowDest rd, const RopeFreqs rf) {
+    const int32_t *ctx_len, int32_t *ctx_snap, int B) {
   __shared__ float red[32];
-  __shared__ int s_pos;
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x, tid = threadIdx.x;
@@ -363,12 +390,6 @@ __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
     vec4_issue(y, n, col, act, ld[k][0]);
     vec4_issue(y, n, col + 4, act, ld[k][1]);
   }
-  if (rd.dst && tid == 0) {
-    int r, i, page = 0, slot = 0, pos = 0;
-    const bool w = row_of(rd.m, n, &r, &i) && ctx_row_dest(rd.m, r, i, &page, &slot, &pos, true);
-    rd.dst[n] = make_int4(w ? page : -1, slot, pos, 0);
-    s_pos = w ? pos : -1;
-  }
   float h[kWideNormGroups][8];
   float ss = 0.f;
 #pragma unroll
@@ -382,16 +403,8 @@ __global__ void __launch_bounds__(256) hidden_norm_wide_kernel(
       ss += h[k][e] * h[k][e];
     }
   }
-  const float tot = block_sum(ss, red);  // its barriers also publish s_pos
+  const float tot = block_sum(ss, red);
   const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
-  // the row's RoPE cos/sin, once per (row, pair) for every head and layer
-  // of the epilogue (the angle is formed in double precision)
-  if (rd.dst && s_pos >= 0)
-    for (int f = tid; f < rd.nf; f += blockDim.x) {
-      float c, sn;
-      rope_cos_sin(s_pos, rf.f[f], &c, &sn);
-      rd.cs[static_cast<size_t>(n) * rd.nf + f] = make_float2(c, sn);
-    }
   if (!act) return;
   const bool g16 = (reinterpret_cast<uintptr_t>(gamma) & 15u) == 0;
 #pragma unroll
@@ -744,7 +757,9 @@ size_t ctx_workspace_bytes(const dflash_geom &g, int B) { return ctx_ws_map(g, B
 
 namespace {
 
-// The launch chain prep -> fc GEMM -> hidden norm -> K/V GEMM -> epilogue.
+// The launch chain [row set-up] -> [prep] -> fc GEMM -> hidden norm -> K/V GEMM
+// -> epilogue (the row set-up for the many-row epilogue, the prep for fp32
+// hidden rows).
 // staged == nullptr: the fused update.  Otherwise the projection half of a
 // split update: the norm records the pre-step ctx_len in staged_c and the
 // epilogue writes every row's values to staged (mask arguments unused).
@@ -761,34 +776,7 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   int32_t *snap = split ? staged_c : W.ctx_snap;
   cudaError_t e;
 
-  // prep: fp32 hidden -> bf16
-  const bool f32 = hidden_dtype == DFLASH_DTYPE_F32;
-  if (f32) {
-    const int threads = 256;
-    int blocks = (d.Npad * d.D_in + threads - 1) / threads;
-    if (blocks > 4 * device_sm_count()) blocks = 4 * device_sm_count();
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(blocks);
-    cfg.blockDim = dim3(threads);
-    cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, prep_kernel, static_cast<const float *>(hidden), W.x,
-                                d.N * d.D_in, d.D_in, d.Npad)) != cudaSuccess)
-      return e;
-  }
-  const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
-
-  // fc GEMM
-  GemmOut y1, y2;
-  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, st,
-                       /*pdl=*/true, s, &y1)) != cudaSuccess)
-    return e;
-
-  // epilogue arguments (the norm resolves row destinations with them)
+  // epilogue arguments (the row set-up resolves row destinations with them)
   MaskArgs m;
   m.n_acc = n_acc;
   m.ctx_snap = snap;
@@ -817,6 +805,47 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   RopeFreqs rf;
   fill_rope_freqs(&rf, gqa ? g.head_dim : g.rope_dim, g.rope_theta);
 
+  // row set-up of the many-row epilogue (destinations, RoPE cos/sin)
+  if (wide_epi) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((d.N + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, row_setup_kernel, rd, rf, d.N)) != cudaSuccess) return e;
+  }
+
+  // prep: fp32 hidden -> bf16
+  const bool f32 = hidden_dtype == DFLASH_DTYPE_F32;
+  if (f32) {
+    const int threads = 256;
+    int blocks = (d.Npad * d.D_in + threads - 1) / threads;
+    if (blocks > 4 * device_sm_count()) blocks = 4 * device_sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, prep_kernel, static_cast<const float *>(hidden), W.x,
+                                d.N * d.D_in, d.D_in, d.Npad)) != cudaSuccess)
+      return e;
+  }
+  const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
+
+  // fc GEMM
+  GemmOut y1, y2;
+  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, st,
+                       /*pdl=*/true, s, &y1)) != cudaSuccess)
+    return e;
+
   // hidden RMSNorm: a cluster of G CTAs per row for decode-sized row counts,
   // one CTA per row beyond
   if (wide) {
@@ -833,7 +862,7 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_wide_kernel, y1,
                                 static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
                                 static_cast<float>(g.eps_hidden),
-                                static_cast<const int32_t *>(ctx_len), snap, B, rd, rf)) != cudaSuccess)
+                                static_cast<const int32_t *>(ctx_len), snap, B)) != cudaSuccess)
       return e;
   } else {
     int G = (d.D + 511) / 512;

@@ -33,6 +33,9 @@ def test_headline_bytes_per_call():
     # QK and PV: 2 FLOPs per multiply-add, 16 tokens x 32 heads, 128 dims each
     assert flops == 2 * 2 * kv * (16 * 32) * 128
     assert bench.kernel_launches_per_step(g) == 1 + 4 + 5 * 3
+    # beyond 256 update rows the many-row epilogue adds its row set-up launch
+    assert bench.kernel_launches_per_step(g, B=16) == 1 + 4 + 5 * 3
+    assert bench.kernel_launches_per_step(g, B=17) == 1 + 4 + 1 + 5 * 3
 
 
 def test_sliding_window_reads_only_the_window():
