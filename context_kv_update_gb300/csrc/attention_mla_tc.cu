@@ -28,12 +28,13 @@
 // memory: Q (9 chunks of 64 rows x 64 dims, 72 KB), two half-tile buffers of
 // 9 chunks of 64 keys x 64 dims (72 KB each), P^T (8 KB).
 //
-// The softmax warps hold one key per thread (lanes 0-15 of each warp, the
-// lanes the M = 64 result occupies) and 64 row scores.  They keep a per-row
-// reference maximum m_ref in shared memory and only rebuild it (an exact
-// cross-lane maximum, O^T and the row-sum partials rescaled) when some score
-// of the half-tile exceeds m_ref by more than 2^8 -- on the first one and
-// rarely after.  P = exp2(s - m_ref) goes to shared memory as the PV operand
+// The softmax warps read one key per lane from lanes 0-15 of each warp (the
+// lanes the M = 64 result occupies); lane l keeps the key's rows 0-31 and
+// hands rows 32-63 to lane l + 16, so every lane scores 32 rows.  They keep a
+// per-row reference maximum m_ref in shared memory and only rebuild it (an
+// exact cross-lane maximum, O^T and the row-sum partials rescaled) when some
+// score of the half-tile exceeds m_ref by more than 2^8 -- on the first one
+// and rarely after.  P = exp2(s - m_ref) goes to shared memory as the PV operand
 // once the previous PV has read it; each thread accumulates its key's share
 // of the row sums, reduced across the keys once at the end.
 //
@@ -92,17 +93,17 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int unit16) {
   return static_cast<uint32_t>(row * 128 + ((unit16 ^ (row & 7)) << 4));
 }
 
-// Reduce 64 per-lane values across the warp, one row per value: after five
-// exchange steps (32 + 16 + 8 + 4 + 2 shuffles instead of 5 per row) lane L
-// holds the results of rows 2L and 2L + 1 in v[0], v[1] (at the step that
-// exchanges lane bit o, the lane with that bit set keeps the upper half).
-// MAX selects fmaxf, else addition.
+// Reduce 32 per-lane values over each 16-lane half of the warp, one row per
+// value: after four exchange steps (16 + 8 + 4 + 2 shuffles instead of 4 per
+// row) lane L holds the results of rows 2(L mod 16) and 2(L mod 16) + 1 of its
+// half in v[0], v[1] (at the step that exchanges lane bit o, the lane with
+// that bit set keeps the upper half).  MAX selects fmaxf, else addition.
 template <bool MAX>
-__device__ __forceinline__ void warp_transpose_reduce64(float (&v)[64], int lane) {
+__device__ __forceinline__ void half_warp_transpose_reduce32(float (&v)[32], int lane) {
 #pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int o = 16 >> st;      // lane bit exchanged at this step
-    const int half = 32 >> st;   // values kept per lane after the step
+  for (int st = 0; st < 4; ++st) {
+    const int o = 8 >> st;       // lane bit exchanged at this step
+    const int half = 16 >> st;   // values kept per lane after the step
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int j = 0; j < half; ++j) {
@@ -354,10 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax (warps 4-7)
     // The M = 64 result puts key 16*q4 + l of the half-tile in TMEM lane
-    // 32*q4 + l (l < 16); lanes 16-31 of each warp carry no key.
+    // 32*q4 + l (l < 16); lanes 16-31 of each warp carry no key.  Lane l keeps
+    // rows 0-31 of key 16*q4 + l and hands rows 32-63 to lane l + 16, so every
+    // lane scores 32 rows of one key.
     const int q4 = warp & 3;
-    const bool act = lane < 16;
-    const int key = 16 * q4 + lane;  // valid when act
+    const int hf = lane >> 4;               // this lane's rows: 32*hf .. 32*hf + 31
+    const int key = 16 * q4 + (lane & 15);  // the half-tile key they belong to
+    constexpr int kR = kRowsN / 2;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     // visible key range of a query token
     auto lo_of = [&](int i) {
@@ -372,47 +376,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_first = R0 / p.hq, i_last = max(R_last, R0) / p.hq;
     const int lo_max = lo_of(i_last), hi_min = hi_of(i_first);
     int cur = 0;  // m_ref buffer in use
-    float lp[kRowsN];
+    float lp[kR];
 #pragma unroll
-    for (int c = 0; c < kRowsN; ++c) lp[c] = 0.f;
+    for (int c = 0; c < kR; ++c) lp[c] = 0.f;
     bool bad = false;
     for (int h = 0; h < nh; ++h) {
       const bool got = __all_sync(0xffffffffu,
                                   ptx::mbar_wait(ptx::smem_u32(&s_full[h & 1]),
                                                  static_cast<uint32_t>((h >> 1) & 1), abort_flag));
-      float sv[kRowsN];
+      float sv[kR];
       if (got) {
         ptx::tc_fence_after();
         const uint32_t sa = tm_s + lane_off + (h & 1) * (2 * kRowsN);
-        ptx::tmem_ld64f_sync(sa, sv);
+        float sf[kRowsN];
+        ptx::tmem_ld64f_sync(sa, sf);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float s2[32];
           ptx::tmem_ld32f_sync(sa + kRowsN + 32 * hh, s2);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sv[32 * hh + c] += s2[c];
+          for (int c = 0; c < 32; ++c) sf[32 * hh + c] += s2[c];
         }
-      }
-      if (!got || !act) {
 #pragma unroll
-        for (int c = 0; c < kRowsN; ++c) sv[c] = -INFINITY;
+        for (int c = 0; c < kR; ++c) {
+          const float up = __shfl_sync(0xffffffffu, sf[kR + c], lane & 15);
+          sv[c] = hf ? up : sf[c];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kR; ++c) sv[c] = -INFINITY;
       }
       const int tile0 = kbase_of(h);
       const int kpos = tile0 + key;
-      if (act && !(tile0 >= lo_max && tile0 + kHK - 1 <= hi_min)) {
+      if (!(tile0 >= lo_max && tile0 + kHK - 1 <= hi_min)) {
         // a half-tile some row sees only in part (or past kv_len): mask per row
 #pragma unroll
-        for (int c = 0; c < kRowsN; ++c) {
-          const int R = R0 + c;
+        for (int c = 0; c < kR; ++c) {
+          const int R = R0 + kR * hf + c;
           const int i = R / p.hq;
           if (R > R_last || kpos < lo_of(i) || kpos > hi_of(i)) sv[c] = -INFINITY;
         }
       }
-      const float *mr = m_ref + 64 * cur;
+      const float *mr = m_ref + 64 * cur;  // all 64 rows
+      const float *mrh = mr + kR * hf;    // this lane's rows
       bool need = false;
 #pragma unroll
-      for (int c4 = 0; c4 < kRowsN / 4; ++c4) {
-        const float4 m4 = *reinterpret_cast<const float4 *>(mr + 4 * c4);
+      for (int c4 = 0; c4 < kR / 4; ++c4) {
+        const float4 m4 = *reinterpret_cast<const float4 *>(mrh + 4 * c4);
         need |= sv[4 * c4] * P.scale_log2 > m4.x + 8.f;
         need |= sv[4 * c4 + 1] * P.scale_log2 > m4.y + 8.f;
         need |= sv[4 * c4 + 2] * P.scale_log2 > m4.z + 8.f;
@@ -439,11 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- rebuild m_ref: exact half-tile maxima, rescale O^T and the row sums
         ptx::tc_fence_after();
         {
-          float mx[kRowsN];
+          float mx[kR];
 #pragma unroll
-          for (int c = 0; c < kRowsN; ++c) mx[c] = sv[c];
-          warp_transpose_reduce64<true>(mx, lane);
-          const int row0 = 2 * lane;
+          for (int c = 0; c < kR; ++c) mx[c] = sv[c];
+          half_warp_transpose_reduce32<true>(mx, lane);
+          const int row0 = kR * hf + 2 * (lane & 15);
           xm[row0 * 4 + q4] = mx[0];
           xm[(row0 + 1) * 4 + q4] = mx[1];
         }
@@ -458,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::bar_sync(2, 128);
 #pragma unroll
-        for (int c = 0; c < kRowsN; ++c) {
-          const float old = mr[c], nw = mn[c];
+        for (int c = 0; c < kR; ++c) {
+          const float old = mr[kR * hf + c], nw = mn[kR * hf + c];
           lp[c] *= (old == -INFINITY || old == nw) ? 1.f : ptx::ex2(old - nw);
         }
         if (h > 0) {
@@ -480,12 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cur ^= 1;
       }
-      // P = exp2(s - m_ref) in place (row sums as it goes), then -> P^T row
-      // `key` (64 rows = 8 units of 8) once the previous PV is done
-      if (act) {
-        const float *m2 = m_ref + 64 * cur;
+      // P = exp2(s - m_ref) in place (row sums as it goes), then -> units
+      // 4*hf .. 4*hf+3 of P^T row `key` (64 rows = 8 units of 8) once the
+      // previous PV is done
+      {
+        const float *m2 = m_ref + 64 * cur + kR * hf;
 #pragma unroll
-        for (int c4 = 0; c4 < kRowsN / 4; ++c4) {
+        for (int c4 = 0; c4 < kR / 4; ++c4) {
           const float4 m4 = *reinterpret_cast<const float4 *>(m2 + 4 * c4);
           const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
@@ -502,15 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad = true;  // the next half-tile's barrier (or the epilogue's) carries it
         continue;
       }
-      if (act) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t pk[4];
+      for (int u = 0; u < 4; ++u) {
+        uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) pk[e] = ptx::pack_bf16x2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
-          *reinterpret_cast<uint4 *>(sPT + sw128_off(key, u)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        for (int e = 0; e < 4; ++e) pk[e] = ptx::pack_bf16x2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
+        *reinterpret_cast<uint4 *>(sPT + sw128_off(key, 4 * hf + u)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -528,9 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool any_bad = ptx::bar_or(2, 128, !okf && nh > 0);
     // the P^T region is idle from here (the last PV is done, or the CTA is
     // winding down and writes no partial)
-    warp_transpose_reduce64<false>(lp, lane);
+    half_warp_transpose_reduce32<false>(lp, lane);
     if (!any_bad) {
-      const int row0 = 2 * lane;
+      const int row0 = kR * hf + 2 * (lane & 15);
       xl[row0 * 4 + q4] = lp[0];
       xl[(row0 + 1) * 4 + q4] = lp[1];
       // per-row workspace offsets, computed once
