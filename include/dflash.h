@@ -471,9 +471,9 @@ DFLASH_API size_t dflash_attention_workspace_bytes(const dflash_geom *g, int B, 
  * Key j lives at page block_table[r, j/P], slot j%P of layer `layer`.
  * The visible span [lo_0, hi_{Tq-1}] is cut into num_segments slices of whole
  * 128-key tiles; each (request, kv head, slice) CTA -- one per 128 query rows
- * of the kv head's group, rows being (token, head) pairs -- writes a partial
- * (max, sum, weighted values) to the workspace and a second pass merges them
- * (log-sum-exp) with the sink.
+ * (64 for MLA) of the kv head's group, rows being (token, head) pairs --
+ * writes a partial (max, sum, weighted values) to the workspace and a second
+ * pass merges them (log-sum-exp) with the sink.
  *
  * GQA: q device bf16 [B, Tq, hq, head_dim]; q_rope NULL; out bf16
  *      [B, Tq, hq, head_dim].
