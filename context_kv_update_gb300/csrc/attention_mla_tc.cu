@@ -85,6 +85,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 struct MlaParams {
   AttnParams a;
   int GT, RT, box_rows;
+  int skip_h;  // tests only: the producer never issues this half-tile (-1: off)
   uint32_t idesc_qk, idesc_pv;
   float scale_log2;
 };
@@ -242,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[b]), kBufBytes);
+      const bool skip = h == P.skip_h;
+      if (lane == 0 && !skip) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[b]), kBufBytes);
       __syncwarp();
       const int kbase = kbase_of(h);
       uint8_t *buf = sBuf + b * kBufBytes;
@@ -251,14 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jj = j0 + lane;
         const int c = (jj < nb ? jj : 0) / bph, bx = (jj < nb ? jj : 0) % bph;
         const int page = __shfl_sync(0xffffffffu, cur, hb * bph + bx);
-        if (jj < nb) {
+        if (jj < nb && !skip) {
           const int key0 = kbase + bx * P.box_rows;
           const long long row0 = (static_cast<long long>(p.layer) * p.NP + page) * p.P + key0 % p.P;
           ptx::tma_load_2d(ptx::smem_u32(buf + c * kChunkBytes + bx * P.box_rows * 128), &tm,
                            c * 64, static_cast<int32_t>(row0), ptx::smem_u32(&full[b]));
         }
       }
-      last_fill[b] = h;
+      if (!skip) last_fill[b] = h;
     }
     if (!ok && lane == 0) {
       // let the copies in flight land before the CTA exits
@@ -619,6 +621,8 @@ cudaError_t launch_attn_mla_tc(const AttnParams &a, const dflash_geom &g, cudaSt
   P.GT = a.Tq * a.hq;
   P.RT = (P.GT + kRowsN - 1) / kRowsN;
   P.box_rows = a.P < kHK ? a.P : kHK;
+  const int skip_tile = attention_test_skip_tile_value();
+  P.skip_h = skip_tile >= 0 ? 2 * skip_tile : -1;
   P.idesc_qk = ptx::idesc_bf16_f32(kHK, kRowsN, false, false);
   P.idesc_pv = ptx::idesc_bf16_f32(128, kRowsN, true, true);
   P.scale_log2 = a.scale * 1.4426950408889634f;

@@ -690,6 +690,7 @@ thread_local int t_skip_tile = -1;
 }  // namespace
 
 void attention_test_skip_tile(int tile) { t_skip_tile = tile; }
+int attention_test_skip_tile_value() { return t_skip_tile; }
 
 cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream_t s) {
   TcParams P;

@@ -152,6 +152,7 @@ cudaError_t launch_embedding_gather(int n, const int32_t *ids, const void *table
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq);
 void attention_test_skip_tile(int tile);
+int attention_test_skip_tile_value();  // the calling thread's setting (-1: off)
 float default_attention_scale(const dflash_geom &g);
 int attention_args_status(const dflash_geom *g, int B, int layer, int Tq, const void *q_rope,
                           int32_t window, float *scale, int mask_mode, int num_segments);

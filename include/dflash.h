@@ -541,9 +541,10 @@ DFLASH_API size_t dflash_block_attention_noalloc_max_scratch_bytes(void);
 
 /* ---------------------------------------------------------------------
  * dflash_test_attention_skip_tile -- for tests of the bounded-wait path only.
- * While set (tile >= 0), every GQA dflash_block_attention launched from the
- * calling host thread leaves key tile `tile` of each CTA's segment unloaded:
- * the wait for it runs out (about 2 s), the kernel winds down, ORs
+ * While set (tile >= 0), every dflash_block_attention launched from the
+ * calling host thread leaves key tile `tile` of each CTA's segment unloaded
+ * (MLA: the first 64-key half of it): the wait for it runs out (about 2 s),
+ * the kernel winds down, ORs
  * DFLASH_DEV_WAIT_TIMEOUT into *dev_status and the context stays usable.
  * tile < 0 turns it off (the default).  Never set it in production.
  * ------------------------------------------------------------------- */
