@@ -631,7 +631,7 @@ cudaError_t launch_attn_mla_tc(const AttnParams &a, const dflash_geom &g, cudaSt
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, kWidth, kWidth, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit(attn_mla_tc_kernel, 227 * 1024)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_mla_tc_kernel>(227 * 1024)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, 1, a.B);

@@ -723,7 +723,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit(attn_tc_kernel, kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel>(kSmemMax)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, a.nkv, a.B);

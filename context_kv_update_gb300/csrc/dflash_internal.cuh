@@ -82,14 +82,17 @@ int device_sm_count();
 
 // Raise a kernel's dynamic shared-memory limit once per device (before any
 // graph capture the first eager call does it; later calls only read a flag).
-template <typename Kernel>
-cudaError_t ensure_smem_limit(Kernel k, int bytes) {
+// The kernel is a template argument so that every kernel -- also two
+// instantiations of one kernel template, which share a type -- has its own
+// flag.
+template <auto Kernel>
+cudaError_t ensure_smem_limit(int bytes) {
   static bool done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }

@@ -347,7 +347,7 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
 
   const size_t smem = 1024 + static_cast<size_t>(s.stages) * (a_tile_bytes() + b_tile_bytes(s.ntile)) +
                       (2 * s.stages + 5) * 8 + 32;
-  if ((e = ensure_smem_limit(gemm_tc_kernel, kMaxSmem)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<gemm_tc_kernel>(kMaxSmem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(s.ctas);
