@@ -79,6 +79,9 @@ struct TcParams {
   float scale_log2;
 };
 
+// kSplit: the split layout (a KV head's query rows fit in 64); each
+// instantiation carries only its own softmax.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const TcParams P) {
   const AttnParams &p = P.a;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // one arrival per softmax warp at work: all four in the split layout,
     // else those owning at least one real row
     const int real_rows = min(kRows, P.GT - static_cast<int>(blockIdx.x % P.RT) * kRows);
-    const uint32_t sm_warps = P.split ? 4u : static_cast<uint32_t>((real_rows + 31) / 32);
+    const uint32_t sm_warps = kSplit ? 4u : static_cast<uint32_t>((real_rows + 31) / 32);
     ptx::mbar_init(ptx::smem_u32(p_full), sm_warps);
     ptx::mbar_init(ptx::smem_u32(&s_free[0]), sm_warps);
     ptx::mbar_init(ptx::smem_u32(&s_free[1]), sm_warps);
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   // zeroes the half of its P columns that it never writes.
   if (warp >= 4 && ntiles > 0) {
     const int q4 = warp & 3;
-    const int row = P.split ? 32 * (q4 & 1) + lane : 32 * q4 + lane;
+    const int row = kSplit ? 32 * (q4 & 1) + lane : 32 * q4 + lane;
     const int R = rt * kRows + row;
     const bool real = R < P.GT;
     const int i = real ? R / p.G : 0;
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::tmem_st16(tm_q + lane_off + 16 * c, w16);
       }
     }
-    if (P.split) {
+    if (kSplit) {
       uint32_t z[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) z[e] = 0u;
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::mbar_wait(ptx::smem_u32(drain_pv), 0u, &dummy);
       }
     }
-  } else if (warp >= 4 && P.split) {
+  } else if (warp >= 4 && kSplit) {
     // ------------------------------------------------ softmax, split layout
     // Warp pair (q4, q4 ^ 2) shares query rows 32*(q4&1)..+31: warp q4 < 2
     // takes key columns 0-63 from TMEM lanes of rows 0-63, warp q4 >= 2 takes
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && !kSplit) {
     // ------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;
@@ -723,7 +726,8 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<attn_tc_kernel>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<true>>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<false>>(kSmemMax)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, a.nkv, a.B);
@@ -734,7 +738,8 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, tm, P);
+  return P.split ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tm, P)
+                 : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tm, P);
 }
 
 }  // namespace dflash
