@@ -535,7 +535,7 @@ def run_e2e(dl, step, stream, steps):
         host_out[0].copy_(step.out_buf, non_blocking=True)
 
     copy_stream = torch.cuda.Stream()
-    n_pipe = 10
+    n_pipe = 20
 
     def pipelined(n):
         comp = torch.cuda.current_stream()
