@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *s_full = bars + 4;    // [2] S^T buffer written (2 issuers)
   uint64_t *p_full = bars + 6;    //     P^T written (4 softmax warps)
   uint64_t *o_done = bars + 7;    //     PV of the half-tile complete (2 issuers)
-  uint64_t *q_full = bars + 8;    //     Q in shared memory (2 warps)
+  uint64_t *q_full = bars + 8;    //     Q in shared memory (6 warps)
   uint64_t *drain = bars + 9;     // [2] per-issuer wind-down
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_u32(p_full), 4);
     ptx::mbar_init(ptx::smem_u32(o_done), 2);
-    ptx::mbar_init(ptx::smem_u32(q_full), 2);
+    ptx::mbar_init(ptx::smem_u32(q_full), 6);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
@@ -184,25 +184,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tm_s = tmem + kColS;
   const uint32_t tm_o = tmem + kColO;
 
-  if (warp < 2 && nh > 0) {
-    // ------------------------------------------------ Q -> smem (warps 0-1)
-    // one row per thread: 64 latent + 8 rope 16-byte units, K-major SW128
-    const int rho = threadIdx.x;
-    const int R = R0 + rho;
-    const bool real = R < P.GT;
-    const int i = real ? R / p.hq : 0, h = real ? R % p.hq : 0;
-    const size_t qi = (static_cast<size_t>(r) * p.Tq + i) * p.hq + h;
-    const uint4 *ql = reinterpret_cast<const uint4 *>(p.q + qi * kLat);
-    const uint4 *qr = reinterpret_cast<const uint4 *>(p.q_rope + qi * (kWidth - kLat));
-#pragma unroll 8
-    for (int u = 0; u < kChunks * 8; ++u) {
-      const uint4 v = !real ? make_uint4(0, 0, 0, 0) : (u < 64 ? ql[u] : qr[u - 64]);
-      *reinterpret_cast<uint4 *>(sQ + (u >> 3) * kQChunkBytes + sw128_off(rho, u & 7)) = v;
+  // ------------------------------------------------ Q -> smem, K-major SW128
+  // The CTA's 64 query rows (token i, head h) = rows R0 .. R0 + 63 of the
+  // request's [Tq * hq] rows are contiguous in q and in q_rope.  Warps 4-7
+  // copy the latent part (64 x 64 16-byte units) and warps 0-1 the rope part
+  // (64 x 8 units), each lane a strided run of units, all loads of a batch in
+  // flight before the first store (a row per thread with a load-store pair
+  // per unit costs one memory round trip per unit).
+  if (nh > 0 && (warp >= 4 || warp < 2)) {
+    const size_t q0 = static_cast<size_t>(r) * p.Tq * p.hq + R0;
+    if (warp >= 4) {
+      const int tid = threadIdx.x - 128;
+      const uint4 *ql = reinterpret_cast<const uint4 *>(p.q + q0 * kLat);
+#pragma unroll
+      for (int k0 = 0; k0 < 32; k0 += 16) {
+        uint4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int g = tid + 128 * (k0 + k);
+          v[k] = R0 + (g >> 6) < P.GT ? ql[g] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int g = tid + 128 * (k0 + k), row = g >> 6, u = g & 63;
+          *reinterpret_cast<uint4 *>(sQ + (u >> 3) * kQChunkBytes + sw128_off(row, u & 7)) = v[k];
+        }
+      }
+    } else {
+      const int tid = threadIdx.x;
+      const uint4 *qr = reinterpret_cast<const uint4 *>(p.q_rope + q0 * (kWidth - kLat));
+      uint4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int g = tid + 64 * k;
+        v[k] = R0 + (g >> 3) < P.GT ? qr[g] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int g = tid + 64 * k;
+        *reinterpret_cast<uint4 *>(sQ + 8 * kQChunkBytes + sw128_off(g >> 3, g & 7)) = v[k];
+      }
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(q_full));
-  } else if (nh > 0 && warp == 2) {
+  }
+  if (nh > 0 && warp == 2) {
     // ------------------------------------------------ TMA producer (warp 2)
     // half-tile h goes to buffer h & 1 once both issuers' PV of h - 2 has
     // read it; its boxes (chunk x page box) are issued by different lanes
