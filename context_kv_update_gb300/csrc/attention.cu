@@ -23,38 +23,68 @@ namespace dflash {
 // (MLA latent); this file holds the merge, the segment count and dispatch.
 
 // ----------------------------------------------------------- merge
-// One CTA per output row (r, i, h), one thread per value dim.  Segments are
-// merged in batches of 32 (16 for 512-wide rows) with a running maximum
-// (online log-sum-exp).  Lane j of every warp holds segment j's m and l, so
-// the batch maximum and the denominator are warp reductions and each thread
-// keeps only its own O elements: about 50 registers a thread, so the whole
-// grid is resident beside the main kernel from its launch and starts the
-// moment that kernel completes.  All loads of a batch are issued before any is
+// One CTA per output row (r, i, h), VEC value dims per thread (one for head
+// dims up to 128, four for the 512-wide latent rows).  Segments are merged
+// in batches of 32 (16 for 512-wide rows) with a running maximum (online
+// log-sum-exp).  Lane j of every warp holds segment j's m and l, so the batch
+// maximum and the denominator are warp reductions and each thread keeps only
+// its own O elements.  The CTAs are small enough for the whole grid to be
+// resident at once (~50 registers a thread; 128 threads a row for the latent,
+// whose 512 one-dim threads a row took two waves), so it starts the moment
+// the main kernel completes.  All loads of a batch are issued before any is
 // used (one memory round trip for up to one batch of segments).  The sink
 // starts the running state as an extra logit with no value.  O of an empty
 // segment (m_s = -inf) is loaded but never used (selected away), so a NaN
 // there cannot leak.
-template <int DV>
-__global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
+template <int VEC>
+struct MergeVec {
+  float v[VEC];
+};
+template <int VEC>
+__device__ __forceinline__ MergeVec<VEC> merge_load(const float *p) {
+  MergeVec<VEC> r;
+  if constexpr (VEC == 4) {
+    const float4 t = __ldcg(reinterpret_cast<const float4 *>(p));
+    r.v[0] = t.x;
+    r.v[1] = t.y;
+    r.v[2] = t.z;
+    r.v[3] = t.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) r.v[e] = __ldcg(p + e);
+  }
+  return r;
+}
+
+template <int DV, int VEC>
+__global__ void __launch_bounds__(DV / VEC) attn_merge_kernel(const AttnParams p) {
   griddep_launch();
   griddep_wait();
   constexpr int kBatch = DV >= 512 ? 16 : 32;
   const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
-  const int d = threadIdx.x, lane = d & 31;
+  const int d0 = threadIdx.x * VEC, lane = threadIdx.x & 31;
   const size_t base = static_cast<size_t>(row) * p.S;
   const int S = p.S;
   float M = p.sinks ? p.sinks[h] : -INFINITY;
   float den = p.sinks ? 1.f : 0.f;
-  float acc = 0.f;
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   for (int s0 = 0; s0 < S; s0 += kBatch) {
     const bool in = lane < kBatch && s0 + lane < S;
     const float mj = in ? __ldcg(p.ws_m + base + s0 + lane) : -INFINITY;
     const float lj = in ? __ldcg(p.ws_l + base + s0 + lane) : 0.f;
-    float ov[kBatch];
+    MergeVec<VEC> ov[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-      ov[j] = s0 + j < S ? __ldcg(p.ws_o + (base + s0 + j) * DV + d) : 0.f;
+    for (int j = 0; j < kBatch; ++j) {
+      if (s0 + j < S) {
+        ov[j] = merge_load<VEC>(p.ws_o + (base + s0 + j) * DV + d0);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) ov[j].v[e] = 0.f;
+      }
+    }
     const float Mn = fmaxf(M, warp_max(mj));
     if (Mn == -INFINITY) continue;
     const float sc = (M == -INFINITY) ? 0.f : __expf(M - Mn);
@@ -62,15 +92,27 @@ __global__ void __launch_bounds__(DV) attn_merge_kernel(const AttnParams p) {
     const float wj = live ? __expf(mj - Mn) : 0.f;
     const unsigned live_mask = __ballot_sync(0xffffffffu, live);
     den = den * sc + warp_sum(wj * lj);
-    acc *= sc;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] *= sc;
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const float w = __shfl_sync(0xffffffffu, wj, j);
-      acc += ((live_mask >> j) & 1u) ? w * ov[j] : 0.f;
+      const bool lj_live = ((live_mask >> j) & 1u) != 0;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] += lj_live ? w * ov[j].v[e] : 0.f;
     }
     M = Mn;
   }
-  p.out[static_cast<size_t>(row) * DV + d] = f32_to_bf16_rn(den > 0.f ? acc / den : 0.f);
+  uint16_t *o = p.out + static_cast<size_t>(row) * DV + d0;
+  if constexpr (VEC == 4) {
+    float f[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = den > 0.f ? acc[e] / den : 0.f;
+    *reinterpret_cast<uint2 *>(o) = make_uint2(ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) o[e] = f32_to_bf16_rn(den > 0.f ? acc[e] / den : 0.f);
+  }
 }
 
 int attention_num_segments(const dflash_geom &g, int B, int Tq) {
@@ -127,16 +169,16 @@ cudaError_t launch_attn_merge(const AttnParams &p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(p.B * p.Tq * p.hq);
-  cfg.blockDim = dim3(p.dv);
+  cfg.blockDim = dim3(p.dv >= 512 ? p.dv / 4 : p.dv);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   switch (p.dv) {
-    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p);
-    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
-    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<512>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64, 1>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128, 1>, p);
+    case 512: return cudaLaunchKernelEx(&cfg, attn_merge_kernel<512, 4>, p);
     default: return cudaErrorInvalidValue;
   }
 }

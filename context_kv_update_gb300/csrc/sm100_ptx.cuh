@@ -135,6 +135,21 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t c0
                : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from shared to global memory, both
+// addresses 16-byte aligned, tracked in the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+// Close the thread's bulk group and wait until its copies have completed
+// (written to global memory).
+__device__ __forceinline__ void bulk_commit_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Relaxed GPU-scope load: well defined even while another grid may be
 // writing the word (the value is then either the old or the new one).
 __device__ __forceinline__ int ld_relaxed_s32(const int32_t *p) {
