@@ -86,7 +86,7 @@ def attention_work(prob):
 # DRAM traffic (read + write) of one attention call (main kernel + merge) from
 # the committed ncu capture, keyed by
 # the hash of the attention sources it was taken on (None = not captured).
-ATTN_TRAFFIC = {"sources_sha": "e0b354c5bc875652", "bytes_per_launch": 142893824,
+ATTN_TRAFFIC = {"sources_sha": "1f9e750a434231de", "bytes_per_launch": 142656768,
                 "profile": "profiles/attention_qwen3_8b_32k.md"}
 
 
