@@ -196,19 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 4) {
       const int tid = threadIdx.x - 128;
       const uint4 *ql = reinterpret_cast<const uint4 *>(p.q + q0 * kLat);
+      uint4 v[32];
 #pragma unroll
-      for (int k0 = 0; k0 < 32; k0 += 16) {
-        uint4 v[16];
+      for (int k = 0; k < 32; ++k) {
+        const int g = tid + 128 * k;
+        v[k] = R0 + (g >> 6) < P.GT ? ql[g] : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int g = tid + 128 * (k0 + k);
-          v[k] = R0 + (g >> 6) < P.GT ? ql[g] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int g = tid + 128 * (k0 + k), row = g >> 6, u = g & 63;
-          *reinterpret_cast<uint4 *>(sQ + (u >> 3) * kQChunkBytes + sw128_off(row, u & 7)) = v[k];
-        }
+      for (int k = 0; k < 32; ++k) {
+        const int g = tid + 128 * k, row = g >> 6, u = g & 63;
+        *reinterpret_cast<uint4 *>(sQ + (u >> 3) * kQChunkBytes + sw128_off(row, u & 7)) = v[k];
       }
     } else {
       const int tid = threadIdx.x;
