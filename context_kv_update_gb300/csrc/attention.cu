@@ -25,14 +25,15 @@ namespace dflash {
 // ----------------------------------------------------------- merge
 // One CTA per output row (r, i, h), VEC value dims per thread (one for head
 // dims up to 128, four for the 512-wide latent rows).  Segments are merged
-// in batches of 32 (16 for 512-wide rows) with a running maximum (online
+// in batches of 32 (20 for 512-wide rows) with a running maximum (online
 // log-sum-exp).  Lane j of every warp holds segment j's m and l, so the batch
 // maximum and the denominator are warp reductions and each thread keeps only
 // its own O elements.  The CTAs are small enough for the whole grid to be
-// resident at once (~50 registers a thread; 128 threads a row for the latent,
-// whose 512 one-dim threads a row took two waves), so it starts the moment
-// the main kernel completes.  All loads of a batch are issued before any is
-// used (one memory round trip for up to one batch of segments).  The sink
+// resident at once (56 registers a thread; for the latent 128 threads a row
+// of 112 registers, whose 512 one-dim threads a row took two waves), so it
+// starts the moment the main kernel completes.  All loads of a batch are
+// issued before any is used (one memory round trip for up to one batch of
+// segments).  The sink
 // starts the running state as an extra logit with no value.  O of an empty
 // segment (m_s = -inf) is loaded but never used (selected away), so a NaN
 // there cannot leak.
@@ -60,7 +61,7 @@ template <int DV, int VEC>
 __global__ void __launch_bounds__(DV / VEC) attn_merge_kernel(const AttnParams p) {
   griddep_launch();
   griddep_wait();
-  constexpr int kBatch = DV >= 512 ? 16 : 32;
+  constexpr int kBatch = DV >= 512 ? 20 : 32;
   const int row = blockIdx.x;  // (r * Tq + i) * hq + h
   const int h = row % p.hq;
   const int d0 = threadIdx.x * VEC, lane = threadIdx.x & 31;

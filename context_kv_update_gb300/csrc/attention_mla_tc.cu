@@ -415,13 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t sa = tm_s + lane_off + (h & 1) * (2 * kRowsN);
         float sf[kRowsN];
-        ptx::tmem_ld64f_sync(sa, sf);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        {
           float s2[32];
-          ptx::tmem_ld32f_sync(sa + kRowsN + 32 * hh, s2);
+          ptx::tmem_ld64_ld32f_sync(sa, sa + kRowsN, sf, s2);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sf[32 * hh + c] += s2[c];
+          for (int c = 0; c < 32; ++c) sf[c] += s2[c];
+          ptx::tmem_ld32f_sync(sa + kRowsN + 32, s2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sf[32 + c] += s2[c];
         }
 #pragma unroll
         for (int c = 0; c < kR; ++c) {
