@@ -298,13 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (nh > 0 && lane == 0 && (warp == 3 || warp == 0)) {
     // ------------------------------------------------ MMA issuers
-    // issuer 0 (warp 3) runs QK over latent chunks 0-4 into one S^T partial
-    // and PV blocks 0-1; issuer 1 (warp 0, after its Q rows) QK over chunks
-    // 5-8 (rope) into the second partial and PV blocks 2-3.  Descriptors are
+    // issuer 0 (warp 3) runs the first half of QK's 36 K-steps (chunks 0-3
+    // and half of chunk 4) into one S^T partial and PV blocks 0-1; issuer 1
+    // (warp 0, after its Q rows) the other 18 (the rest of the latent and the
+    // rope chunk) into the second partial and PV blocks 2-3.  Descriptors are
     // formed once and advanced by adding the byte offset (>> 4) to the
     // address field.
     const int role = warp == 3 ? 0 : 1;
-    const int c_lo = role == 0 ? 0 : 5, c_hi = role == 0 ? 5 : kChunks;
+    constexpr int kQkSteps = kChunks * 4;
+    const int ks_lo = role * (kQkSteps / 2), ks_hi = ks_lo + kQkSteps / 2;
     const int b_lo = 2 * role;
     const uint64_t dq0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sQ), 0);
     const uint64_t dk0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sBuf), 0);
@@ -317,12 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t d_s = tm_s + static_cast<uint32_t>((b * 2 + role) * kRowsN);
       const uint32_t boff = b * kBufBytes;
-      for (int c = c_lo; c < c_hi; ++c) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          ptx::mma_bf16(d_s, dk0 + ((boff + c * kChunkBytes + j * 32) >> 4),
-                        dq0 + ((c * kQChunkBytes + j * 32) >> 4), P.idesc_qk,
-                        (c > c_lo || j > 0) ? 1u : 0u);
+      for (int ks = ks_lo; ks < ks_hi; ++ks) {
+        const int c = ks >> 2, j = ks & 3;
+        ptx::mma_bf16(d_s, dk0 + ((boff + c * kChunkBytes + j * 32) >> 4),
+                      dq0 + ((c * kQChunkBytes + j * 32) >> 4), P.idesc_qk,
+                      ks > ks_lo ? 1u : 0u);
       }
       ptx::mma_commit(ptx::smem_u32(&s_full[b]));
       return true;
