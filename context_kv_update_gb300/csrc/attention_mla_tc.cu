@@ -18,12 +18,13 @@
 //   O^T[512 dims x 64 rows] += V^T[512 x 64] . P^T    (four 128-dim blocks;
 //                                                      A = the same latent rows
 //                                                      read MN-major)
-// The MMAs of a half-tile are issued by two threads (one thread issues a
-// tcgen05.mma only every ~70 cycles): each runs QK over part of the chunks
-// into its own S^T partial, which the softmax adds, and two of the four PV
-// blocks.  Each issuer takes PV of half-tile h as soon as its P is written
-// and QK of h+1 as soon as h+1 has landed, so scoring the next half-tile
-// overlaps the softmax of this one.
+// QK of a half-tile is issued by two threads (one thread issues a
+// tcgen05.mma only every ~70 cycles), each over half of the K-steps into its
+// own S^T partial, which the softmax adds; QK of h+1 starts as soon as h+1
+// has landed, so scoring the next half-tile overlaps the softmax of this one.
+// PV is issued by the softmax warps themselves: once all four have written
+// their P^T rows, each warp's lane 0 applies P^T to its own 128-dim block of
+// O^T, with no hand-off to another thread.
 // TMEM: two S^T buffers of 2 x 64 columns + 4 x 64 O^T columns.  Shared
 // memory: Q (9 chunks of 64 rows x 64 dims, 72 KB), two half-tile buffers of
 // 9 chunks of 64 keys x 64 dims (72 KB each), P^T (8 KB).
@@ -70,7 +71,7 @@ constexpr uint32_t kBufBytes = kChunks * kChunkBytes;  // one half-tile
 constexpr uint32_t kBufOff = kChunks * kQChunkBytes;
 constexpr uint32_t kPTOff = kBufOff + 2 * kBufBytes;
 constexpr uint32_t kBarOff = kPTOff + kHK * 128;  // P^T: 64 keys x 64 rows bf16
-constexpr int kNumBars = 12;
+constexpr int kNumBars = 14;
 constexpr uint32_t kXOff = (kBarOff + kNumBars * 8 + 8 + 15) & ~15u;
 constexpr uint32_t kXBytes = (2 * 64 + 64 * 4) * 4;  // m_ref[2][64], xm[64][4]
 constexpr uint32_t kSmemBytes = 1024 + kXOff + kXBytes;
@@ -127,12 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sPT = sm + kPTOff;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kBarOff);
   uint64_t *full = bars;          // [2] half-tile buffer filled
-  uint64_t *empty = bars + 2;     // [2] buffer read by both issuers' PV
+  uint64_t *empty = bars + 2;     // [2] buffer read by the four PV blocks
   uint64_t *s_full = bars + 4;    // [2] S^T buffer written (2 issuers)
-  uint64_t *p_full = bars + 6;    //     P^T written (4 softmax warps)
-  uint64_t *o_done = bars + 7;    //     PV of the half-tile complete (2 issuers)
-  uint64_t *q_full = bars + 8;    //     Q in shared memory (6 warps)
-  uint64_t *drain = bars + 9;     // [2] per-issuer wind-down
+  uint64_t *o_done = bars + 6;    //     PV of the half-tile complete (4 softmax warps)
+  uint64_t *q_full = bars + 7;    //     Q in shared memory (6 warps)
+  uint64_t *drain = bars + 8;     // [2] per-issuer wind-down
+  uint64_t *drain_sm = bars + 10; // [4] per-softmax-warp wind-down
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   float *m_ref = reinterpret_cast<float *>(sm + kXOff);  // [2][64], log2 units
@@ -149,12 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&full[b]), 1);
-      ptx::mbar_init(ptx::smem_u32(&empty[b]), 2);
+      ptx::mbar_init(ptx::smem_u32(&empty[b]), 4);
       ptx::mbar_init(ptx::smem_u32(&s_full[b]), 2);
       ptx::mbar_init(ptx::smem_u32(&drain[b]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(p_full), 4);
-    ptx::mbar_init(ptx::smem_u32(o_done), 2);
+    for (int w = 0; w < 4; ++w) ptx::mbar_init(ptx::smem_u32(&drain_sm[w]), 1);
+    ptx::mbar_init(ptx::smem_u32(o_done), 4);
     ptx::mbar_init(ptx::smem_u32(q_full), 6);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -297,25 +298,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (nh > 0 && lane == 0 && (warp == 3 || warp == 0)) {
-    // ------------------------------------------------ MMA issuers
-    // issuer 0 (warp 3) runs the first half of QK's 36 K-steps (chunks 0-3
-    // and half of chunk 4) into one S^T partial and PV blocks 0-1; issuer 1
-    // (warp 0, after its Q rows) the other 18 (the rest of the latent and the
-    // rope chunk) into the second partial and PV blocks 2-3.  Descriptors are
-    // formed once and advanced by adding the byte offset (>> 4) to the
-    // address field.
+    // ------------------------------------------------ QK issuers
+    // QK(h) = S^T of half-tile h once it has landed.  Issuer 0 (warp 3) runs
+    // the first 18 of QK's 36 K-steps into one S^T partial, issuer 1 (warp 0,
+    // after its Q rows) the other 18 into a second partial; the softmax adds
+    // the two.  The S^T buffer QK(h) writes is free then: the copies of h
+    // were issued only after PV(h - 2), which the softmax issues after it has
+    // read S^T(h - 2).  Descriptors are formed once and advanced by adding
+    // the byte offset (>> 4) to the address field.
     const int role = warp == 3 ? 0 : 1;
     constexpr int kQkSteps = kChunks * 4;
     const int ks_lo = role * (kQkSteps / 2), ks_hi = ks_lo + kQkSteps / 2;
-    const int b_lo = 2 * role;
     const uint64_t dq0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sQ), 0);
     const uint64_t dk0 = ptx::desc_kmajor_sw128(ptx::smem_u32(sBuf), 0);
-    const uint64_t dv0 = ptx::smem_desc(ptx::smem_u32(sBuf), kChunkBytes, 1024, ptx::kSwizzle128B);
-    const uint64_t dp0 = ptx::smem_desc(ptx::smem_u32(sPT), kChunkBytes, 1024, ptx::kSwizzle128B);
-    auto qk = [&](int h) -> bool {
+    bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag);
+    for (int h = 0; ok && h < nh; ++h) {
       const int b = h & 1;
-      if (!ptx::mbar_wait(ptx::smem_u32(&full[b]), static_cast<uint32_t>((h >> 1) & 1), abort_flag))
-        return false;
+      ok = ptx::mbar_wait(ptx::smem_u32(&full[b]), static_cast<uint32_t>((h >> 1) & 1), abort_flag);
+      if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t d_s = tm_s + static_cast<uint32_t>((b * 2 + role) * kRowsN);
       const uint32_t boff = b * kBufBytes;
@@ -326,53 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       ks > ks_lo ? 1u : 0u);
       }
       ptx::mma_commit(ptx::smem_u32(&s_full[b]));
-      return true;
-    };
-    auto pv = [&](int h) -> bool {
-      const int b = h & 1;
-      if (!ptx::mbar_wait(ptx::smem_u32(p_full), static_cast<uint32_t>(h & 1), abort_flag))
-        return false;
-      ptx::tc_fence_after();
-      const uint32_t boff = b * kBufBytes;
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int blk = b_lo + bb;
-#pragma unroll
-        for (int ks = 0; ks < kHK / 16; ++ks)
-          ptx::mma_bf16(tm_o + blk * kRowsN, dv0 + ((boff + 2 * blk * kChunkBytes + ks * 2048) >> 4),
-                        dp0 + ((ks * 2048) >> 4), P.idesc_pv, (h > 0 || ks > 0) ? 1u : 0u);
-      }
-      ptx::mma_commit(ptx::smem_u32(&empty[b]));
-      ptx::mma_commit(ptx::smem_u32(o_done));
-      return true;
-    };
-    // After QK(0) the issuer takes whichever is ready first: PV(np) once the
-    // softmax has written P (it frees a buffer for the next copies), or
-    // QK(nq) once half-tile nq has landed and PV(nq - 2) has been issued
-    // (QK(nq) rewrites the S^T buffer the softmax read for nq - 2).
-    bool ok = ptx::mbar_wait(ptx::smem_u32(q_full), 0u, abort_flag) && qk(0);
-    int nq = 1, np = 0;
-    uint64_t t_idle = ptx::globaltimer_ns();
-    uint32_t spins = 0;
-    while (ok && np < nh) {
-      if (ptx::mbar_test(ptx::smem_u32(p_full), static_cast<uint32_t>(np & 1))) {
-        ok = pv(np++);
-      } else if (nq < nh && nq <= np + 1 &&
-                 ptx::mbar_test(ptx::smem_u32(&full[nq & 1]), static_cast<uint32_t>((nq >> 1) & 1))) {
-        ok = qk(nq++);
-      } else {
-        if ((++spins & 1023u) == 0) {
-          const uint64_t now = ptx::globaltimer_ns();
-          if (*abort_flag) {
-            ok = false;
-          } else if (now - t_idle > ptx::kWaitLimitNs) {
-            *abort_flag = 1;
-            ok = false;
-          }
-        }
-        continue;
-      }
-      t_idle = ptx::globaltimer_ns();
     }
     if (!ok) {
       ptx::mma_commit(ptx::smem_u32(&drain[role]));
@@ -390,6 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = 16 * q4 + (lane & 15);  // the half-tile key they belong to
     constexpr int kR = kRowsN / 2;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    // PV: this warp's lane 0 applies P^T to O^T block q4 (dims 128*q4 ..
+    // +127; A = the half-tile's latent rows read MN-major, B = P^T)
+    const uint64_t dv0 = ptx::smem_desc(ptx::smem_u32(sBuf), kChunkBytes, 1024, ptx::kSwizzle128B);
+    const uint64_t dp0 = ptx::smem_desc(ptx::smem_u32(sPT), kChunkBytes, 1024, ptx::kSwizzle128B);
+    bool pv_issued = false;
     // visible key range of a query token
     auto lo_of = [&](int i) {
       if (p.window <= 0) return 0;
@@ -535,24 +493,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!o_seen && !__all_sync(0xffffffffu,
-                                 ptx::mbar_wait(ptx::smem_u32(o_done),
-                                                static_cast<uint32_t>((h - 1) & 1), abort_flag))) {
-        bad = true;  // the next half-tile's barrier (or the epilogue's) carries it
-        continue;
-      }
+      const bool got_o =
+          o_seen || __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(o_done),
+                                                           static_cast<uint32_t>((h - 1) & 1),
+                                                           abort_flag));
+      if (got_o) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t pk[4];
+        for (int u = 0; u < 4; ++u) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[e] = ptx::pack_bf16x2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
-        *reinterpret_cast<uint4 *>(sPT + sw128_off(key, 4 * hf + u)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int e = 0; e < 4; ++e)
+            pk[e] = ptx::pack_bf16x2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]);
+          *reinterpret_cast<uint4 *>(sPT + sw128_off(key, 4 * hf + u)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        ptx::fence_proxy_async_smem();
       }
-      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
+      // every warp's P^T rows are in place (or all four wind down together)
+      if (ptx::bar_or(3, 128, !got_o)) {
+        bad = true;
+        break;
+      }
+      if (lane == 0) {
+        ptx::tc_fence_after();
+        const uint32_t boff = (h & 1) * kBufBytes;
+#pragma unroll
+        for (int ks = 0; ks < kHK / 16; ++ks)
+          ptx::mma_bf16(tm_o + q4 * kRowsN, dv0 + ((boff + 2 * q4 * kChunkBytes + ks * 2048) >> 4),
+                        dp0 + ((ks * 2048) >> 4), P.idesc_pv, (h > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&empty[h & 1]));
+        ptx::mma_commit(ptx::smem_u32(o_done));
+      }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(p_full));
+      pv_issued = true;
     }
     // ---- epilogue: row sums over the keys, then (m, l, O) per real row
     bool okf = !bad && nh > 0;
@@ -562,6 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    abort_flag));
       ptx::tc_fence_after();
     }
+    if (!okf && pv_issued && lane == 0) {
+      // winding down: this warp's PV MMAs finish before TMEM is released
+      ptx::mma_commit(ptx::smem_u32(&drain_sm[q4]));
+      volatile int dummy = 0;
+      ptx::mbar_wait(ptx::smem_u32(&drain_sm[q4]), 0u, &dummy);
+    }
+    __syncwarp();
     const bool any_bad = ptx::bar_or(2, 128, !okf && nh > 0);
     // the P^T region is idle from here (the last PV is done, or the CTA is
     // winding down and writes no partial)
