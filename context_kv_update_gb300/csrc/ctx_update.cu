@@ -39,6 +39,8 @@ struct CtxWs {
   float *part2;       // K/V (or latent) partial tiles (Y2)
   int4 *dst;          // [Npad] row destinations (many-row epilogue)
   float2 *cs;         // [Npad][nf] RoPE cos/sin per row (many-row epilogue)
+  uint16_t *h;        // [64][D] bf16(Y1) from the cluster fc GEMM (up to 64 rows)
+  float *ssq;         // [D / 32][64] per-slice sums of h^2 (cluster fc GEMM)
   size_t bytes;
 };
 
@@ -80,6 +82,11 @@ CtxWs ctx_ws_map_rows(const dflash_geom &g, int B, int N, void *base) {
   off = align_up(off + sizeof(int4) * d.Npad, 256);
   w.cs = reinterpret_cast<float2 *>(p + off);
   off = align_up(off + sizeof(float2) * d.Npad * d.nf, 256);
+  const size_t hrows = d.N <= 64 ? 64 : 0;
+  w.h = reinterpret_cast<uint16_t *>(p + off);
+  off = align_up(off + sizeof(uint16_t) * hrows * d.D, 256);
+  w.ssq = reinterpret_cast<float *>(p + off);
+  off = align_up(off + sizeof(float) * hrows * (d.D / 32), 256);
   w.bytes = off;
   return w;
 }
@@ -170,6 +177,46 @@ __global__ void __launch_bounds__(kNormThreads) hidden_norm_kernel(
     if (col < c1) hn[static_cast<size_t>(n) * D + col] = f32_to_bf16_rn(h[i] * inv * gv[i]);
   }
   ptx::cluster_wait();  // no CTA leaves while another may still read its s_part
+}
+
+// hn = bf16(h * gamma_h / rms(h)) when the cluster fc GEMM has already formed
+// h = bf16(Y1) and each row's sum of squares in nsl 32-feature slices: CTA
+// (x, n) normalises columns 512x .. 512x + 511 of row n, 8 a thread, and adds
+// the row's slices in the same order as every other CTA of the row (one rms
+// per row).  CTA (0, 0) also snapshots ctx_len for the epilogue.
+__global__ void __launch_bounds__(64) hidden_norm_h_kernel(
+    const uint16_t *h, const float *ssq, int nsl, int rows, const uint16_t *gamma, uint16_t *hn,
+    int D, float eps, const int32_t *ctx_len, int32_t *ctx_snap, int B) {
+  __shared__ float red[2];
+  griddep_launch();
+  const int n = blockIdx.y, tid = threadIdx.x;
+  const int c0 = blockIdx.x * 512 + tid * 8;
+  const bool in = c0 < D;
+  const uint4 gv = in ? *reinterpret_cast<const uint4 *>(gamma + c0) : make_uint4(0, 0, 0, 0);
+  griddep_wait();
+  if (n == 0 && blockIdx.x == 0)
+    for (int r = tid; r < B; r += 64) ctx_snap[r] = ctx_len[r];
+  const uint4 hv = in ? *reinterpret_cast<const uint4 *>(h + static_cast<size_t>(n) * D + c0)
+                      : make_uint4(0, 0, 0, 0);
+  float part = 0.f;
+  for (int sl = tid; sl < nsl; sl += 64) part += ssq[static_cast<size_t>(sl) * rows + n];
+  part = warp_sum(part);
+  if ((tid & 31) == 0) red[tid >> 5] = part;
+  __syncthreads();
+  const float inv = rsqrtf((red[0] + red[1]) / static_cast<float>(D) + eps);
+  if (in) {
+    const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float h0 = __uint_as_float(hw[k] << 16), h1 = __uint_as_float(hw[k] & 0xffff0000u);
+      const float g0 = __uint_as_float(gw[k] << 16), g1 = __uint_as_float(gw[k] & 0xffff0000u);
+      o[k] = static_cast<uint32_t>(f32_to_bf16_rn(h0 * inv * g0)) |
+             (static_cast<uint32_t>(f32_to_bf16_rn(h1 * inv * g1)) << 16);
+    }
+    *reinterpret_cast<uint4 *>(hn + static_cast<size_t>(n) * D + c0) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // ----------------------------------------------------------- write mask
@@ -840,15 +887,40 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   }
   const uint16_t *X = f32 ? W.x : static_cast<const uint16_t *>(hidden);
 
-  // fc GEMM
+  // fc GEMM + hidden RMSNorm.  Up to 64 rows: the fc GEMM as clusters that
+  // finish h = bf16(Y1) and its per-slice sums of squares themselves, then a
+  // plain elementwise norm.
   GemmOut y1, y2;
-  if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.part1, st,
-                       /*pdl=*/true, s, &y1)) != cudaSuccess)
+  const bool fc_cl = !wide && aligned16(w.gamma_h) && fc_cluster_ok(d.N, d.D_in, d.D);
+  if (fc_cl) {
+    if ((e = launch_fc_cluster(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.h,
+                               W.ssq, st, s)) != cudaSuccess)
+      return e;
+  } else if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D,
+                              W.part1, st, /*pdl=*/true, s, &y1)) != cudaSuccess) {
     return e;
+  }
 
-  // hidden RMSNorm: a cluster of G CTAs per row for decode-sized row counts,
-  // one CTA per row beyond
-  if (wide) {
+  // hidden RMSNorm: after the cluster fc GEMM a plain elementwise kernel;
+  // otherwise a cluster of G CTAs per row for decode-sized row counts, one
+  // CTA per row beyond
+  if (fc_cl) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((d.D + 511) / 512, d.N);
+    cfg.blockDim = dim3(64);
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, hidden_norm_h_kernel, static_cast<const uint16_t *>(W.h),
+                                static_cast<const float *>(W.ssq), d.D / 32, fc_cluster_rows(d.N),
+                                static_cast<const uint16_t *>(w.gamma_h), W.hn, d.D,
+                                static_cast<float>(g.eps_hidden),
+                                static_cast<const int32_t *>(ctx_len), snap, B)) != cudaSuccess)
+      return e;
+  } else if (wide) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(d.N);

@@ -251,6 +251,207 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ fc as cluster split-K
+// Y = X W^T for decode row counts (up to 64 rows), each 128-feature output
+// tile computed by a cluster of kFcCluster CTAs that split its K range; the
+// CTAs add their accumulators through distributed shared memory (rank order,
+// deterministic) and CTA k of the cluster finishes features 32k .. 32k + 31:
+// it writes h = bf16(Y) and, per row, the sum of h^2 over those 32 features.
+// Each CTA pushes every quarter of its accumulator straight into the shared
+// memory of the quarter's owner, so one cluster barrier separates the pushes
+// from the local sums and no CTA reads another's memory afterwards.
+// No partial tiles leave the cluster, so the consumer (the hidden RMSNorm)
+// reads one bf16 value per element instead of adding fp32 partials.
+constexpr int kFcCluster = 4;
+
+struct FcParams {
+  int ntile;   // rows (Npad: 16 .. 64, a multiple of 16)
+  int kb_per;  // 64-deep K blocks per CTA
+  int stages;
+  int M;       // output features (row stride of h)
+  uint32_t idesc, tmem_cols;
+  uint16_t *h;  // [ntile][M] bf16
+  float *ssq;   // [M / 128 * kFcCluster][ntile]
+  int32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fc_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const FcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  const uint32_t abytes = a_tile_bytes(), bbytes = b_tile_bytes(p.ntile);
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + S * abytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * bbytes);
+  uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S, *drain = bars + 2 * S + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *consumed = reinterpret_cast<int *>(tmem_slot + 2);
+  // this CTA's 32 features of the tile as pushed by every CTA of the cluster:
+  // [kFcCluster source ranks][ntile rows][32] fp32, outside the ring
+  float *red_in = reinterpret_cast<float *>(
+      smem + ((reinterpret_cast<uintptr_t>(tmem_slot + 4) - reinterpret_cast<uintptr_t>(smem) + 15) &
+              ~static_cast<uintptr_t>(15)));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / kFcCluster, rank = blockIdx.x % kFcCluster;
+  const int kb0 = rank * p.kb_per;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty[i]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), p.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+
+  if (warp == 0) {
+    // ---------------- TMA producer: the weight tiles of the first ring slots
+    // before the dependency wait, the activations after it
+    const uint64_t pol_w = ptx::policy_evict_first();
+    const int total = p.kb_per, pre = total < S ? total : S;
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i)
+        ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[i]), abytes + bbytes);
+    __syncwarp();
+    for (int i = 0; i < pre; ++i)
+      if (lane == 2 * (i & 15))
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + i * abytes), &tmW, (kb0 + i) * 64, mt * 128,
+                              ptx::smem_u32(&full[i]), pol_w);
+    griddep_wait();
+    for (int i = 0; i < pre; ++i)
+      if (lane == 2 * (i & 15) + 1)
+        ptx::tma_load_2d(ptx::smem_u32(sB + i * bbytes), &tmX, (kb0 + i) * 64, 0,
+                         ptx::smem_u32(&full[i]));
+    bool ok = true;
+    int issued = pre;
+    for (int i = pre; i < total; ++i) {
+      const int st = i % S;
+      const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+      bool got = true;
+      if (lane == 0) got = ptx::mbar_spin(ptx::smem_u32(&empty[st]), ph ^ 1u, abort_flag);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[st]), abytes + bbytes);
+      __syncwarp();
+      if (lane == 2 * (i & 15))
+        ptx::tma_load_2d_hint(ptx::smem_u32(sA + st * abytes), &tmW, (kb0 + i) * 64, mt * 128,
+                              ptx::smem_u32(&full[st]), pol_w);
+      if (lane == 2 * (i & 15) + 1)
+        ptx::tma_load_2d(ptx::smem_u32(sB + st * bbytes), &tmX, (kb0 + i) * 64, 0,
+                         ptx::smem_u32(&full[st]));
+      ++issued;
+    }
+    if (!ok && lane == 0) {
+      // wind down: let the copies already issued land before the CTA exits
+      for (int it = *reinterpret_cast<volatile int *>(consumed); it < issued; ++it) {
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(&full[it % S]), static_cast<uint32_t>((it / S) & 1), &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: the CTA's K range into one accumulator
+      bool ok = true;
+      for (int i = 0; i < p.kb_per && ok; ++i) {
+        const int st = i % S;
+        ok = ptx::mbar_spin(ptx::smem_u32(&full[st]), static_cast<uint32_t>((i / S) & 1),
+                            abort_flag);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t a_base = ptx::smem_u32(sA + st * abytes);
+        const uint32_t b_base = ptx::smem_u32(sB + st * bbytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_bf16(tmem, ptx::desc_kmajor_sw128(a_base, k), ptx::desc_kmajor_sw128(b_base, k),
+                        p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&empty[st]));
+        *reinterpret_cast<volatile int *>(consumed) = i + 1;
+      }
+      ptx::mma_commit(ptx::smem_u32(ok ? acc_full : drain));
+      if (!ok) {
+        volatile int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(drain), 0u, &dummy);
+      }
+    }
+  } else {
+    // ---------------- accumulator quarter q (TMEM lanes, i.e. features,
+    // 32q .. +31) -> red_in[rank][row][feature - 32q] of cluster CTA q
+    // (consecutive lanes write consecutive words)
+    const int q = warp & 3;
+    const bool got = ptx::mbar_wait(ptx::smem_u32(acc_full), 0u, abort_flag);
+    if (__all_sync(0xffffffffu, got)) {
+      ptx::tc_fence_after();
+      for (int n0 = 0; n0 < p.ntile; n0 += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld16_sync(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(n0),
+                            r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          ptx::st_dsmem_f32(red_in + (rank * p.ntile + n0 + j) * 32 + lane, static_cast<uint32_t>(q),
+                            __uint_as_float(r[j]));
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  // every quarter is in its owner's shared memory (an aborted CTA pushes
+  // nothing and leaves garbage; its status flag reports the timeout)
+  ptx::cluster_sync();
+  if (warp >= 2) {
+    // ---------------- features 32*rank .. +31 of the tile, added over the
+    // cluster in rank order: tpr threads a row, fpt features each
+    const int t = threadIdx.x - 64;
+    const int tpr = 128 / p.ntile, fpt = 32 / tpr;
+    const int n = t / tpr, part = t % tpr;
+    const int f0 = 32 * rank + part * fpt;
+    float ss = 0.f;
+    for (int j0 = 0; j0 < fpt; j0 += 4) {
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < kFcCluster; ++c) {
+        const float4 v =
+            *reinterpret_cast<const float4 *>(red_in + (c * p.ntile + n) * 32 + part * fpt + j0);
+        y.x += v.x;
+        y.y += v.y;
+        y.z += v.z;
+        y.w += v.w;
+      }
+      const uint32_t lo = ptx::pack_bf16x2(y.x, y.y), hi = ptx::pack_bf16x2(y.z, y.w);
+      const float hx = __uint_as_float(lo << 16), hy = __uint_as_float(lo & 0xffff0000u);
+      const float hz = __uint_as_float(hi << 16), hw = __uint_as_float(hi & 0xffff0000u);
+      ss += (hx * hx + hy * hy) + (hz * hz + hw * hw);
+      *reinterpret_cast<uint2 *>(p.h + static_cast<size_t>(n) * p.M + mt * 128 + f0 + j0) =
+          make_uint2(lo, hi);
+    }
+    for (int o = 1; o < tpr; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (part == 0) p.ssq[(mt * kFcCluster + rank) * p.ntile + n] = ss;
+  }
+  if (*abort_flag && threadIdx.x == 0) raise_status(p.status, DFLASH_DEV_WAIT_TIMEOUT);
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
 // ------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -366,6 +567,101 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
   out->maxc = s.maxc;
   out->ntile = s.ntile;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmW, tmX, p);
+}
+
+
+namespace {
+// Clusters of kFcCluster fc CTAs (one per SM at this shared memory) that fit
+// at once on the current device, cached per device and ring depth.
+int fc_max_active_clusters(size_t smem) {
+  static std::mutex mu;
+  static int cache[64][16];  // [device][stages]: count + 1, 0 = not asked yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int key = static_cast<int>(smem / (16 * 1024)) & 15;
+  std::lock_guard<std::mutex> lock(mu);
+  int &slot = cache[dev][key];
+  if (slot > 0) return slot - 1;
+  int n = 0;
+  if (ensure_smem_limit<fc_cluster_kernel>(kMaxSmem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(kFcCluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kFcCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fc_cluster_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();  // a refused query leaves no sticky error behind
+  slot = n + 1;
+  return n;
+}
+
+struct FcShape {
+  int ntile, kb_per, stages, mtiles;
+  size_t smem;
+};
+FcShape fc_shape(int N, int K, int M) {
+  FcShape f;
+  f.ntile = N <= 16 ? 16 : (N <= 32 ? 32 : 64);  // divides 128: whole rows per reducing thread group
+  f.mtiles = M / 128;
+  f.kb_per = K / 64 / kFcCluster;
+  const int stage_bytes = static_cast<int>(a_tile_bytes() + b_tile_bytes(f.ntile));
+  const int red_bytes = kFcCluster * f.ntile * 32 * 4;  // the pushed quarters
+  f.stages = std::min({kMaxStages, f.kb_per, (kMaxSmem - 2048 - red_bytes) / stage_bytes});
+  f.smem = 1024 + static_cast<size_t>(f.stages) * stage_bytes + (2 * f.stages + 2) * 8 + 32 +
+           red_bytes;
+  return f;
+}
+}  // namespace
+
+bool fc_cluster_ok(int N, int K, int M) {
+  if (N < 1 || N > 64 || M % 128 != 0 || K % (64 * kFcCluster) != 0) return false;
+  const FcShape f = fc_shape(N, K, M);
+  return f.stages >= 2 && f.smem <= static_cast<size_t>(kMaxSmem) &&
+         fc_max_active_clusters(f.smem) >= f.mtiles;
+}
+
+int fc_cluster_rows(int N) { return fc_shape(N, 256, 128).ntile; }
+
+cudaError_t launch_fc_cluster(const uint16_t *X, int N, int K, const uint16_t *W, int M,
+                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st) {
+  const FcShape f = fc_shape(N, K, M);
+  CUtensorMap tmW, tmX;
+  cudaError_t e;
+  if ((e = make_tmap_bf16_2d(&tmW, W, M, K, K, 128, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tmX, X, N, K, K, f.ntile, 64)) != cudaSuccess) return e;
+  FcParams p;
+  p.ntile = f.ntile;
+  p.kb_per = f.kb_per;
+  p.stages = f.stages;
+  p.M = M;
+  p.idesc = ptx::idesc_bf16_f32(128, f.ntile);
+  p.tmem_cols = f.ntile <= 32 ? 32u : 64u;
+  p.h = h;
+  p.ssq = ssq;
+  p.status = status;
+  if ((e = ensure_smem_limit<fc_cluster_kernel>(kMaxSmem)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = dim3(f.mtiles * kFcCluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = f.smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kFcCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, fc_cluster_kernel, tmW, tmX, p);
 }
 
 }  // namespace dflash

@@ -84,4 +84,16 @@ size_t gemm_partial_bytes(int M, int K, int Npad);
 cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int M, float *part,
                         int32_t *status, bool pdl, cudaStream_t s, GemmOut *out);
 
+
+// Decode-sized fc projection as a cluster split-K GEMM: h = bf16(X W^T)
+// [R rows][M] bf16 (R = fc_cluster_rows(N): 16, 32 or 64; rows past N are
+// zero) and, per 32-feature slice and row, the sum of h^2: ssq[M / 32][R]
+// (the slices of a row, added in order, give its sum of squares).
+// fc_cluster_ok: the shape (N <= 64 rows, M % 128 == 0, K % 256 == 0) and
+// the device (every cluster resident at once) allow it.
+bool fc_cluster_ok(int N, int K, int M);
+int fc_cluster_rows(int N);
+cudaError_t launch_fc_cluster(const uint16_t *X, int N, int K, const uint16_t *W, int M,
+                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st);
+
 }  // namespace dflash

@@ -275,6 +275,26 @@ __device__ __forceinline__ float ld_dsmem_f32(const void *p, uint32_t rank) {
   return v;
 }
 
+// Store a float into the shared memory of cluster CTA `rank`, at the address
+// that `p` has in this CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_f32(void *p, uint32_t rank, float v) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+// Four consecutive floats (16-byte aligned) from the shared memory of cluster
+// CTA `rank`, at the address `p` has in this CTA's shared memory.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const void *p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32"
