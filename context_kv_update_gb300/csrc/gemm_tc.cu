@@ -323,10 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch();
 
   if (warp == 0) {
-    // ---------------- TMA producer: the weight tiles of the first ring slots
-    // before the dependency wait, the activations after it
+    // ---------------- TMA producer: the weight tiles of the first kFcPreWait
+    // ring slots before the dependency wait, the activations after it.  All
+    // 128 CTAs start together at the head of the step; a deep burst of weight
+    // requests there delays the preceding small kernel's own memory traffic
+    // and with it the release (3 slots: step 190.6 -> 189.2 us against 12).
+    constexpr int kFcPreWait = 3;
     const uint64_t pol_w = ptx::policy_evict_first();
-    const int total = p.kb_per, pre = total < S ? total : S;
+    const int total = p.kb_per, pre = total < kFcPreWait ? total : (S < kFcPreWait ? S : kFcPreWait);
     if (lane == 0)
       for (int i = 0; i < pre; ++i)
         ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[i]), abytes + bbytes);
