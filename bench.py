@@ -86,7 +86,7 @@ def attention_work(prob):
 # DRAM traffic (read + write) of one attention call (main kernel + merge) from
 # the committed ncu capture, keyed by
 # the hash of the attention sources it was taken on (None = not captured).
-ATTN_TRAFFIC = {"sources_sha": "1f9e750a434231de", "bytes_per_launch": 142656768,
+ATTN_TRAFFIC = {"sources_sha": "5e5314bc14151b3d", "bytes_per_launch": 142508032,
                 "profile": "profiles/attention_qwen3_8b_32k.md"}
 
 
