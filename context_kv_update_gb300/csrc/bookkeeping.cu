@@ -33,13 +33,23 @@ struct BkArgs {
   int32_t *st;
 };
 
+// Two memory round trips on the dependent path: the table row and the
+// request's scalars load together; then the bonus token and every row's page
+// lookup.  Each thread derives the request's scalars itself from shared
+// memory, so no second barrier sits between them and the row outputs.
 __global__ void __launch_bounds__(128) bookkeeping_kernel(const BkArgs a) {
   __shared__ int s_cnt[4];
-  __shared__ int s_scalar[6];  // ok, n, c, A, c', bonus
+  __shared__ int s_in[3];  // n, c, live
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r = blockIdx.x;
   const int32_t *orow = a.off + static_cast<int64_t>(r) * a.off_stride;
+  int n_in = 0, c_in = 0, live_in = 1;
+  if (threadIdx.x == 0) {  // issued now, used after the table loads
+    n_in = a.n_acc[r];
+    c_in = a.ctx_pre[r];
+    live_in = a.valid ? (a.valid[r] != 0) : 1;
+  }
 
   // 1. block-table decode: count of non-negative offsets, clamp and divide.
   int cnt = 0;
@@ -50,53 +60,40 @@ __global__ void __launch_bounds__(128) bookkeeping_kernel(const BkArgs a) {
   }
   cnt = warp_sum_int(cnt);
   if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
-  __syncthreads();
-
-  // 2. per-request scalars (thread 0).
   if (threadIdx.x == 0) {
-    int np = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) np += s_cnt[w];
-    const int n = a.n_acc[r];
-    const int c = a.ctx_pre[r];
-    const bool live = a.valid ? (a.valid[r] != 0) : true;
-    bool ok = live;
-    unsigned bits = 0;
-    if (live && (n < 1 || n > a.T)) { ok = false; bits |= DFLASH_DEV_BAD_NACCEPTED; }
-    if (live && c < 0) { ok = false; bits |= DFLASH_DEV_BAD_CTX_LEN; }
-    if (!ok) np = 0;
-    const long long cap = static_cast<long long>(np) * a.P;
-    const int A = ok ? static_cast<int>(cap < a.max_ctx ? cap : a.max_ctx) : 0;
-    int cn = 0;
-    if (ok) {
-      const long long s = static_cast<long long>(c) + n;
-      cn = static_cast<int>(s < A ? s : A);
-      if (c > A) bits |= DFLASH_DEV_CTX_OUTRUN;
-    }
-    const int b = ok ? a.acc[static_cast<int64_t>(r) * a.acc_stride + (n - 1)] : a.mask_id;
-    a.o.n_pages[r] = np;
-    a.o.alloc_limit[r] = A;
-    a.o.bonus[r] = b;
-    a.o.ctx_len_new[r] = cn;
-    a.o.seq_lens[r] = ok ? cn + a.T : 0;
-    if (bits) raise_status(a.st, bits);
-    s_scalar[0] = ok;
-    s_scalar[1] = n;
-    s_scalar[2] = c;
-    s_scalar[3] = A;
-    s_scalar[4] = cn;
-    s_scalar[5] = b;
+    s_in[0] = n_in;
+    s_in[1] = c_in;
+    s_in[2] = live_in;
   }
   __syncthreads();
-  const int ok = s_scalar[0], n = s_scalar[1], c = s_scalar[2], A = s_scalar[3], cn = s_scalar[4];
-  const int b = s_scalar[5];
+
+  // 2. per-request scalars (every thread; thread 0 writes them out).
   int np = 0;
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) np += s_cnt[w];
-  const long long cap = ok ? static_cast<long long>(np) * a.P : 0;
+  const int n = s_in[0], c = s_in[1];
+  const bool live = s_in[2] != 0;
+  bool okb = live;
+  unsigned bits = 0;
+  if (live && (n < 1 || n > a.T)) { okb = false; bits |= DFLASH_DEV_BAD_NACCEPTED; }
+  if (live && c < 0) { okb = false; bits |= DFLASH_DEV_BAD_CTX_LEN; }
+  if (!okb) np = 0;
+  const long long cap = static_cast<long long>(np) * a.P;
+  const int A = okb ? static_cast<int>(cap < a.max_ctx ? cap : a.max_ctx) : 0;
+  int cn = 0;
+  if (okb) {
+    const long long sum = static_cast<long long>(c) + n;
+    cn = static_cast<int>(sum < A ? sum : A);
+    if (c > A) bits |= DFLASH_DEV_CTX_OUTRUN;
+  }
+  const int ok = okb ? 1 : 0;
+  // the bonus token's load goes out with the rows' page lookups; everything
+  // that uses it is stored last
+  int b = a.mask_id;
+  if (threadIdx.x == 0 && ok) b = a.acc[static_cast<int64_t>(r) * a.acc_stride + (n - 1)];
 
-  // 3. per-row outputs.
+  // 3. per-row outputs (row 0's bonus token: thread 0, which loaded it).
   for (int i = threadIdx.x; i < a.T; i += blockDim.x) {
     const int64_t k = static_cast<int64_t>(r) * a.T + i;
-    a.o.emb_ids[k] = (i == 0) ? b : a.mask_id;
 
     // context row i at c + i
     const int p = ok ? c + i : 0;
@@ -127,6 +124,15 @@ __global__ void __launch_bounds__(128) bookkeeping_kernel(const BkArgs a) {
     a.o.blk_mask[k] = static_cast<uint8_t>(bw);
     a.o.blk_page[k] = bpage;
     a.o.blk_slot[k] = bslot;
+    a.o.emb_ids[k] = (i == 0) ? b : a.mask_id;
+  }
+  if (threadIdx.x == 0) {
+    a.o.bonus[r] = b;
+    a.o.n_pages[r] = np;
+    a.o.alloc_limit[r] = A;
+    a.o.ctx_len_new[r] = cn;
+    a.o.seq_lens[r] = ok ? cn + a.T : 0;
+    if (bits) raise_status(a.st, bits);
   }
 }
 
