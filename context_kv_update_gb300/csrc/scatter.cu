@@ -43,15 +43,17 @@ __global__ void __launch_bounds__(kScatterThreads) block_scatter_kernel(
   };
   // The first vectors of the row are loaded before the destination is known:
   // those loads do not depend on it, so they overlap the mask / page / slot
-  // lookups.
+  // lookups, which are all issued before the mask is tested (one memory
+  // round trip in all).
   uint4 v[kScatterVecs];
 #pragma unroll
   for (int u = 0; u < kScatterVecs; ++u) {
     const int t = threadIdx.x + u * kScatterThreads;
     if (t < nv) v[u] = src(t);
   }
-  if (!mask[row]) return;
+  const uint8_t placed = mask[row];
   const int pg = page[row], sl = slot[row];
+  if (!placed) return;
   if (pg < 0 || pg >= NP || sl < 0 || sl >= P) {
     if (threadIdx.x == 0) raise_status(st, DFLASH_DEV_BAD_PAGE);
     return;
