@@ -26,6 +26,7 @@
 // set-up kernel, and an epilogue of 16-byte loads and 8-byte stores.
 #include <algorithm>
 
+#include "ctx_rows.cuh"
 #include "dflash_internal.cuh"
 #include "gemm_tc.cuh"
 
@@ -221,64 +222,6 @@ __global__ void __launch_bounds__(64) hidden_norm_h_kernel(
   }
 }
 
-// ----------------------------------------------------------- write mask
-struct MaskArgs {
-  const int32_t *n_acc;
-  const int32_t *ctx_snap;
-  const int32_t *alloc_limit;
-  const int32_t *tbl;
-  const uint8_t *valid;
-  const int32_t *cu_rows;  // prefill: request r owns rows cu_rows[r] .. cu_rows[r+1]-1
-  int T, M, P, NP, B;
-  int32_t *st;
-};
-
-// Request and in-request index of GEMM row n: (n / T, n % T) for the decode
-// update, a binary search of cu_rows for the prefill store.  False when the
-// prefill row lies in no request's range (cu_rows inconsistent with the row
-// count; the row is skipped).
-__device__ __forceinline__ bool row_of(const MaskArgs &m, int n, int *r, int *i) {
-  if (!m.cu_rows) {
-    *r = n / m.T;
-    *i = n % m.T;
-    return true;
-  }
-  int lo = 0, hi = m.B - 1;  // the last request whose first row is <= n
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (m.cu_rows[mid] <= n) lo = mid; else hi = mid - 1;
-  }
-  const int a = m.cu_rows[lo], b = m.cu_rows[lo + 1];
-  *r = lo;
-  *i = n - a;
-  return n >= a && n < b;
-}
-
-// Destination of context row (r, i), or false when the row is not written.
-__device__ __forceinline__ bool ctx_row_dest(const MaskArgs &m, int r, int i, int *page, int *slot,
-                                             int *pos, bool report) {
-  // the row's scalars are independent loads, issued together
-  const int n = m.cu_rows ? i + 1 : m.n_acc[r];  // prefill: every row of the request
-  const int c = m.ctx_snap[r];
-  const int A = m.alloc_limit[r];
-  const bool live = m.valid ? (m.valid[r] != 0) : true;
-  if (!live || n < 1 || (!m.cu_rows && n > m.T) || c < 0 || i >= n) return false;
-  const int p = c + i;
-  if (p >= A) return false;
-  const int lp = p / m.P;
-  if (lp >= m.M) return false;
-  const int pg = m.tbl[static_cast<int64_t>(r) * m.M + lp];
-  if (pg < 0) return false;
-  if (pg >= m.NP) {
-    if (report) raise_status(m.st, DFLASH_DEV_BAD_PAGE);
-    return false;
-  }
-  *page = pg;
-  *slot = p % m.P;
-  *pos = p;
-  return true;
-}
-
 // Advance of ctx_len[r] from the pre-step length c (the snapshot).
 __device__ __forceinline__ void advance_ctx_len(const MaskArgs &m, int32_t *ctx_len, int B) {
   for (int r = threadIdx.x; r < B; r += blockDim.x) {
@@ -378,14 +321,6 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
 }
 
-// Destination of each GEMM row, resolved once per row by the norm for the
-// epilogue: {page, slot, position, 0}, page -1 when the row is not stored.
-struct RowDest {
-  int4 *dst;     // [N] or nullptr (the epilogue resolves rows itself)
-  float2 *cs;    // [N][nf] cos/sin of the row's RoPE angles
-  int nf;        // rotate-half pairs per row (GQA hd/2, MLA rope/2)
-  MaskArgs m;    // ctx_snap = the live ctx_len (nothing advances it before the epilogue)
-};
 
 // Row set-up of the many-row epilogue, the first launch of the chain: one
 // warp per GEMM row resolves the row's destination (request by binary search
@@ -398,22 +333,8 @@ __global__ void __launch_bounds__(256) row_setup_kernel(const RowDest rd, const 
   griddep_launch();
   griddep_wait();
   const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (n >= N) return;  // warp-uniform
-  int pos = -1;
-  if (lane == 0) {
-    int r, i, page = 0, slot = 0, p = 0;
-    const bool w = row_of(rd.m, n, &r, &i) && ctx_row_dest(rd.m, r, i, &page, &slot, &p, true);
-    rd.dst[n] = make_int4(w ? page : -1, slot, p, 0);
-    pos = w ? p : -1;
-  }
-  pos = __shfl_sync(0xffffffffu, pos, 0);
-  if (pos < 0) return;
-  for (int f = lane; f < rd.nf; f += 32) {
-    float c, sn;
-    rope_cos_sin(pos, rf.f[f], &c, &sn);
-    rd.cs[static_cast<size_t>(n) * rd.nf + f] = make_float2(c, sn);
-  }
+  row_setup_warp(rd, rf, n, threadIdx.x & 31);
 }
 
 // hn = bf16(bf16(Y1 row) * gamma_h / rms), one CTA of D/32 threads per row:
@@ -644,7 +565,8 @@ __global__ void __launch_bounds__(256) epilogue_mla_wide_kernel(
 template <bool kStaged>
 __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_k, uint16_t *pool, uint16_t *staged,
-                                    int L, int nkv, int hd, float eps, int32_t *ctx_len, int B) {
+                                    int L, int nkv, int hd, float eps, int32_t *ctx_len, int B,
+                                    const int4 *dst, const float2 *cs) {
   __shared__ float red[32];
   __shared__ __align__(16) uint16_t obuf[kMaxHeadDim];  // the bf16 row, stored as 16-byte vectors
   griddep_launch();
@@ -663,6 +585,16 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
     gemm_out_issue(y, t0, act ? gemm_tile_parts(y, t0) : 0, nr, c0 & 127, ld0);
     gemm_out_issue(y, t1, act ? gemm_tile_parts(y, t1) : 0, nr, c1 & 127, ld1);
   }
+  const int l = head / (2 * nkv);
+  const int kv = (head / nkv) & 1;
+  const int h = head % nkv;
+  // a set-up row's destination and cos/sin go out with the Y2 loads
+  int4 d = make_int4(-1, 0, 0, 0);
+  float2 csv = make_float2(1.f, 0.f);
+  if (!kStaged && dst) {
+    d = dst[n];
+    if (kv == 0 && act) csv = cs[static_cast<size_t>(n) * (hd >> 1) + t];
+  }
   // ctx_len advance; every reader of the pre-step value uses the snapshot
   if (!kStaged && n == 0 && head == 0) advance_ctx_len(m, ctx_len, B);
   int r, i;
@@ -670,12 +602,14 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
+  } else if (dst) {
+    if (d.x < 0) return;
+    page = d.x;
+    slot = d.y;
+    pos = d.z;
   } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, head == 0 && t == 0)) {
     return;
   }
-  const int l = head / (2 * nkv);
-  const int kv = (head / nkv) & 1;
-  const int h = head % nkv;
   float v0 = gemm_out_finish(y, ld0), v1 = gemm_out_finish(y, ld1);
   if (kv == 0) {
     const float ss = block_sum(act ? v0 * v0 + v1 * v1 : 0.f, red);
@@ -684,7 +618,12 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
       const float k0 = v0 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t]);
       const float k1 = v1 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t + half]);
       float c, s;
-      rope_cos_sin(pos, rf.f[t], &c, &s);
+      if (!kStaged && dst) {
+        c = csv.x;
+        s = csv.y;
+      } else {
+        rope_cos_sin(pos, rf.f[t], &c, &s);
+      }
       v0 = k0 * c - k1 * s;
       v1 = k1 * c + k0 * s;
     }
@@ -710,7 +649,8 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
 template <bool kStaged>
 __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
                                     const uint16_t *gamma_kv, uint16_t *pool, uint16_t *staged,
-                                    int L, int lat, int rope, float eps, int32_t *ctx_len, int B) {
+                                    int L, int lat, int rope, float eps, int32_t *ctx_len, int B,
+                                    const int4 *dst, const float2 *cs) {
   __shared__ float red[32];
   __shared__ __align__(16) uint16_t obuf[1024];  // lat + rope <= 1024
   griddep_launch();
@@ -732,12 +672,24 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
     gemm_out_issue(y, t0, act ? gemm_tile_parts(y, t0) : 0, nr, g0 & 127, ld0);
     gemm_out_issue(y, t1, act ? gemm_tile_parts(y, t1) : 0, nr, g1 & 127, ld1);
   }
+  // a set-up row's destination and cos/sin go out with the Y2 loads
+  int4 d = make_int4(-1, 0, 0, 0);
+  float2 csv = make_float2(1.f, 0.f);
+  if (!kStaged && dst) {
+    d = dst[n];
+    if (is_rope) csv = cs[static_cast<size_t>(n) * hr + (t - hl)];
+  }
   if (!kStaged && n == 0 && l == 0) advance_ctx_len(m, ctx_len, B);
   int r, i;
   if (!row_of(m, n, &r, &i)) return;
   int page = 0, slot = 0, pos;
   if (kStaged) {
     pos = m.ctx_snap[r] + i;
+  } else if (dst) {
+    if (d.x < 0) return;
+    page = d.x;
+    slot = d.y;
+    pos = d.z;
   } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, l == 0 && t == 0)) {
     return;
   }
@@ -750,7 +702,12 @@ __global__ void epilogue_mla_kernel(const GemmOut y, const MaskArgs m, const Rop
     o1 = v1 * inv * bf16_to_f32(gamma_kv[static_cast<size_t>(l) * lat + cb]);
   } else if (is_rope) {
     float c, s;
-    rope_cos_sin(pos, rf.f[t - hl], &c, &s);
+    if (!kStaged && dst) {
+      c = csv.x;
+      s = csv.y;
+    } else {
+      rope_cos_sin(pos, rf.f[t - hl], &c, &s);
+    }
     o0 = v0 * c - v1 * s;
     o1 = v1 * c + v0 * s;
   }
@@ -894,9 +851,15 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
   // plain elementwise norm.
   GemmOut y1, y2;
   const bool fc_cl = !wide && aligned16(w.gamma_h) && fc_cluster_ok(d.N, d.D_in, d.D);
+  // the fused update's row set-up (destination, RoPE cos/sin) runs in idle
+  // warps of the cluster fc GEMM; the epilogue then reads it
+  const bool fc_setup = fc_cl && !split;
   if (fc_cl) {
+    RowDest frd = rd;
+    frd.dst = W.dst;
     if ((e = launch_fc_cluster(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D, W.h,
-                               W.ssq, st, s)) != cudaSuccess)
+                               W.ssq, st, s, fc_setup ? &frd : nullptr,
+                               fc_setup ? &rf : nullptr)) != cudaSuccess)
       return e;
   } else if ((e = launch_gemm(X, d.N, d.D_in, static_cast<const uint16_t *>(w.w_fc), d.D,
                               W.part1, st, /*pdl=*/true, s, &y1)) != cudaSuccess) {
@@ -1004,7 +967,9 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     cfg.blockDim = dim3(std::max(32, (g.head_dim / 2 + 31) / 32 * 32));
     e = cudaLaunchKernelEx(&cfg, split ? epilogue_gqa_kernel<true> : epilogue_gqa_kernel<false>, y2,
                            m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
-                           g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B);
+                           g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B,
+                           static_cast<const int4 *>(fc_setup ? W.dst : nullptr),
+                           static_cast<const float2 *>(fc_setup ? W.cs : nullptr));
   } else {
     fill_rope_freqs(&rf, g.rope_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers);
@@ -1012,7 +977,8 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
     e = cudaLaunchKernelEx(&cfg, split ? epilogue_mla_kernel<true> : epilogue_mla_kernel<false>, y2,
                            m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
                            g.num_layers, g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k),
-                           ctx_len, B);
+                           ctx_len, B, static_cast<const int4 *>(fc_setup ? W.dst : nullptr),
+                           static_cast<const float2 *>(fc_setup ? W.cs : nullptr));
   }
   return e;
 }

@@ -277,6 +277,9 @@ struct FcParams {
   uint16_t *h;  // [ntile][M] bf16
   float *ssq;   // [M / 128 * kFcCluster][ntile]
   int32_t *status;
+  int setup_rows;  // rows whose set-up warp 2 of CTA n runs (0: none)
+  RowDest rd;
+  RopeFreqs rf;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -402,6 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
+    // ---------------- the epilogue's row set-up, while the weights stream
+    if (warp == 2 && static_cast<int>(blockIdx.x) < p.setup_rows) {
+      griddep_wait();  // it reads the call's index inputs
+      row_setup_warp(p.rd, p.rf, blockIdx.x, lane);
+    }
     // ---------------- accumulator quarter q (TMEM lanes, i.e. features,
     // 32q .. +31) -> red_in[rank][row][feature - 32q] of cluster CTA q
     // (consecutive lanes write consecutive words)
@@ -638,7 +646,8 @@ bool fc_cluster_ok(int N, int K, int M) {
 int fc_cluster_rows(int N) { return fc_shape(N, 256, 128).ntile; }
 
 cudaError_t launch_fc_cluster(const uint16_t *X, int N, int K, const uint16_t *W, int M,
-                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st) {
+                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st,
+                              const RowDest *rd, const RopeFreqs *rf) {
   const FcShape f = fc_shape(N, K, M);
   CUtensorMap tmW, tmX;
   cudaError_t e;
@@ -654,6 +663,12 @@ cudaError_t launch_fc_cluster(const uint16_t *X, int N, int K, const uint16_t *W
   p.h = h;
   p.ssq = ssq;
   p.status = status;
+  p.setup_rows = 0;
+  if (rd && rf && rd->dst && N <= f.mtiles * kFcCluster) {
+    p.setup_rows = N;
+    p.rd = *rd;
+    p.rf = *rf;
+  }
   if ((e = ensure_smem_limit<fc_cluster_kernel>(kMaxSmem)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

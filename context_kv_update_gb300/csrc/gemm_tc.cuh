@@ -17,6 +17,7 @@
 
 #include <cuda.h>
 
+#include "ctx_rows.cuh"
 #include "dflash_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -93,7 +94,11 @@ cudaError_t launch_gemm(const uint16_t *X, int N, int K, const uint16_t *W, int 
 // the device (every cluster resident at once) allow it.
 bool fc_cluster_ok(int N, int K, int M);
 int fc_cluster_rows(int N);
+// rd / rf (optional, nullptr = none): while its CTAs wait for their
+// accumulators, warp 2 of CTA n < N runs the row set-up of row n
+// (row_setup_warp) for the epilogue.
 cudaError_t launch_fc_cluster(const uint16_t *X, int N, int K, const uint16_t *W, int M,
-                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st);
+                              uint16_t *h, float *ssq, int32_t *status, cudaStream_t st,
+                              const RowDest *rd = nullptr, const RopeFreqs *rf = nullptr);
 
 }  // namespace dflash
