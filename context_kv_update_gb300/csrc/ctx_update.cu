@@ -19,10 +19,11 @@
 // Y1 and Y2 stay as the GEMMs' per-CTA partial tiles; the norm and the
 // epilogue add them up as they read (gemm_out_issue / gemm_out_finish).
 // Up to 64 rows the fc GEMM runs as 4-CTA clusters that finish h = bf16(Y1)
-// and its per-slice sums of squares themselves, and the norm is an
-// elementwise pass; up to 256 rows the norm is a cluster per row and the
-// epilogue a CTA per (row, head); beyond (prefill, large batches) one CTA per
-// row of 16-byte loads, with the row destinations resolved once by a row
+// and its per-slice sums of squares themselves (and, in an idle warp, the
+// epilogue's row set-up: destination and RoPE cos/sin per row), and the norm
+// is an elementwise pass; up to 256 rows the norm is a cluster per row and
+// the epilogue a CTA per (row, head); beyond (prefill, large batches) one CTA
+// per row of 16-byte loads, with the row destinations resolved once by a row
 // set-up kernel, and an epilogue of 16-byte loads and 8-byte stores.
 #include <algorithm>
 
