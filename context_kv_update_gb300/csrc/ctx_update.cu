@@ -643,6 +643,92 @@ __global__ void epilogue_gqa_kernel(const GemmOut y, const MaskArgs m, const Rop
   }
 }
 
+// The same epilogue with kEpiHeads heads of one row per CTA (grid (N rows,
+// L*2*nkv / kEpiHeads)): a quarter of the CTAs, each head's k-norm sum over
+// its own warps (one barrier for all heads), when the head count divides.
+constexpr int kEpiHeads = 4;
+template <bool kStaged>
+__global__ void epilogue_gqa_heads_kernel(const GemmOut y, const MaskArgs m, const RopeFreqs rf,
+                                          const uint16_t *gamma_k, uint16_t *pool,
+                                          uint16_t *staged, int L, int nkv, int hd, float eps,
+                                          int32_t *ctx_len, int B, const int4 *dst,
+                                          const float2 *cs) {
+  __shared__ float red[kEpiHeads][4];
+  __shared__ __align__(16) uint16_t obuf[kEpiHeads][kMaxHeadDim];
+  griddep_launch();
+  griddep_wait();
+  const int n = blockIdx.x;
+  const int tph = blockDim.x / kEpiHeads;  // threads per head: a multiple of 32
+  const int hs = threadIdx.x / tph, t = threadIdx.x % tph;
+  const int head = blockIdx.y * kEpiHeads + hs;  // ((l * 2 + kv) * nkv + h)
+  const int half = hd >> 1;
+  const bool act = t < half;
+  GemmOutLoad ld0, ld1;
+  {
+    const int c0 = head * hd + (act ? t : 0), c1 = c0 + half;
+    const int nt = n / y.ntile, nr = n - nt * y.ntile;
+    const unsigned t0 = static_cast<unsigned>(nt) * y.mtiles + (c0 >> 7);
+    const unsigned t1 = static_cast<unsigned>(nt) * y.mtiles + (c1 >> 7);
+    gemm_out_issue(y, t0, act ? gemm_tile_parts(y, t0) : 0, nr, c0 & 127, ld0);
+    gemm_out_issue(y, t1, act ? gemm_tile_parts(y, t1) : 0, nr, c1 & 127, ld1);
+  }
+  const int l = head / (2 * nkv);
+  const int kv = (head / nkv) & 1;
+  const int h = head % nkv;
+  int4 d = make_int4(-1, 0, 0, 0);
+  float2 csv = make_float2(1.f, 0.f);
+  if (!kStaged && dst) {
+    d = dst[n];
+    if (kv == 0 && act) csv = cs[static_cast<size_t>(n) * half + t];
+  }
+  if (!kStaged && n == 0 && blockIdx.y == 0) advance_ctx_len(m, ctx_len, B);
+  int r, i;
+  if (!row_of(m, n, &r, &i)) return;  // the whole CTA: one row
+  int page = 0, slot = 0, pos;
+  if (kStaged) {
+    pos = m.ctx_snap[r] + i;
+  } else if (dst) {
+    if (d.x < 0) return;
+    page = d.x;
+    slot = d.y;
+    pos = d.z;
+  } else if (!ctx_row_dest(m, r, i, &page, &slot, &pos, blockIdx.y == 0 && threadIdx.x == 0)) {
+    return;
+  }
+  float v0 = gemm_out_finish(y, ld0), v1 = gemm_out_finish(y, ld1);
+  const float part = warp_sum((kv == 0 && act) ? v0 * v0 + v1 * v1 : 0.f);
+  if ((t & 31) == 0) red[hs][t >> 5] = part;
+  __syncthreads();
+  if (kv == 0 && act) {
+    float ss = 0.f;
+    for (int w = 0; w < (tph >> 5); ++w) ss += red[hs][w];
+    const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
+    const float k0 = v0 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t]);
+    const float k1 = v1 * inv * bf16_to_f32(gamma_k[static_cast<size_t>(l) * hd + t + half]);
+    float c, sn;
+    if (!kStaged && dst) {
+      c = csv.x;
+      sn = csv.y;
+    } else {
+      rope_cos_sin(pos, rf.f[t], &c, &sn);
+    }
+    v0 = k0 * c - k1 * sn;
+    v1 = k1 * c + k0 * sn;
+  }
+  if (act) {
+    obuf[hs][t] = f32_to_bf16_rn(v0);
+    obuf[hs][t + half] = f32_to_bf16_rn(v1);
+  }
+  __syncthreads();
+  if (t < hd / 8) {  // head_dim % 8 == 0: the row leaves as 16-byte vectors
+    uint16_t *row =
+        kStaged ? staged + static_cast<size_t>(n) * L * 2 * nkv * hd + head * hd
+                : pool + ((((static_cast<size_t>(l) * m.NP + page) * 2 + kv) * nkv + h) * m.P +
+                          slot) * hd;
+    reinterpret_cast<uint4 *>(row)[t] = reinterpret_cast<const uint4 *>(obuf[hs])[t];
+  }
+}
+
 // ------------------------------------------------------ MLA epilogue
 // grid (N rows, L), block = lat / 2 + rope / 2 threads rounded up to a warp:
 // thread t < lat/2 holds latent columns t and t + lat/2; thread lat/2 + j
@@ -962,6 +1048,16 @@ cudaError_t launch_ctx_chain(const dflash_geom &g, int B, const void *hidden, in
                            static_cast<const float2 *>(W.cs),
                            static_cast<const uint16_t *>(w.gamma_k), pool16, d.N, g.num_layers,
                            g.latent_dim, g.rope_dim, static_cast<float>(g.eps_k), ctx_len, B);
+  } else if (gqa && (g.num_layers * 2 * g.nkv) % kEpiHeads == 0 && g.head_dim <= 128) {
+    fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
+    cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv / kEpiHeads);
+    cfg.blockDim = dim3(kEpiHeads * std::max(32, (g.head_dim / 2 + 31) / 32 * 32));
+    e = cudaLaunchKernelEx(&cfg,
+                           split ? epilogue_gqa_heads_kernel<true> : epilogue_gqa_heads_kernel<false>,
+                           y2, m, rf, static_cast<const uint16_t *>(w.gamma_k), pool16, staged,
+                           g.num_layers, g.nkv, g.head_dim, static_cast<float>(g.eps_k), ctx_len, B,
+                           static_cast<const int4 *>(fc_setup ? W.dst : nullptr),
+                           static_cast<const float2 *>(fc_setup ? W.cs : nullptr));
   } else if (gqa) {
     fill_rope_freqs(&rf, g.head_dim, g.rope_theta);
     cfg.gridDim = dim3(d.N, g.num_layers * 2 * g.nkv);
