@@ -2,7 +2,9 @@
 """Benchmark of the drafter decode-step hot path on one GB300.
 
 One step = dflash_step_bookkeeping + dflash_ctx_kv_update + L x
-(dflash_block_kv_scatter + dflash_block_attention) on the Qwen3-8B-shaped
+dflash_block_scatter_attention (the layer's block scatter fused into its block
+attention; --layer-calls separate issues dflash_block_kv_scatter and
+dflash_block_attention instead) on the Qwen3-8B-shaped
 drafter (D = 4096, L = 5, hq = 32, nkv = 8, hd = 128, T = 16, page 64) at
 B = 1 and a 32K context, on seeded synthetic inputs resident in HBM.  The KV
 stream alone (640 MiB/step) is larger than L2, so no explicit flush is needed.
@@ -82,6 +84,14 @@ def attention_work(prob):
         nbytes = keys * g["nkv"] * g["hd"] * 2 * 2
         flops = 4 * keys * rows * g["hd"]
     return nbytes, flops, int(kv.max())
+
+
+def block_scatter_bytes(prob):
+    """Algorithmic bytes of one layer's block scatter: every block row read
+    and written once (GQA: K and V of every KV head; MLA: the latent row)."""
+    g = prob["g"]
+    row = (2 * g["nkv"] * g["hd"] if g["kind"] == "gqa" else g["latent"] + g["rope_dim"]) * 2
+    return 2 * prob["B"] * g["T"] * row
 
 # DRAM traffic (read + write) of one attention call (main kernel + merge) from
 # the committed ncu capture, keyed by
@@ -168,7 +178,7 @@ class ClockSampler:
 class Step:
     """Device buffers + the launch sequence of one drafter step."""
 
-    def __init__(self, dl, prob, dev_status=True, split_update=False):
+    def __init__(self, dl, prob, dev_status=True, split_update=False, fused_layer=True):
         import torch
         self.dl, self.prob = dl, prob
         g = prob["g"]
@@ -201,6 +211,8 @@ class Step:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if dev_status else None
         self.scale = inputs.attention_scale(g)
         self.launches_per_step = None
+        # each layer: one fused scatter + attention call, or the two calls
+        self.fused_layer = fused_layer
         # split update: the projection half runs on an auxiliary stream, forked
         # before the bookkeeping and joined before the commit
         self.split_update = split_update
@@ -304,29 +316,47 @@ class Step:
                                     o["alloc_limit"], o["block_table"], None, self.weights,
                                     self.pool, self.ctx_ws, self.status)
         for layer in range(g["L"]):
-            dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer],
-                                       None if self.mla else self.blk_v[layer],
-                                       o["blk_page"], o["blk_slot"], o["blk_mask"], self.pool,
-                                       self.status)
+            if not self.fused_layer:
+                dl.dflash_block_kv_scatter(self.geom, layer, self.blk_k[layer],
+                                           None if self.mla else self.blk_v[layer],
+                                           o["blk_page"], o["blk_slot"], o["blk_mask"],
+                                           self.pool, self.status)
             if events is not None:
                 events[layer][0].record()
-            dl.dflash_block_attention(self.geom, layer, self.q[layer], self.pool, o["block_table"],
-                                      o["seq_lens"], self.attn_out[layer], self.attn_ws,
-                                      q_rope=None if self.q_rope is None else self.q_rope[layer],
-                                      window=self.prob["window"], sinks=self.sinks,
-                                      scale=self.scale, dev_status=self.status)
+            self.attention_call(layer)
             if events is not None:
                 events[layer][1].record()
 
+    def attention_call(self, layer, num_segments=0, ws=None):
+        """The layer's attention: fused with its block scatter, or alone (the
+        scatter then comes first, as its own call)."""
+        dl, o = self.dl, self.outs
+        q_rope = None if self.q_rope is None else self.q_rope[layer]
+        ws = self.attn_ws if ws is None else ws
+        if self.fused_layer:
+            dl.dflash_block_scatter_attention(
+                self.geom, layer, self.blk_k[layer], None if self.mla else self.blk_v[layer],
+                o["blk_page"], o["blk_slot"], o["blk_mask"], self.q[layer], self.pool,
+                o["block_table"], o["seq_lens"], self.attn_out[layer], ws, q_rope=q_rope,
+                window=self.prob["window"], sinks=self.sinks, scale=self.scale,
+                num_segments=num_segments, dev_status=self.status)
+        else:
+            dl.dflash_block_attention(self.geom, layer, self.q[layer], self.pool, o["block_table"],
+                                      o["seq_lens"], self.attn_out[layer], ws, q_rope=q_rope,
+                                      window=self.prob["window"], sinks=self.sinks,
+                                      scale=self.scale, num_segments=num_segments,
+                                      dev_status=self.status)
 
-def kernel_launches_per_step(g, hidden_is_f32=False, split_update=False, B=1) -> int:
+
+def kernel_launches_per_step(g, hidden_is_f32=False, split_update=False, B=1,
+                             fused_layer=True) -> int:
     # bookkeeping 1; update: fc gemm, hidden norm, kv gemm, epilogue = 4 (+ the
     # fp32 -> bf16 prep for fp32 hidden; + the commit when split; + the row
-    # set-up of the many-row epilogue beyond 256 rows); per layer: scatter 1 +
-    # attention (split + merge) 2
+    # set-up of the many-row epilogue beyond 256 rows); per layer: attention
+    # (split + merge) 2, + the scatter 1 when it is not fused
     many = B * g["T"] > 256 and not split_update
     return (1 + 4 + (1 if hidden_is_f32 else 0) + (1 if split_update else 0) + (1 if many else 0)
-            + g["L"] * 3)
+            + g["L"] * (2 if fused_layer else 3))
 
 
 def make_events(n_layers, count):
@@ -361,7 +391,8 @@ def run_ours(args, rank, world):
     _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=rank)
     g = prob["g"]
-    step = Step(dl, prob, split_update=args.split_update)
+    step = Step(dl, prob, split_update=args.split_update,
+                fused_layer=args.layer_calls == "fused")
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -453,7 +484,8 @@ def run_ours(args, rank, world):
 
 
 def attention_steady_state(dl, step, stream, rounds=5):
-    """Per-call duration of dflash_block_attention (main kernel + merge) in
+    """Per-call duration of the step's attention call (main kernel + merge,
+    with the block scatter fused in unless --layer-calls separate) in
     steady state: one CUDA graph of `rounds` passes over the L layers' calls
     back to back (each call reads its own layer plane of the pool, together
     larger than L2), events only around the replay, divided by the number of
@@ -466,12 +498,7 @@ def attention_steady_state(dl, step, stream, rounds=5):
     def calls():
         for _ in range(rounds):
             for layer in range(g["L"]):
-                dl.dflash_block_attention(
-                    step.geom, layer, step.q[layer], step.pool, o["block_table"], o["seq_lens"],
-                    step.attn_out[layer], step.attn_ws,
-                    q_rope=None if step.q_rope is None else step.q_rope[layer],
-                    window=step.prob["window"], sinks=step.sinks, scale=step.scale,
-                    dev_status=step.status)
+                step.attention_call(layer)
 
     gr = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gr, stream=stream):
@@ -928,6 +955,9 @@ def main():
                     help="override the workload's sliding window (0 = full range)")
     ap.add_argument("--rows", type=int, default=8192,
                     help="prompt rows of the prefill workloads (prefill_mla, prefill_qwen3_8b)")
+    ap.add_argument("--layer-calls", choices=("fused", "separate"), default="fused",
+                    help="per layer: the block scatter fused into the attention call "
+                         "(default) or the scatter and attention calls one after the other")
     ap.add_argument("--split-update", action="store_true",
                     help="run the context update as project (on an auxiliary stream, beside "
                          "the bookkeeping) + commit instead of the fused call")
@@ -961,6 +991,9 @@ def main():
     tag, _ = workload_config(args)
     headline = tag == WORKLOAD_TAG
     attn_bytes, attn_flops, kv_len = attention_work(prob)
+    fused = args.layer_calls == "fused"
+    if fused:
+        attn_bytes += block_scatter_bytes(prob)
     peaks = measured_peaks()
     # the roofline takes the steady-state per-call duration (calls back to
     # back, as the layer loop issues them); the per-call figure inside the
@@ -985,7 +1018,9 @@ def main():
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": traffic, "bytes_per_launch": attn_bytes,
                 "peak_source": peaks["source"] + " hbm_gbs (of " + peaks["source"] + ")"}
-    roof.update({"kernel": "dflash_block_attention (split + merge)",
+    roof.update({"kernel": ("dflash_block_scatter_attention (block scatter fused into the "
+                            "split kernel + merge)" if fused
+                            else "dflash_block_attention (split + merge)"),
                  "launch_ms": round(res["attn_ss_ms"], 5),
                  "launch_timing": "CUDA-graph replay of 5 x L back-to-back calls (one layer "
                                   "plane each), CUDA events around the replay",
@@ -1002,7 +1037,9 @@ def main():
                      else "per-step KV + weight bytes as the workload gives"),
               "parallelism": "replicas" if world > 1 else "single GPU",
               "update": ("split: project on an auxiliary stream, commit after the join"
-                         if args.split_update else "fused")}
+                         if args.split_update else "fused"),
+              "layer_calls": ("block scatter fused into the attention call" if fused
+                              else "block scatter, then attention")}
     if g["kind"] == "mla":
         config.update({"latent": g["latent"], "rope_dim": g["rope_dim"]})
     line = {
@@ -1016,7 +1053,8 @@ def main():
         "clocks": res["clocks"],
         "e2e": res["e2e"],
         "gpu_launches": kernel_launches_per_step(
-            g, prob["hidden"].dtype == np.float32, args.split_update, prob["B"]) * args.steps,
+            g, prob["hidden"].dtype == np.float32, args.split_update, prob["B"],
+            fused) * args.steps,
         "device_status": res["status"],
     }
     if not args.no_cpu_baseline and headline:

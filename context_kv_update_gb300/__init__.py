@@ -11,6 +11,7 @@ from ._lib import (DflashError, Geom, LayerWeights, StepOutputs, Weights,  # noq
                    dflash_attention_num_segments, dflash_attention_workspace_bytes,
                    dflash_block_attention, dflash_block_attention_noalloc,
                    dflash_block_attention_noalloc_max_scratch_bytes, dflash_block_kv_scatter,
+                   dflash_block_scatter_attention,
                    dflash_ctx_kv_commit, dflash_ctx_kv_prefill, dflash_ctx_kv_project,
                    dflash_ctx_kv_update, dflash_ctx_prefill_workspace_bytes,
                    dflash_ctx_staged_bytes, dflash_ctx_workspace_bytes, dflash_q_norm_rope,

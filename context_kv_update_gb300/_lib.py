@@ -44,7 +44,8 @@ EXPORTS = ("dflash_step_bookkeeping", "dflash_ctx_workspace_bytes", "dflash_ctx_
            "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
            "dflash_packed_kv_bytes", "dflash_packed_gamma_bytes", "dflash_pack_weights",
            "dflash_strict_accept", "dflash_embedding_gather", "dflash_ctx_prefill_workspace_bytes",
-           "dflash_ctx_kv_prefill", "dflash_test_attention_skip_tile")
+           "dflash_ctx_kv_prefill", "dflash_test_attention_skip_tile",
+           "dflash_block_scatter_attention")
 
 
 class DflashError(RuntimeError):
@@ -117,6 +118,10 @@ def load():
     lib.dflash_block_attention.argtypes = [G, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
                                            vp, vp, i32, vp, ctypes.c_float, ctypes.c_int,
                                            ctypes.c_int, vp, sz, vp, vp, vp]
+    lib.dflash_block_scatter_attention.argtypes = [G, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp,
+                                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
+                                                   sz, vp, vp, vp]
     lib.dflash_block_attention_noalloc.argtypes = [G, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                    vp, vp, vp, vp, i32, vp, ctypes.c_float,
                                                    ctypes.c_int, ctypes.c_int, vp, vp, vp]
@@ -144,7 +149,7 @@ def load():
                  "dflash_block_attention", "dflash_attention_num_segments", "dflash_abi_version",
                  "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_q_norm_rope",
                  "dflash_pack_weights", "dflash_strict_accept", "dflash_embedding_gather",
-                 "dflash_ctx_kv_prefill"):
+                 "dflash_ctx_kv_prefill", "dflash_block_scatter_attention"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -290,6 +295,21 @@ def dflash_block_attention(geom, layer, q, kv_pool, block_table, kv_len, out, wo
     scale = 0.0 if scale is None else scale  # 0 = the library's default scale
     _check("dflash_block_attention", lib.dflash_block_attention(
         ctypes.byref(geom), B, layer, Tq, _ptr(q), _ptr(q_rope), _ptr(kv_pool), _ptr(block_table),
+        _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(dev_status), _stream(stream)))
+
+
+def dflash_block_scatter_attention(geom, layer, blk_k, blk_v, blk_page, blk_slot, blk_mask, q,
+                                   kv_pool, block_table, kv_len, out, workspace, *, q_rope=None,
+                                   window=0, sinks=None, scale=None, mask_mode=MASK_CAUSAL_TAIL,
+                                   num_segments=0, dev_status=None, stream=None):
+    lib = load()
+    B, Tq = int(q.shape[0]), int(q.shape[1])
+    scale = 0.0 if scale is None else scale  # 0 = the library's default scale
+    _check("dflash_block_scatter_attention", lib.dflash_block_scatter_attention(
+        ctypes.byref(geom), B, layer, Tq, _ptr(blk_k), _ptr(blk_v), _ptr(blk_page),
+        _ptr(blk_slot), _ptr(blk_mask), _ptr(q), _ptr(q_rope), _ptr(kv_pool), _ptr(block_table),
         _ptr(kv_len), int(window), _ptr(sinks), float(scale), int(mask_mode), int(num_segments),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _ptr(dev_status), _stream(stream)))

@@ -153,10 +153,29 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
                                    const int32_t *kv_len, int32_t window, const float *sinks,
                                    float scale, int mask_mode, int S, void *ws, void *out,
                                    int32_t *st, cudaStream_t s) {
+  return launch_block_scatter_attention(g, B, layer, Tq, nullptr, nullptr, nullptr, nullptr,
+                                        nullptr, q, q_rope, pool, tbl, kv_len, window, sinks,
+                                        scale, mask_mode, S, ws, out, st, s);
+}
+
+cudaError_t launch_block_scatter_attention(const dflash_geom &g, int B, int layer, int Tq,
+                                           const void *blk_k, const void *blk_v,
+                                           const int32_t *blk_page, const int32_t *blk_slot,
+                                           const uint8_t *blk_mask, const void *q,
+                                           const void *q_rope, const void *pool,
+                                           const int32_t *tbl, const int32_t *kv_len,
+                                           int32_t window, const float *sinks, float scale,
+                                           int mask_mode, int S, void *ws, void *out, int32_t *st,
+                                           cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   if (S <= 0) S = attention_num_segments(g, B, Tq);
   AttnParams p = make_attn_params(g, B, layer, Tq, q, q_rope, pool, tbl, kv_len, window, sinks,
                                   scale, mask_mode, S, ws, out, st);
+  p.blk_k = static_cast<const uint4 *>(blk_k);
+  p.blk_v = static_cast<const uint4 *>(blk_v);
+  p.blk_page = blk_page;
+  p.blk_slot = blk_slot;
+  p.blk_mask = blk_mask;
   cudaError_t e;
   if (g.kind == DFLASH_KIND_GQA)
     e = launch_attn_tc(p, g, s);

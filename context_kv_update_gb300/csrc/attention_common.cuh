@@ -23,6 +23,12 @@ struct AttnParams {
   float *ws_m, *ws_l, *ws_o;
   uint16_t *out;
   int32_t *st;
+  // Fused block scatter (blk_k null: none).  Block rows [B, Tq] of this
+  // layer: GQA K and V [B, Tq, nkv, hd], MLA latents [B, Tq, W] (blk_v null),
+  // placed at (blk_page, blk_slot) where blk_mask is set.
+  const uint4 *blk_k, *blk_v;
+  const int32_t *blk_page, *blk_slot;
+  const uint8_t *blk_mask;
 };
 
 inline AttnParams make_attn_params(const dflash_geom &g, int B, int layer, int Tq, const void *q,
@@ -70,6 +76,9 @@ inline AttnParams make_attn_params(const dflash_geom &g, int B, int layer, int T
   p.ws_o = reinterpret_cast<float *>(w + 2 * align_up(rows * sizeof(float), 256));
   p.out = static_cast<uint16_t *>(out);
   p.st = st;
+  p.blk_k = p.blk_v = nullptr;
+  p.blk_page = p.blk_slot = nullptr;
+  p.blk_mask = nullptr;
   return p;
 }
 
@@ -133,6 +142,80 @@ __device__ __forceinline__ SegRange segment_range_for(const AttnParams &p, int k
 __device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, int s) {
   return segment_range_for(p, clamped_kv_len(p, r, s == 0 && blockIdx.y == 0 && threadIdx.x == 0),
                            s);
+}
+
+// Fused block scatter.  The block's row (r, i) holds the key at position
+// kv_len - Tq + i (the last Tq keys, which every window sees), so the CTAs
+// whose segment range [k0, k1) covers that position are the ones that read
+// it: each of them writes the rows of its own range (the row tiles of a
+// segment write the same bytes) before its copies of those keys are issued.
+// Rows at positions no segment reads (kv_len < Tq) are written by the CTAs of
+// segment 0, row tile 0.  GQA: head kvh's K and V rows; MLA: the latent row.
+// Warp-wide; each lane ends with a proxy fence, so tensor copies issued after
+// a later barrier (an mbarrier the warp arrives on) read the new rows.
+// First key position this CTA must not copy before the scatter (INT_MAX: none).
+__device__ __forceinline__ int block_scatter_first_key(const AttnParams &p, const SegRange &sr) {
+  if (p.blk_k == nullptr || sr.kv_len <= 0) return 0x7fffffff;
+  const int lo = max(sr.kv_len - p.Tq, sr.k0), hi = min(sr.kv_len, sr.k1);
+  return lo < hi ? lo : 0x7fffffff;
+}
+
+__device__ __forceinline__ void block_scatter_rows(const AttnParams &p, int r, int kvh,
+                                                   const SegRange &sr, bool first_cta, int lane) {
+  constexpr int kBatch = 8;  // 16-byte vectors a lane has in flight
+  const int kl = sr.kv_len;
+  int lo0 = 0, hi0 = 0;
+  if (kl > 0) row_key_range(p, kl, 0, &lo0, &hi0);
+  // Most CTAs hold none of the block's rows: they skip the loop and the fence
+  // (the warp shares its issue slots with a softmax warp).
+  const bool any_covered = kl > 0 && max(kl - p.Tq, sr.k0) < min(kl, sr.k1);
+  const bool any_uncovered = first_cta && (kl <= 0 || kl - p.Tq < lo0);
+  if (!any_covered && !any_uncovered) return;
+  const bool gqa = p.kind == DFLASH_KIND_GQA;
+  const int vw = p.W / 8;               // vectors of one cache row
+  const int vrow = gqa ? 2 * vw : vw;   // vectors of one block row (GQA: K, V)
+  const int total = p.Tq * vrow;
+  uint16_t *pool = const_cast<uint16_t *>(p.pool);
+  for (int t0 = 0; t0 < total; t0 += 32 * kBatch) {
+    // every load of the batch is issued before any is used
+    uint4 v[kBatch];
+    int pg[kBatch], sl[kBatch];
+    uint8_t placed[kBatch];
+    bool mine[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int t = t0 + 32 * u + lane;
+      const int i = t / vrow, e = t - i * vrow;
+      const int pos = kl - p.Tq + i;
+      const bool covered = kl > 0 && pos >= lo0;
+      mine[u] = t < total && (covered ? (pos >= sr.k0 && pos < sr.k1) : first_cta);
+      placed[u] = 0;
+      if (mine[u]) {
+        const int64_t k = static_cast<int64_t>(r) * p.Tq + i;
+        const int kv = gqa && e >= vw ? 1 : 0, ee = e - kv * vw;
+        v[u] = gqa ? (kv ? p.blk_v : p.blk_k)[(k * p.nkv + kvh) * vw + ee] : p.blk_k[k * vw + ee];
+        placed[u] = p.blk_mask[k];
+        pg[u] = p.blk_page[k];
+        sl[u] = p.blk_slot[k];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (!placed[u]) continue;
+      if (pg[u] < 0 || pg[u] >= p.NP || sl[u] < 0 || sl[u] >= p.P) {
+        raise_status(p.st, DFLASH_DEV_BAD_PAGE);
+        continue;
+      }
+      const int t = t0 + 32 * u + lane;
+      const int e = t % vrow;
+      const int kv = gqa && e >= vw ? 1 : 0, ee = e - kv * vw;
+      const size_t row = gqa ? ((((static_cast<size_t>(p.layer) * p.NP + pg[u]) * 2 + kv) * p.nkv +
+                                 kvh) * p.P + sl[u])
+                             : ((static_cast<size_t>(p.layer) * p.NP + pg[u]) * p.P + sl[u]);
+      reinterpret_cast<uint4 *>(pool + row * p.W)[ee] = v[u];
+    }
+  }
+  ptx::fence_proxy_async_global();
 }
 
 // Cache rows of key j (GQA: K and V of head kvh; MLA: the latent row twice).

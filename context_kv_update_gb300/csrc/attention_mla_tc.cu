@@ -39,6 +39,10 @@
 // once the previous PV has read it; each thread accumulates its key's share
 // of the row sums, reduced across the keys once at the end.
 //
+// When the call fuses the block scatter, warp 1 (after its share of the query
+// load) writes the block's own latent rows into the cache, and the producer
+// holds back the copies of those keys until it has.
+//
 // The copies of a half-tile (9 chunks x its pages) are issued by different
 // lanes at once: a TMA issue does not return before the copy engine takes
 // it, so boxes issued one after another refill a buffer ~2x slower.  Every
@@ -71,7 +75,7 @@ constexpr uint32_t kBufBytes = kChunks * kChunkBytes;  // one half-tile
 constexpr uint32_t kBufOff = kChunks * kQChunkBytes;
 constexpr uint32_t kPTOff = kBufOff + 2 * kBufBytes;
 constexpr uint32_t kBarOff = kPTOff + kHK * 128;  // P^T: 64 keys x 64 rows bf16
-constexpr int kNumBars = 14;
+constexpr int kNumBars = 15;
 constexpr uint32_t kXOff = (kBarOff + kNumBars * 8 + 8 + 15) & ~15u;
 constexpr uint32_t kXBytes = (2 * 64 + 64 * 4) * 4;  // m_ref[2][64], xm[64][4]
 constexpr uint32_t kSmemBytes = 1024 + kXOff + kXBytes;
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *q_full = bars + 7;    //     Q in shared memory (6 warps)
   uint64_t *drain = bars + 8;     // [2] per-issuer wind-down
   uint64_t *drain_sm = bars + 10; // [4] per-softmax-warp wind-down
+  uint64_t *scat_done = bars + 14; //     block rows written (fused scatter)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   float *m_ref = reinterpret_cast<float *>(sm + kXOff);  // [2][64], log2 units
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 4; ++w) ptx::mbar_init(ptx::smem_u32(&drain_sm[w]), 1);
     ptx::mbar_init(ptx::smem_u32(o_done), 4);
     ptx::mbar_init(ptx::smem_u32(q_full), 6);
+    ptx::mbar_init(ptx::smem_u32(scat_done), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
@@ -227,6 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(q_full));
   }
+  if (warp == 1 && p.blk_k != nullptr) {
+    // ------------------------------------------------ fused block scatter (warp 1)
+    // the block's own latent rows into the cache, before the producer copies
+    // those keys (every row group of the segment writes the same bytes)
+    block_scatter_rows(p, r, 0, sr, s == 0 && rg == 0, lane);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(scat_done));
+  }
   if (nh > 0 && warp == 2) {
     // ------------------------------------------------ TMA producer (warp 2)
     // half-tile h goes to buffer h & 1 once both issuers' PV of h - 2 has
@@ -253,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nxt = fetch_page(halves_per_batch);
     int last_fill[2] = {-1, -1};
     bool ok = true;
+    // fused block scatter: the first key whose row warp 1 writes
+    const int scat_key = block_scatter_first_key(p, sr);
+    bool scat_wait = scat_key != 0x7fffffff;
     for (int h = 0; h < nh; ++h) {
       const int hb = h % halves_per_batch;
       if (hb == 0 && h > 0) {
@@ -267,6 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
         break;
+      }
+      if (scat_wait && kbase_of(h) + kHK > scat_key) {
+        scat_wait = false;
+        bool got_rows = true;
+        if (lane == 0) got_rows = ptx::mbar_wait(ptx::smem_u32(scat_done), 0u, abort_flag);
+        if (!__shfl_sync(0xffffffffu, got_rows ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
       }
       const bool skip = h == P.skip_h;
       if (lane == 0 && !skip) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[b]), kBufBytes);

@@ -25,10 +25,12 @@
 // stream), so tiles are 128 keys wide: per key that halves the QK
 // instructions and the waits and commits of a 64-key tile.
 //
-// Roles (8 warps): warp 2 issues TMA, warp 3 issues tcgen05.mma and owns the
-// TMEM allocation, warps 4-7 run the softmax (warp w reads and writes TMEM
-// lanes 32*(w%4)..+31, i.e. runs on SM sub-partition w%4), warps 0-1 only join
-// the final barrier.  When the group has at most 64 query rows (the decode
+// Roles (8 warps): warp 2 issues TMA, warp 3 issues QK and owns the TMEM
+// allocation, lane 0 of warp 0 issues PV, warps 4-7 run the softmax (warp w
+// reads and writes TMEM lanes 32*(w%4)..+31, i.e. runs on SM sub-partition
+// w%4), and warp 1 writes the block's own K/V rows into the cache when the
+// call fuses the block scatter (the producer holds back the copies of those
+// keys until it has).  When the group has at most 64 query rows (the decode
 // case: a 16-token block times a few heads per KV head), those rows are
 // loaded twice, as MMA rows r and r + 64: the tensor core then hands all four
 // sub-partitions a copy of the scores and each softmax warp takes half of a
@@ -93,8 +95,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
   uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
   uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1, *q_full = drain + 1;
-  uint64_t *s_free = q_full + 1, *drain_pv = s_free + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain_pv + 1);
+  uint64_t *s_free = q_full + 1, *drain_pv = s_free + 2, *scat_done = drain_pv + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(scat_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *consumed = reinterpret_cast<volatile int *>(tslot + 2);
 
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::mbar_init(ptx::smem_u32(drain), 1);
     ptx::mbar_init(ptx::smem_u32(drain_pv), 1);
     ptx::mbar_init(ptx::smem_u32(q_full), 4u);  // one arrival per softmax warp
+    ptx::mbar_init(ptx::smem_u32(scat_done), 1u);
     *abort_flag = 0;
     *consumed = 0;
     ptx::fence_mbar_init();
@@ -252,6 +255,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     int nxt = fetch_page(tiles_per_batch);
     int issued = 0;
     bool ok = true;
+    // fused block scatter: the first key whose rows warp 1 writes
+    const int scat_key = block_scatter_first_key(p, sr);
+    bool scat_wait = scat_key != 0x7fffffff;
     for (int t = 0; t < ntiles; ++t) {
       const int tb = t % tiles_per_batch;
       if (tb == 0 && t > 0) {
@@ -266,6 +272,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
         break;
+      }
+      if (scat_wait && (sr.t0 + t + 1) * kKT > scat_key) {
+        scat_wait = false;
+        bool got_rows = true;
+        if (lane == 0) got_rows = ptx::mbar_wait(ptx::smem_u32(scat_done), 0u, abort_flag);
+        if (!__shfl_sync(0xffffffffu, got_rows ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
       }
       const bool skip = t == P.skip_tile;
       if (lane == 0 && !skip)
@@ -362,6 +377,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::mbar_wait(ptx::smem_u32(drain_pv), 0u, &dummy);
       }
     }
+  } else if (warp == 1 && p.blk_k != nullptr) {
+    // ------------------------------------------------ fused block scatter (warp 1)
+    block_scatter_rows(p, r, kvh, sr, s == 0 && rt == 0, lane);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(scat_done));
   } else if (warp >= 4 && kSplit) {
     // ------------------------------------------------ softmax, split layout
     // Warp pair (q4, q4 ^ 2) shares query rows 32*(q4&1)..+31: warp q4 < 2
@@ -709,11 +729,11 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.k_bytes = P.chunks * kVChunk;
   P.stage_bytes = 2 * P.k_bytes;
   const uint32_t x_bytes = 320 * 4;  // split-layout row maxima and row sums
-  const uint32_t bar_bytes = 8 * 8 * 2 + 10 * 8 + 16;
+  const uint32_t bar_bytes = 8 * 8 * 2 + 11 * 8 + 16;
   P.nst = std::max(2, std::min<int>(8, static_cast<int>((kSmemMax - 1024 - bar_bytes - x_bytes) /
                                                           P.stage_bytes)));
   P.bar_off = P.nst * P.stage_bytes;
-  P.x_off = (P.bar_off + (2 * P.nst + 10) * 8 + 16 + 15) & ~15u;
+  P.x_off = (P.bar_off + (2 * P.nst + 11) * 8 + 16 + 15) & ~15u;
   const uint32_t smem = 1024 + P.x_off + x_bytes;
   P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);

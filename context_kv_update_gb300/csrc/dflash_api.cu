@@ -290,15 +290,9 @@ extern "C" int dflash_block_kv_scatter(const dflash_geom *g, int B, int layer, c
                                        dflash_stream_t stream) {
   if (!geom_ok(g) || B < 0 || layer < 0 || layer >= g->num_layers) return DFLASH_ERR_INVALID_ARG;
   if (B == 0) return DFLASH_OK;
-  if (!blk_k || !blk_page || !blk_slot || !blk_mask || !kv_pool) return DFLASH_ERR_INVALID_ARG;
-  if (g->kind == DFLASH_KIND_GQA) {
-    if (!blk_v || !aligned16(blk_v)) return DFLASH_ERR_INVALID_ARG;
-    if (g->head_dim % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
-  } else {
-    if (blk_v) return DFLASH_ERR_INVALID_ARG;
-    if ((g->latent_dim + g->rope_dim) % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
-  }
-  if (!aligned16(blk_k) || !aligned16(kv_pool)) return DFLASH_ERR_INVALID_ARG;
+  if (const int st = block_scatter_args_status(*g, blk_k, blk_v, blk_page, blk_slot, blk_mask,
+                                               kv_pool))
+    return st;
   return cuda_status(launch_block_scatter(*g, B, layer, blk_k, blk_v, blk_page, blk_slot, blk_mask,
                                           kv_pool, dev_status,
                                           reinterpret_cast<cudaStream_t>(stream)));
@@ -356,6 +350,22 @@ int attention_ptrs_status(int B, const void *q, const void *q_rope, const void *
   return DFLASH_OK;
 }
 
+// Pointers and row widths of a block scatter (standalone or fused).
+int block_scatter_args_status(const dflash_geom &g, const void *blk_k, const void *blk_v,
+                              const int32_t *blk_page, const int32_t *blk_slot,
+                              const uint8_t *blk_mask, const void *kv_pool) {
+  if (!blk_k || !blk_page || !blk_slot || !blk_mask || !kv_pool) return DFLASH_ERR_INVALID_ARG;
+  if (g.kind == DFLASH_KIND_GQA) {
+    if (!blk_v || !aligned16(blk_v)) return DFLASH_ERR_INVALID_ARG;
+    if (g.head_dim % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  } else {
+    if (blk_v) return DFLASH_ERR_INVALID_ARG;
+    if ((g.latent_dim + g.rope_dim) % 8 != 0) return DFLASH_ERR_UNSUPPORTED_GEOM;
+  }
+  if (!aligned16(blk_k) || !aligned16(kv_pool)) return DFLASH_ERR_INVALID_ARG;
+  return DFLASH_OK;
+}
+
 float default_attention_scale(const dflash_geom &g) {
   // GQA: 1/sqrt(head_dim).  MLA: the absorbed-latent form keeps the scale of
   // the unabsorbed head, a 128-wide no-rope part plus the rope part.
@@ -385,4 +395,29 @@ extern "C" int dflash_block_attention(const dflash_geom *g, int B, int layer, in
                                             kv_len, window, sinks, scale, mask_mode, S, workspace,
                                             out, dev_status,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dflash_block_scatter_attention(
+    const dflash_geom *g, int B, int layer, int Tq, const void *blk_k, const void *blk_v,
+    const int32_t *blk_page, const int32_t *blk_slot, const uint8_t *blk_mask, const void *q,
+    const void *q_rope, void *kv_pool, const int32_t *block_table, const int32_t *kv_len,
+    int32_t window, const float *sinks, float scale, int mask_mode, int num_segments,
+    void *workspace, size_t ws_bytes, void *out, int32_t *dev_status, dflash_stream_t stream) {
+  if (const int st =
+          attention_args_status(g, B, layer, Tq, q_rope, window, &scale, mask_mode, num_segments))
+    return st;
+  if (Tq != g->block_size) return DFLASH_ERR_INVALID_ARG;
+  if (B == 0) return DFLASH_OK;
+  if (const int st = attention_ptrs_status(B, q, q_rope, kv_pool, block_table, kv_len, out))
+    return st;
+  if (const int st =
+          block_scatter_args_status(*g, blk_k, blk_v, blk_page, blk_slot, blk_mask, kv_pool))
+    return st;
+  if (!workspace || !aligned16(workspace)) return DFLASH_ERR_INVALID_ARG;
+  const int S = num_segments > 0 ? num_segments : attention_num_segments(*g, B, Tq);
+  if (ws_bytes < attention_workspace_bytes(*g, B, Tq, S)) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_block_scatter_attention(
+      *g, B, layer, Tq, blk_k, blk_v, blk_page, blk_slot, blk_mask, q, q_rope, kv_pool,
+      block_table, kv_len, window, sinks, scale, mask_mode, S, workspace, out, dev_status,
+      reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -167,5 +167,19 @@ cudaError_t launch_block_attention(const dflash_geom &g, int B, int layer, int T
                                    const int32_t *kv_len, int32_t window, const float *sinks,
                                    float scale, int mask_mode, int S, void *ws, void *out,
                                    int32_t *st, cudaStream_t s);
+// The same with the layer's block scatter fused in (blk_k null: none);
+// Tq == g.block_size.
+cudaError_t launch_block_scatter_attention(const dflash_geom &g, int B, int layer, int Tq,
+                                           const void *blk_k, const void *blk_v,
+                                           const int32_t *blk_page, const int32_t *blk_slot,
+                                           const uint8_t *blk_mask, const void *q,
+                                           const void *q_rope, const void *pool,
+                                           const int32_t *tbl, const int32_t *kv_len,
+                                           int32_t window, const float *sinks, float scale,
+                                           int mask_mode, int S, void *ws, void *out, int32_t *st,
+                                           cudaStream_t s);
+int block_scatter_args_status(const dflash_geom &g, const void *blk_k, const void *blk_v,
+                              const int32_t *blk_page, const int32_t *blk_slot,
+                              const uint8_t *blk_mask, const void *kv_pool);
 
 }  // namespace dflash

@@ -173,6 +173,11 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy global stores before later async-proxy
+// (tensor copy) reads of the same lines.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Named barrier over `nthreads` threads that also returns the OR of `v`
 // across them (a uniform decision for every participating warp).

@@ -502,6 +502,33 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
                            dflash_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * dflash_block_scatter_attention -- dflash_block_kv_scatter followed by
+ * dflash_block_attention on the same layer, in one launch pair (main kernel
+ * + merge) instead of three: the two calls the pages run back to back for
+ * every drafter layer [TRT-20550 Description: the per-layer block scatter;
+ * VLLM-54092 Purpose 2: the split-KV block attention that reads it].
+ *
+ * Arguments: those of dflash_block_kv_scatter (blk_k, blk_v, blk_page,
+ * blk_slot, blk_mask, kv_pool) and of dflash_block_attention, with
+ * Tq == g->block_size.  The result -- the pool and `out` -- is the one the two
+ * calls give in that order, provided the placement is the bookkeeping's: the
+ * block's row i sits at the position kv_len[r] - Tq + i (dflash_step_outputs
+ * blk_page / blk_slot / blk_mask with kv_len = seq_lens), and its pool slot is
+ * read by this call at that position only (the block's pages are the
+ * request's own).  Each attention CTA writes the block rows of its own key
+ * range before it copies those keys; rows no range reads (kv_len < Tq) are
+ * still written.
+ * Errors: those of the two calls; DFLASH_ERR_INVALID_ARG also for
+ * Tq != g->block_size.
+ * ------------------------------------------------------------------- */
+DFLASH_API int dflash_block_scatter_attention(
+    const dflash_geom *g, int B, int layer, int Tq, const void *blk_k, const void *blk_v,
+    const int32_t *blk_page, const int32_t *blk_slot, const uint8_t *blk_mask, const void *q,
+    const void *q_rope, void *kv_pool, const int32_t *block_table, const int32_t *kv_len,
+    int32_t window, const float *sinks, float scale, int mask_mode, int num_segments,
+    void *workspace, size_t ws_bytes, void *out, int32_t *dev_status, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * dflash_block_attention_noalloc -- the same computation as
  * dflash_block_attention, for callers that cannot allocate device memory
  * where they run it: a plugin whose host framework owns every device buffer

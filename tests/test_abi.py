@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
               "dflash_ctx_kv_project", "dflash_ctx_kv_commit", "dflash_ctx_staged_bytes",
               "dflash_q_norm_rope", "dflash_pack_weights", "dflash_packed_kv_bytes",
               "dflash_packed_gamma_bytes", "dflash_strict_accept", "dflash_embedding_gather",
-              "dflash_ctx_kv_prefill", "dflash_ctx_prefill_workspace_bytes"):
+              "dflash_ctx_kv_prefill", "dflash_ctx_prefill_workspace_bytes",
+              "dflash_block_scatter_attention"):
         assert n in names
 
 
@@ -146,6 +147,25 @@ def test_validation_rejects_without_launching(lib):
                                        null) == _lib.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_block_kv_scatter(G, 1, 3, p, p, p, p, p, p, null,
                                        null) == _lib.DFLASH_ERR_INVALID_ARG
+
+
+def test_fused_scatter_attention_validation(lib):
+    """The fused scatter + attention call checks the block width against the
+    geometry's block_size, before the B == 0 no-op (every pointer stays null:
+    nothing can launch)."""
+    from context_kv_update_gb300 import _lib
+    g = _geom()  # block_size 4
+    G = ctypes.byref(g)
+    null = None
+
+    def call(Tq, B=1, blk_k=null, blk_v=null, page=null, slot=null, mask=null):
+        return lib.dflash_block_scatter_attention(G, B, 0, Tq, blk_k, blk_v, page, slot, mask,
+                                                  null, null, null, null, null, 0, null, 1.0, 0,
+                                                  0, null, 0, null, null, null)
+    assert call(5) == _lib.DFLASH_ERR_INVALID_ARG          # Tq != block_size
+    assert call(5, B=0) == _lib.DFLASH_ERR_INVALID_ARG     # checked before the B == 0 no-op
+    assert call(4, B=0) == _lib.DFLASH_OK
+    assert call(4) == _lib.DFLASH_ERR_INVALID_ARG          # null buffers
 
 
 def test_workspace_queries(lib):

@@ -32,10 +32,14 @@ def test_headline_bytes_per_call():
     assert nbytes == kv * 8 * 128 * 2 * 2
     # QK and PV: 2 FLOPs per multiply-add, 16 tokens x 32 heads, 128 dims each
     assert flops == 2 * 2 * kv * (16 * 32) * 128
-    assert bench.kernel_launches_per_step(g) == 1 + 4 + 5 * 3
+    # per layer the fused scatter + attention call: main kernel + merge
+    assert bench.kernel_launches_per_step(g) == 1 + 4 + 5 * 2
+    assert bench.kernel_launches_per_step(g, fused_layer=False) == 1 + 4 + 5 * 3
     # beyond 256 update rows the many-row epilogue adds its row set-up launch
-    assert bench.kernel_launches_per_step(g, B=16) == 1 + 4 + 5 * 3
-    assert bench.kernel_launches_per_step(g, B=17) == 1 + 4 + 1 + 5 * 3
+    assert bench.kernel_launches_per_step(g, B=16) == 1 + 4 + 5 * 2
+    assert bench.kernel_launches_per_step(g, B=17) == 1 + 4 + 1 + 5 * 2
+    # the block scatter: 16 rows x K, V of 8 heads x 128 dims, read and written
+    assert bench.block_scatter_bytes(prob) == 2 * 16 * 2 * 8 * 128 * 2
 
 
 def test_sliding_window_reads_only_the_window():
@@ -57,6 +61,7 @@ def test_mla_intensity():
     rows = 8 * 64
     assert flops == 2 * kv * rows * (576 + 512)
     assert round(flops / nbytes) == 967
+    assert bench.block_scatter_bytes(prob) == 2 * 8 * 576 * 2
 
 
 def test_batch_sweep_counts_every_request():
@@ -71,5 +76,6 @@ def test_launch_counts_of_the_variants():
     _, prob = _prob(workload="tiny")
     g = prob["g"]
     assert prob["hidden"].dtype == np.float32
-    assert bench.kernel_launches_per_step(g, True) == 1 + 4 + 1 + 1 * 3
-    assert bench.kernel_launches_per_step(g, True, True) == 1 + 4 + 1 + 1 + 1 * 3
+    assert bench.kernel_launches_per_step(g, True) == 1 + 4 + 1 + 1 * 2
+    assert bench.kernel_launches_per_step(g, True, True) == 1 + 4 + 1 + 1 + 1 * 2
+    assert bench.kernel_launches_per_step(g, True, True, 1, False) == 1 + 4 + 1 + 1 + 1 * 3
