@@ -151,31 +151,59 @@ __device__ __forceinline__ SegRange segment_range(const AttnParams &p, int r, in
 // segment write the same bytes) before its copies of those keys are issued.
 // Rows at positions no segment reads (kv_len < Tq) are written by the CTAs of
 // segment 0, row tile 0.  GQA: head kvh's K and V rows; MLA: the latent row.
-// Warp-wide; each lane ends with a proxy fence, so tensor copies issued after
-// a later barrier (an mbarrier the warp arrives on) read the new rows.
-// First key position this CTA must not copy before the scatter (INT_MAX: none).
-__device__ __forceinline__ int block_scatter_first_key(const AttnParams &p, const SegRange &sr) {
-  if (p.blk_k == nullptr || sr.kv_len <= 0) return 0x7fffffff;
-  const int lo = max(sr.kv_len - p.Tq, sr.k0), hi = min(sr.kv_len, sr.k1);
-  return lo < hi ? lo : 0x7fffffff;
+// Warp-wide (the producer warp, before its first copy); each lane ends with a
+// proxy fence, so tensor copies issued after the warp's next __syncwarp read
+// the new rows.  Only the kernels' scatter instantiations carry this code.
+// What the scatter reads of the call, gathered from the kernel parameters
+// (constant bank) once.  Measured: an out-of-line scatter reading the fields
+// through a reference to the parameters made the CTAs holding the block's
+// rows finish ~15 us late; passed by value, ~0.4 us slower than inline.
+struct BlockScatterArgs {
+  const uint4 *blk_k, *blk_v;
+  const int32_t *page, *slot;
+  const uint8_t *mask;
+  uint16_t *pool;
+  int32_t *st;
+  int Tq, W, nkv, NP, P, layer;
+  int lo0;  // first visible key of the block's first row (row_key_range)
+  bool gqa;
+};
+
+__device__ __forceinline__ BlockScatterArgs block_scatter_args(const AttnParams &p,
+                                                               const SegRange &sr) {
+  BlockScatterArgs a;
+  a.blk_k = p.blk_k;
+  a.blk_v = p.blk_v;
+  a.page = p.blk_page;
+  a.slot = p.blk_slot;
+  a.mask = p.blk_mask;
+  a.pool = const_cast<uint16_t *>(p.pool);
+  a.st = p.st;
+  a.Tq = p.Tq;
+  a.W = p.W;
+  a.nkv = p.nkv;
+  a.NP = p.NP;
+  a.P = p.P;
+  a.layer = p.layer;
+  int hi0 = 0;
+  a.lo0 = 0;
+  if (sr.kv_len > 0) row_key_range(p, sr.kv_len, 0, &a.lo0, &hi0);
+  a.gqa = p.kind == DFLASH_KIND_GQA;
+  return a;
 }
 
-__device__ __forceinline__ void block_scatter_rows(const AttnParams &p, int r, int kvh,
-                                                   const SegRange &sr, bool first_cta, int lane) {
+__device__ __forceinline__ void block_scatter_rows(const BlockScatterArgs a, int r, int kvh,
+                                                   const SegRange sr, bool first_cta, int lane) {
   constexpr int kBatch = 8;  // 16-byte vectors a lane has in flight
-  const int kl = sr.kv_len;
-  int lo0 = 0, hi0 = 0;
-  if (kl > 0) row_key_range(p, kl, 0, &lo0, &hi0);
-  // Most CTAs hold none of the block's rows: they skip the loop and the fence
-  // (the warp shares its issue slots with a softmax warp).
-  const bool any_covered = kl > 0 && max(kl - p.Tq, sr.k0) < min(kl, sr.k1);
-  const bool any_uncovered = first_cta && (kl <= 0 || kl - p.Tq < lo0);
+  const int kl = sr.kv_len, lo0 = a.lo0;
+  // Most CTAs hold none of the block's rows: they skip the loop and the fence.
+  const bool any_covered = kl > 0 && max(kl - a.Tq, sr.k0) < min(kl, sr.k1);
+  const bool any_uncovered = first_cta && (kl <= 0 || kl - a.Tq < lo0);
   if (!any_covered && !any_uncovered) return;
-  const bool gqa = p.kind == DFLASH_KIND_GQA;
-  const int vw = p.W / 8;               // vectors of one cache row
+  const bool gqa = a.gqa;
+  const int vw = a.W / 8;               // vectors of one cache row
   const int vrow = gqa ? 2 * vw : vw;   // vectors of one block row (GQA: K, V)
-  const int total = p.Tq * vrow;
-  uint16_t *pool = const_cast<uint16_t *>(p.pool);
+  const int total = a.Tq * vrow;
   for (int t0 = 0; t0 < total; t0 += 32 * kBatch) {
     // every load of the batch is issued before any is used
     uint4 v[kBatch];
@@ -186,33 +214,33 @@ __device__ __forceinline__ void block_scatter_rows(const AttnParams &p, int r, i
     for (int u = 0; u < kBatch; ++u) {
       const int t = t0 + 32 * u + lane;
       const int i = t / vrow, e = t - i * vrow;
-      const int pos = kl - p.Tq + i;
+      const int pos = kl - a.Tq + i;
       const bool covered = kl > 0 && pos >= lo0;
       mine[u] = t < total && (covered ? (pos >= sr.k0 && pos < sr.k1) : first_cta);
       placed[u] = 0;
       if (mine[u]) {
-        const int64_t k = static_cast<int64_t>(r) * p.Tq + i;
+        const int64_t k = static_cast<int64_t>(r) * a.Tq + i;
         const int kv = gqa && e >= vw ? 1 : 0, ee = e - kv * vw;
-        v[u] = gqa ? (kv ? p.blk_v : p.blk_k)[(k * p.nkv + kvh) * vw + ee] : p.blk_k[k * vw + ee];
-        placed[u] = p.blk_mask[k];
-        pg[u] = p.blk_page[k];
-        sl[u] = p.blk_slot[k];
+        v[u] = gqa ? (kv ? a.blk_v : a.blk_k)[(k * a.nkv + kvh) * vw + ee] : a.blk_k[k * vw + ee];
+        placed[u] = a.mask[k];
+        pg[u] = a.page[k];
+        sl[u] = a.slot[k];
       }
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       if (!placed[u]) continue;
-      if (pg[u] < 0 || pg[u] >= p.NP || sl[u] < 0 || sl[u] >= p.P) {
-        raise_status(p.st, DFLASH_DEV_BAD_PAGE);
+      if (pg[u] < 0 || pg[u] >= a.NP || sl[u] < 0 || sl[u] >= a.P) {
+        raise_status(a.st, DFLASH_DEV_BAD_PAGE);
         continue;
       }
       const int t = t0 + 32 * u + lane;
       const int e = t % vrow;
       const int kv = gqa && e >= vw ? 1 : 0, ee = e - kv * vw;
-      const size_t row = gqa ? ((((static_cast<size_t>(p.layer) * p.NP + pg[u]) * 2 + kv) * p.nkv +
-                                 kvh) * p.P + sl[u])
-                             : ((static_cast<size_t>(p.layer) * p.NP + pg[u]) * p.P + sl[u]);
-      reinterpret_cast<uint4 *>(pool + row * p.W)[ee] = v[u];
+      const size_t row = gqa ? ((((static_cast<size_t>(a.layer) * a.NP + pg[u]) * 2 + kv) * a.nkv +
+                                 kvh) * a.P + sl[u])
+                             : ((static_cast<size_t>(a.layer) * a.NP + pg[u]) * a.P + sl[u]);
+      reinterpret_cast<uint4 *>(a.pool + row * a.W)[ee] = v[u];
     }
   }
   ptx::fence_proxy_async_global();

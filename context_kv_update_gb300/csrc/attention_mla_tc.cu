@@ -39,9 +39,9 @@
 // once the previous PV has read it; each thread accumulates its key's share
 // of the row sums, reduced across the keys once at the end.
 //
-// When the call fuses the block scatter, warp 1 (after its share of the query
-// load) writes the block's own latent rows into the cache, and the producer
-// holds back the copies of those keys until it has.
+// When the call fuses the block scatter, the producer warp first writes the
+// block's own latent rows of its key range into the cache (a separate
+// instantiation, so the plain kernel carries none of that code).
 //
 // The copies of a half-tile (9 chunks x its pages) are issued by different
 // lanes at once: a TMA issue does not return before the copy engine takes
@@ -75,7 +75,7 @@ constexpr uint32_t kBufBytes = kChunks * kChunkBytes;  // one half-tile
 constexpr uint32_t kBufOff = kChunks * kQChunkBytes;
 constexpr uint32_t kPTOff = kBufOff + 2 * kBufBytes;
 constexpr uint32_t kBarOff = kPTOff + kHK * 128;  // P^T: 64 keys x 64 rows bf16
-constexpr int kNumBars = 15;
+constexpr int kNumBars = 14;
 constexpr uint32_t kXOff = (kBarOff + kNumBars * 8 + 8 + 15) & ~15u;
 constexpr uint32_t kXBytes = (2 * 64 + 64 * 4) * 4;  // m_ref[2][64], xm[64][4]
 constexpr uint32_t kSmemBytes = 1024 + kXOff + kXBytes;
@@ -121,8 +121,9 @@ __device__ __forceinline__ void half_warp_transpose_reduce32(float (&v)[32], int
   }
 }
 
+template <bool kScatter>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm, const MlaParams P) {
+    attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ MlaParams P) {
   const AttnParams &p = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -138,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *q_full = bars + 7;    //     Q in shared memory (6 warps)
   uint64_t *drain = bars + 8;     // [2] per-issuer wind-down
   uint64_t *drain_sm = bars + 10; // [4] per-softmax-warp wind-down
-  uint64_t *scat_done = bars + 14; //     block rows written (fused scatter)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   float *m_ref = reinterpret_cast<float *>(sm + kXOff);  // [2][64], log2 units
@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 4; ++w) ptx::mbar_init(ptx::smem_u32(&drain_sm[w]), 1);
     ptx::mbar_init(ptx::smem_u32(o_done), 4);
     ptx::mbar_init(ptx::smem_u32(q_full), 6);
-    ptx::mbar_init(ptx::smem_u32(scat_done), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
@@ -233,16 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(q_full));
   }
-  if (warp == 1 && p.blk_k != nullptr) {
-    // ------------------------------------------------ fused block scatter (warp 1)
-    // the block's own latent rows into the cache, before the producer copies
-    // those keys (every row group of the segment writes the same bytes)
-    block_scatter_rows(p, r, 0, sr, s == 0 && rg == 0, lane);
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(scat_done));
-  }
-  if (nh > 0 && warp == 2) {
+  if ((nh > 0 || kScatter) && warp == 2) {
     // ------------------------------------------------ TMA producer (warp 2)
+    // Fused block scatter: the producer warp first writes the block's latent
+    // rows of this CTA's key range (every row group of the segment writes the
+    // same bytes); the __syncwarp before the first copy orders every lane's
+    // stores and proxy fence before it.
+    if constexpr (kScatter)
+      block_scatter_rows(block_scatter_args(p, sr), r, 0, sr, s == 0 && rg == 0, lane);
     // half-tile h goes to buffer h & 1 once both issuers' PV of h - 2 has
     // read it; its boxes (chunk x page box) are issued by different lanes
     const int bph = kHK / P.box_rows;        // boxes per chunk of a half-tile
@@ -267,9 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nxt = fetch_page(halves_per_batch);
     int last_fill[2] = {-1, -1};
     bool ok = true;
-    // fused block scatter: the first key whose row warp 1 writes
-    const int scat_key = block_scatter_first_key(p, sr);
-    bool scat_wait = scat_key != 0x7fffffff;
     for (int h = 0; h < nh; ++h) {
       const int hb = h % halves_per_batch;
       if (hb == 0 && h > 0) {
@@ -284,15 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
         break;
-      }
-      if (scat_wait && kbase_of(h) + kHK > scat_key) {
-        scat_wait = false;
-        bool got_rows = true;
-        if (lane == 0) got_rows = ptx::mbar_wait(ptx::smem_u32(scat_done), 0u, abort_flag);
-        if (!__shfl_sync(0xffffffffu, got_rows ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
       }
       const bool skip = h == P.skip_h;
       if (lane == 0 && !skip) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full[b]), kBufBytes);
@@ -664,7 +649,8 @@ cudaError_t launch_attn_mla_tc(const AttnParams &a, const dflash_geom &g, cudaSt
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, kWidth, kWidth, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<attn_mla_tc_kernel>(227 * 1024)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_mla_tc_kernel<false>>(227 * 1024)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_mla_tc_kernel<true>>(227 * 1024)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, 1, a.B);
@@ -675,7 +661,8 @@ cudaError_t launch_attn_mla_tc(const AttnParams &a, const dflash_geom &g, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tm, P);
+  return a.blk_k != nullptr ? cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel<true>, tm, P)
+                            : cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel<false>, tm, P);
 }
 
 }  // namespace dflash

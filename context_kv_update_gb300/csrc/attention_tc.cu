@@ -25,12 +25,12 @@
 // stream), so tiles are 128 keys wide: per key that halves the QK
 // instructions and the waits and commits of a 64-key tile.
 //
-// Roles (8 warps): warp 2 issues TMA, warp 3 issues QK and owns the TMEM
-// allocation, lane 0 of warp 0 issues PV, warps 4-7 run the softmax (warp w
-// reads and writes TMEM lanes 32*(w%4)..+31, i.e. runs on SM sub-partition
-// w%4), and warp 1 writes the block's own K/V rows into the cache when the
-// call fuses the block scatter (the producer holds back the copies of those
-// keys until it has).  When the group has at most 64 query rows (the decode
+// Roles (8 warps): warp 2 issues TMA (and, when the call fuses the block
+// scatter, first writes the block's own K/V rows of its key range into the
+// cache), warp 3 issues QK and owns the TMEM allocation, lane 0 of warp 0
+// issues PV, warps 4-7 run the softmax (warp w reads and writes TMEM lanes
+// 32*(w%4)..+31, i.e. runs on SM sub-partition w%4), warp 1 only joins the
+// final barrier.  When the group has at most 64 query rows (the decode
 // case: a 16-token block times a few heads per KV head), those rows are
 // loaded twice, as MMA rows r and r + 64: the tensor core then hands all four
 // sub-partitions a copy of the scores and each softmax warp takes half of a
@@ -82,10 +82,12 @@ struct TcParams {
 };
 
 // kSplit: the split layout (a KV head's query rows fit in 64); each
-// instantiation carries only its own softmax.
-template <bool kSplit>
+// instantiation carries only its own softmax.  kScatter: the call fuses the
+// layer's block scatter (a separate instantiation: any scatter code inside
+// the plain kernel, even never run, slowed it by ~10%).
+template <bool kSplit, bool kScatter>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const TcParams P) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ TcParams P) {
   const AttnParams &p = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P.bar_off);
   uint64_t *kv_full = bars, *kv_empty = bars + nst, *s_full = bars + 2 * nst;
   uint64_t *p_full = s_full + 2, *o_done = p_full + 1, *drain = o_done + 1, *q_full = drain + 1;
-  uint64_t *s_free = q_full + 1, *drain_pv = s_free + 2, *scat_done = drain_pv + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(scat_done + 1);
+  uint64_t *s_free = q_full + 1, *drain_pv = s_free + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain_pv + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *consumed = reinterpret_cast<volatile int *>(tslot + 2);
 
@@ -122,7 +124,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     ptx::mbar_init(ptx::smem_u32(drain), 1);
     ptx::mbar_init(ptx::smem_u32(drain_pv), 1);
     ptx::mbar_init(ptx::smem_u32(q_full), 4u);  // one arrival per softmax warp
-    ptx::mbar_init(ptx::smem_u32(scat_done), 1u);
     *abort_flag = 0;
     *consumed = 0;
     ptx::fence_mbar_init();
@@ -224,8 +225,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   const int boxes = kKT / P.box_rows;
 
-  if (ntiles > 0 && warp == 2) {
+  if ((ntiles > 0 || kScatter) && warp == 2) {
     // ------------------------------------------------ TMA producer (warp 2)
+    // Fused block scatter: the producer warp first writes the block rows of
+    // this CTA's key range (their tiles are the segment's last, so only that
+    // CTA's copies wait for it); the __syncwarp before the first copy orders
+    // every lane's stores and proxy fence before it.  No warp barrier of its
+    // own: one placed ahead of the role branches slowed the kernel by ~10%
+    // even where it did nothing.
+    if constexpr (kScatter)
+      block_scatter_rows(block_scatter_args(p, sr), r, kvh, sr, s == 0 && rt == 0, lane);
     // The page ids of the segment are fetched warp-wide, one batch of 32
     // (tile, box) lookups ahead, so no table read sits between two TMA issues.
     const int tiles_per_batch = 32 / boxes;
@@ -255,9 +264,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     int nxt = fetch_page(tiles_per_batch);
     int issued = 0;
     bool ok = true;
-    // fused block scatter: the first key whose rows warp 1 writes
-    const int scat_key = block_scatter_first_key(p, sr);
-    bool scat_wait = scat_key != 0x7fffffff;
     for (int t = 0; t < ntiles; ++t) {
       const int tb = t % tiles_per_batch;
       if (tb == 0 && t > 0) {
@@ -272,15 +278,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
         ok = false;
         break;
-      }
-      if (scat_wait && (sr.t0 + t + 1) * kKT > scat_key) {
-        scat_wait = false;
-        bool got_rows = true;
-        if (lane == 0) got_rows = ptx::mbar_wait(ptx::smem_u32(scat_done), 0u, abort_flag);
-        if (!__shfl_sync(0xffffffffu, got_rows ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
       }
       const bool skip = t == P.skip_tile;
       if (lane == 0 && !skip)
@@ -377,11 +374,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::mbar_wait(ptx::smem_u32(drain_pv), 0u, &dummy);
       }
     }
-  } else if (warp == 1 && p.blk_k != nullptr) {
-    // ------------------------------------------------ fused block scatter (warp 1)
-    block_scatter_rows(p, r, kvh, sr, s == 0 && rt == 0, lane);
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(scat_done));
   } else if (warp >= 4 && kSplit) {
     // ------------------------------------------------ softmax, split layout
     // Warp pair (q4, q4 ^ 2) shares query rows 32*(q4&1)..+31: warp q4 < 2
@@ -729,11 +721,11 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   P.k_bytes = P.chunks * kVChunk;
   P.stage_bytes = 2 * P.k_bytes;
   const uint32_t x_bytes = 320 * 4;  // split-layout row maxima and row sums
-  const uint32_t bar_bytes = 8 * 8 * 2 + 11 * 8 + 16;
+  const uint32_t bar_bytes = 8 * 8 * 2 + 10 * 8 + 16;
   P.nst = std::max(2, std::min<int>(8, static_cast<int>((kSmemMax - 1024 - bar_bytes - x_bytes) /
                                                           P.stage_bytes)));
   P.bar_off = P.nst * P.stage_bytes;
-  P.x_off = (P.bar_off + (2 * P.nst + 11) * 8 + 16 + 15) & ~15u;
+  P.x_off = (P.bar_off + (2 * P.nst + 10) * 8 + 16 + 15) & ~15u;
   const uint32_t smem = 1024 + P.x_off + x_bytes;
   P.idesc_qk = ptx::idesc_bf16_f32(kRows, kKT, false);
   P.idesc_pv = ptx::idesc_bf16_f32(kRows, hd, true);
@@ -746,8 +738,13 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
                         static_cast<uint64_t>(g.page_size);
   cudaError_t e = make_tmap_bf16_2d(&tm, a.pool, rows, hd, hd, P.box_rows, 64);
   if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<attn_tc_kernel<true>>(kSmemMax)) != cudaSuccess) return e;
-  if ((e = ensure_smem_limit<attn_tc_kernel<false>>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<true, false>>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<false, false>>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<true, true>>(kSmemMax)) != cudaSuccess) return e;
+  if ((e = ensure_smem_limit<attn_tc_kernel<false, true>>(kSmemMax)) != cudaSuccess) return e;
+  const bool scat = a.blk_k != nullptr;
+  auto kern = P.split ? (scat ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
+                      : (scat ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(a.S * P.RT, a.nkv, a.B);
@@ -758,8 +755,7 @@ cudaError_t launch_attn_tc(const AttnParams &a, const dflash_geom &g, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return P.split ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tm, P)
-                 : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tm, P);
+  return cudaLaunchKernelEx(&cfg, kern, tm, P);
 }
 
 }  // namespace dflash
