@@ -646,7 +646,7 @@ def run_kernel_only(args):
     dl.load()
     _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=0)
-    step = Step(dl, prob)
+    step = Step(dl, prob, fused_layer=args.layer_calls == "fused")
     step.run()
     torch.cuda.synchronize()
     o = step.outs
@@ -665,11 +665,9 @@ def run_kernel_only(args):
         if args.kernel == "q_rope":
             dl.dflash_q_norm_rope(step.geom, qrows, gamma_q, q_pos, q_out, step.status)
         elif args.kernel == "attention":
-            dl.dflash_block_attention(step.geom, layer, step.q[layer], step.pool, o["block_table"],
-                                      o["seq_lens"], step.attn_out[layer], ws,
-                                      q_rope=None if step.q_rope is None else step.q_rope[layer],
-                                      window=prob["window"], sinks=step.sinks, scale=step.scale,
-                                      num_segments=args.segments, dev_status=step.status)
+            # the step's attention call: fused with the block scatter unless
+            # --layer-calls separate
+            step.attention_call(layer, num_segments=args.segments, ws=ws)
         else:
             step.ctx_len.copy_(step.ctx_pre)
             dl.dflash_ctx_kv_update(step.geom, step.hidden, step.n_acc, step.ctx_len,
