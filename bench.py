@@ -86,6 +86,42 @@ def attention_work(prob):
     return nbytes, flops, int(kv.max())
 
 
+def fused_layer_pays(prob, num_segments, sm_count) -> bool:
+    """The caller's choice between the fused scatter + attention call and the
+    two calls, from what a serving host knows (context lengths, geometry).
+    The fused call delays the first copies of the CTAs whose segment holds
+    the block's rows by the scatter's memory round trips: hidden when the grid
+    is one wave and each such segment is at least 3 tiles shorter than the
+    longest; otherwise those CTAs set the call's time (measured: 2K context
+    +3.9 us per call, the 4- and 64-request batch sweeps +4.7 and +17 us).
+    The MLA kernel is left out: fused, its 32K step measured 266.3 against
+    266.8 us while each call took 1.2-1.8 us longer."""
+    g = prob["g"]
+    T, B, S = g["T"], prob["B"], num_segments
+    gqa = g["kind"] == "gqa"
+    if not gqa:
+        return False
+    heads = g["nkv"] if gqa else 1
+    rows = T * g["hq"] // heads
+    row_tiles = -(-rows // (128 if gqa else 64))
+    if B * heads * row_tiles * S > sm_count:
+        return False
+    A = np.asarray(prob["alloc_limit"], np.int64)
+    kv = np.minimum(np.asarray(prob["ctx_len"], np.int64) + np.asarray(prob["n_acc"], np.int64),
+                    A) + T
+    w = int(prob["window"])
+    for k in kv.tolist():
+        lo = max(0, k - T - w + 1) if w > 0 else 0
+        t_lo, t_hi = lo // 128, -(-k // 128)
+        ntiles = t_hi - t_lo
+        per = -(-ntiles // S)
+        for pos in (k - T, k - 1):  # the segments holding the block's first and last rows
+            seg = (max(pos, lo) // 128 - t_lo) // per
+            if min(per, ntiles - seg * per) > per - 3:
+                return False
+    return True
+
+
 def block_scatter_bytes(prob):
     """Algorithmic bytes of one layer's block scatter: every block row read
     and written once (GQA: K and V of every KV head; MLA: the latent row)."""
@@ -93,10 +129,11 @@ def block_scatter_bytes(prob):
     row = (2 * g["nkv"] * g["hd"] if g["kind"] == "gqa" else g["latent"] + g["rope_dim"]) * 2
     return 2 * prob["B"] * g["T"] * row
 
-# DRAM traffic (read + write) of one attention call (main kernel + merge) from
-# the committed ncu capture, keyed by
-# the hash of the attention sources it was taken on (None = not captured).
-ATTN_TRAFFIC = {"sources_sha": "5e5314bc14151b3d", "bytes_per_launch": 142508032,
+# DRAM traffic (read + write) of one attention call of the headline step (the
+# fused scatter + attention: main kernel + merge) from the committed ncu
+# capture, keyed by the hash of the attention sources it was taken on (None =
+# not captured).
+ATTN_TRAFFIC = {"sources_sha": "9aec866e9922ddf8", "bytes_per_launch": 142834176,
                 "profile": "profiles/attention_qwen3_8b_32k.md"}
 
 
@@ -391,8 +428,8 @@ def run_ours(args, rank, world):
     _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=rank)
     g = prob["g"]
-    step = Step(dl, prob, split_update=args.split_update,
-                fused_layer=args.layer_calls == "fused")
+    fused = resolve_layer_calls(args, dl, prob)
+    step = Step(dl, prob, split_update=args.split_update, fused_layer=fused)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -480,6 +517,7 @@ def run_ours(args, rank, world):
     e2e = run_e2e(dl, step, stream, min(args.steps, 200))
     st = int(step.status.item())
     return dict(ms_step=ms_step, attn_ms=attn_ms, attn_ss_ms=attn_ss_ms, floor_ms=floor_ms,
+                fused=step.fused_layer,
                 clocks=clocks, e2e=e2e, prob=prob, status=st, warmup_done=w)
 
 
@@ -636,6 +674,16 @@ def run_e2e(dl, step, stream, steps):
             "pair_outputs_equal": same}
 
 
+def resolve_layer_calls(args, dl, prob) -> bool:
+    """--layer-calls: fused, separate, or auto (fused where fused_layer_pays)."""
+    import torch
+    if args.layer_calls != "auto":
+        return args.layer_calls == "fused"
+    g = prob["g"]
+    S = dl.dflash_attention_num_segments(dl.make_geom(g), prob["B"], g["T"])
+    return fused_layer_pays(prob, S, torch.cuda.get_device_properties(0).multi_processor_count)
+
+
 def run_kernel_only(args):
     """One call of the step, launched eagerly `steps` times after `warmup`
     launches, on the benchmark workload (used under ncu; prints its mean)."""
@@ -646,7 +694,7 @@ def run_kernel_only(args):
     dl.load()
     _, cfg = workload_config(args)
     prob = inputs.make_problem(cfg, seed=0)
-    step = Step(dl, prob, fused_layer=args.layer_calls == "fused")
+    step = Step(dl, prob, fused_layer=resolve_layer_calls(args, dl, prob))
     step.run()
     torch.cuda.synchronize()
     o = step.outs
@@ -953,9 +1001,10 @@ def main():
                     help="override the workload's sliding window (0 = full range)")
     ap.add_argument("--rows", type=int, default=8192,
                     help="prompt rows of the prefill workloads (prefill_mla, prefill_qwen3_8b)")
-    ap.add_argument("--layer-calls", choices=("fused", "separate"), default="fused",
-                    help="per layer: the block scatter fused into the attention call "
-                         "(default) or the scatter and attention calls one after the other")
+    ap.add_argument("--layer-calls", choices=("auto", "fused", "separate"), default="auto",
+                    help="per layer: the block scatter fused into the attention call, the "
+                         "scatter and attention calls one after the other, or auto (fused "
+                         "where its scatter stays off the critical path: fused_layer_pays)")
     ap.add_argument("--split-update", action="store_true",
                     help="run the context update as project (on an auxiliary stream, beside "
                          "the bookkeeping) + commit instead of the fused call")
@@ -989,7 +1038,7 @@ def main():
     tag, _ = workload_config(args)
     headline = tag == WORKLOAD_TAG
     attn_bytes, attn_flops, kv_len = attention_work(prob)
-    fused = args.layer_calls == "fused"
+    fused = res["fused"]
     if fused:
         attn_bytes += block_scatter_bytes(prob)
     peaks = measured_peaks()
@@ -1010,7 +1059,7 @@ def main():
     else:
         achieved = attn_bytes / attn_s / 1e9
         traffic = None
-        if headline and ATTN_TRAFFIC["sources_sha"] == attention_sources_sha():
+        if headline and fused and ATTN_TRAFFIC["sources_sha"] == attention_sources_sha():
             traffic = ATTN_TRAFFIC["bytes_per_launch"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),

@@ -42,6 +42,27 @@ def test_headline_bytes_per_call():
     assert bench.block_scatter_bytes(prob) == 2 * 16 * 2 * 8 * 128 * 2
 
 
+def test_fused_layer_rule():
+    """The caller-side choice of the fused scatter + attention call: the 32K
+    headline (one wave of 152 CTAs, the block in a 5-tile tail segment of
+    14-tile segments) fuses; a 2K context (one-tile segments), the batch
+    sweeps past one wave and the MLA drafter do not."""
+    _, prob = _prob()
+    assert bench.fused_layer_pays(prob, 19, 152)
+    assert not bench.fused_layer_pays(prob, 19, 100)  # more CTAs than SMs
+    _, p2k = _prob(ctx=2048)
+    assert not bench.fused_layer_pays(p2k, 19, 152)
+    _, pb4 = _prob(workload="batch_sweep_4")
+    assert not bench.fused_layer_pays(pb4, 7, 152)
+    _, pm = _prob(workload="mla", ctx=32768)
+    assert not bench.fused_layer_pays(pm, 19, 152)
+    # a block in a full-length segment: kv_len = 34040 fills 266 = 19 x 14
+    # tiles, so the block's rows land in the last of 19 equal segments
+    prob_full = dict(prob, ctx_len=np.array([34040 - 1 - 16], np.int32),
+                     n_acc=np.array([1], np.int32), alloc_limit=np.array([1 << 20], np.int32))
+    assert not bench.fused_layer_pays(prob_full, 19, 152)
+
+
 def test_sliding_window_reads_only_the_window():
     _, prob = _prob(workload="sliding_window")
     nbytes, _, _ = bench.attention_work(prob)
