@@ -12,9 +12,8 @@
 // exists on every GPU that loads this library, for the life of the process.
 // Every call shares it and it keeps the last call's contents; nothing in it
 // needs clearing between calls (each call writes every partial it later
-// reads).  Calls whose GPU work overlaps -- on different streams, or on the
-// same stream through a graph branch -- race on it and must be serialised by
-// the caller.
+// reads).  Calls whose GPU work overlaps (on different streams, for example)
+// race on it and must be serialised by the caller.
 #include <mutex>
 
 #include "attention_common.cuh"

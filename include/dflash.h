@@ -544,7 +544,7 @@ DFLASH_API int dflash_block_scatter_attention(
  * dflash_attention_workspace_bytes(g, B, Tq, num_segments) exceeds it returns
  * DFLASH_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The array is shared by
  * every call and keeps the last call's contents; nothing in it has to start
- * at zero.  Calls whose GPU work overlaps (other streams, graph branches) race
+ * at zero.  Calls whose GPU work overlaps (on other streams, for example) race
  * on it: serialise them.
  * Set-up: the first call on each device looks up the array's device address
  * (with that device current) and caches it.  The call allocates nothing and
