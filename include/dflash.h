@@ -517,7 +517,10 @@ DFLASH_API int dflash_block_attention(const dflash_geom *g, int B, int layer, in
  * read by this call at that position only (the block's pages are the
  * request's own).  Each attention CTA writes the block rows of its own key
  * range before it copies those keys; rows no range reads (kv_len < Tq) are
- * still written.
+ * still written.  Those CTAs start copying later by the scatter's memory
+ * round trips: the fused form is faster where their segment is shorter than
+ * the others and the grid is one wave (a long context, few requests); with
+ * one-tile segments or several waves the two calls are faster.
  * Errors: those of the two calls; DFLASH_ERR_INVALID_ARG also for
  * Tq != g->block_size.
  * ------------------------------------------------------------------- */
